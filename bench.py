@@ -1,0 +1,422 @@
+"""Decode-attention benchmark: µs per decode step, KV-read GB/s and the HBM
+roofline fraction on the 100K-token long-context batch.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--partition-size P]
+
+Prints ONE JSON line.  The default workload is the long-context decode step
+(1 sequence x 100000 tokens, 24 query / 4 KV heads, head_dim 256, bf16 KV
+cache, 16-token blocks, PARTITION_SIZE 512).  A step is one full pa_decode
+call (V2: partition kernel + log-sum-exp reduce) over inputs already resident
+in HBM; the L2 is flushed (256 MiB write) before every timed step, and the
+KV cache (409.6 MB) is larger than L2 as well.
+
+`--impl reference` times the float64 CPU oracle on the host cores instead
+(the reference arm): each step computes a bounded sample of the step's
+query-head rows, scaled to a full step.
+
+Multi-GPU (`torchrun --nproc-per-node N bench.py --gpus N`): every rank runs
+its own replica of the batch on its own GPU (the decode step has no
+cross-GPU exchange), timing is max over ranks, and kv_read_gbs is the sum of
+all ranks' bytes over that time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import paged_attention_decode_v2_gb300 as pa  # noqa: E402
+from paged_attention_decode_v2_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "decode-attention µs/step and KV-read GB/s (% of HBM peak) at 100K context"
+UNIT = "us/step"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+
+# DRAM bytes (read + write) per launch of the dominant kernel, from one ncu
+# capture, keyed by a hash of the kernel sources it was taken on.  A source
+# change makes the figure stale, and the bench then reports null.
+NCU_TRAFFIC = {}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "paged_attention_decode_v2_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(os.path.basename(f).encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.marks = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, name):
+        self.marks.append((name, time.time()))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ts, line in self.lines:
+            if not (t0 <= ts <= t1):
+                continue
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gpu_id_for_smi(device) -> str:
+    """nvidia-smi's id for this device (its UUID when torch knows it)."""
+    try:
+        u = str(torch.cuda.get_device_properties(device).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return str(device.index or 0)
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def run_ours(args, rank, world, device):
+    w = wl.WORKLOADS[args.workload]
+    P = args.partition_size or w.partition_sizes[0]
+    batch = wl.make(w, device=device)
+    params = pa.make_params(batch.q, batch.k_cache, batch.block_tables,
+                            max_seq_len=batch.max_seq_len, scale=batch.scale, partition_size=P,
+                            out_dtype=torch.float32)
+    path = pa.decode_path(params)
+    ws = pa.alloc_workspace(params, device=device)
+    out = torch.empty(tuple(batch.q.shape), dtype=torch.float32, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    kw = dict(max_seq_len=batch.max_seq_len, scale=batch.scale, partition_size=P)
+
+    def step():
+        pa.decode(batch.q, batch.k_cache, batch.v_cache, batch.block_tables, batch.seq_lens, out,
+                  ws, **kw)
+
+    kv_bytes = batch.kv_bytes()
+    alg_bytes = kv_bytes + batch.q_bytes()
+    launches_per_step = 2 if path == 2 else 1
+
+    sampler = ClockSampler(gpu_id_for_smi(device))
+    if rank == 0:
+        sampler.start()
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(device)
+
+    # ---- timed region: K full steps, events around each step ----------------
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(device)
+    t_start = time.time()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(device)
+    if world > 1:
+        torch.distributed.barrier()
+    t_end = time.time()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+
+    # ---- the dominant kernel alone (V2 pass 1), same region shape -----------
+    dom_ms = []
+    if path == 2:
+        evp = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.zero_()
+            evp[i][0].record(stream)
+            pa.decode_v2_partitions(batch.q, batch.k_cache, batch.v_cache, batch.block_tables,
+                                    batch.seq_lens, ws, out_dtype=torch.float32, **kw)
+            evp[i][1].record(stream)
+            pa.decode_v2_reduce(params, batch.seq_lens, ws, out)
+        torch.cuda.synchronize(device)
+        dom_ms = [a.elapsed_time(b) for a, b in evp]
+    else:
+        dom_ms = step_ms
+    t_dom_end = time.time()
+
+    # ---- end to end through the public API with host buffers ---------------
+    q_h = batch.q.cpu().pin_memory()
+    bt_h = batch.block_tables.cpu().pin_memory()
+    sl_h = batch.seq_lens.cpu().pin_memory()
+    out_h = torch.empty(tuple(out.shape), dtype=out.dtype).pin_memory()
+    q_d = torch.empty_like(batch.q)
+    bt_d = torch.empty_like(batch.block_tables)
+    sl_d = torch.empty_like(batch.seq_lens)
+    e2e_s = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        torch.cuda.synchronize(device)
+        t0 = time.perf_counter()
+        q_d.copy_(q_h, non_blocking=True)
+        bt_d.copy_(bt_h, non_blocking=True)
+        sl_d.copy_(sl_h, non_blocking=True)
+        pa.decode(q_d, batch.k_cache, batch.v_cache, bt_d, sl_d, out, ws, **kw)
+        out_h.copy_(out, non_blocking=True)
+        torch.cuda.synchronize(device)
+        if i >= args.warmup:
+            e2e_s.append(time.perf_counter() - t0)
+    h2d = q_h.numel() * q_h.element_size() + bt_h.numel() * 4 + sl_h.numel() * 4
+    d2h = out_h.numel() * out_h.element_size()
+    if rank == 0:
+        sampler.stop()
+
+    assert pa.read_device_status(ws) == pa.PA_OK, "device status not OK after the bench"
+    assert torch.isfinite(out).all().item(), "non-finite output"
+
+    # reduce over ranks: max of times
+    t_step = statistics.mean(step_ms)
+    t_dom = statistics.mean(dom_ms)
+    t_e2e = statistics.mean(e2e_s) * 1e3
+    if world > 1:
+        tt = torch.tensor([t_step, t_dom, t_e2e], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        t_step, t_dom, t_e2e = tt.tolist()
+
+    peak, peak_kind = measured_hbm_peak()
+    achieved = alg_bytes / (t_dom * 1e-3) / 1e9
+    traffic = NCU_TRAFFIC.get((kernel_source_hash(), args.workload, P))
+    result = {
+        "metric": METRIC,
+        "value": round(t_step * 1e3, 3),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(t_step, 6),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == torch.bfloat16 else str(w.dtype).replace("torch.", ""),
+        "data": "synthetic (seeded N(0,1) q/k/v, 0.1% of keys x30, random block table)",
+        "config": {
+            "workload": f"{w.name}: {w.num_seqs} seq x {batch.max_seq_len} tokens, "
+                        f"{w.num_heads} q / {w.num_kv_heads} kv heads, head_dim {w.head_dim}, "
+                        f"{str(w.dtype).replace('torch.', '')} KV, block {w.block_size}",
+            "partition_size": P,
+            "path": "V2 (partition kernel + LSE reduce)" if path == 2 else "V1 single pass",
+            "accumulate": "f32",
+            "l2": "flushed before every timed step (256 MiB write); KV working set "
+                  f"{kv_bytes / 1e6:.1f} MB > 129 MB L2",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "kv_read_gbs": round(world * alg_bytes / (t_step * 1e-3) / 1e9, 1),
+        "hbm_frac_of_step": round(alg_bytes / (t_step * 1e-3) / 1e9 / peak, 4),
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "pa_generic_kernel (V2 pass 1)" if path == 2 else "pa_generic_kernel (V1)",
+            "achieved": round(achieved, 1),
+            "peak": peak,
+            "peak_source": f"{peak_kind} hbm_gbs (copy)",
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": traffic,
+            "algorithmic_bytes_per_launch": alg_bytes,
+            "launch_us": round(t_dom * 1e3, 3),
+        },
+        "e2e": {"value": round(t_e2e * 1e3, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+    }
+    if rank == 0:
+        result["clocks"] = sampler.summary(t_start, t_end)
+        if world == 1 and not args.no_cpu_baseline:
+            result["cpu_baseline"] = cpu_baseline(batch, args.cpu_rows)
+    return result
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores (cpu_baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+def _oracle_rows(batch_cpu, rows):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.decode(batch_cpu.q, batch_cpu.k_cache, batch_cpu.v_cache, batch_cpu.block_tables,
+                  batch_cpu.seq_lens, batch_cpu.scale, rows=rows)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(batch, nrows):
+    import oracle
+    bc = batch.to("cpu")
+    w = bc.workload
+    total_rows = w.num_seqs * w.num_heads
+    rows = list(range(min(nrows, total_rows)))
+    dt = _oracle_rows(bc, rows)
+    per_step_us = dt * 1e6 * total_rows / len(rows)
+    return {"value": round(per_step_us, 1), "unit": UNIT, "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": f"{len(rows)} of {total_rows} query-head rows of one step "
+                      f"({dt:.1f} s), scaled to the full step"}
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the float64 oracle, as it stands, on the host cores.
+    Each step computes one query-head row over at most --ref-tokens of its
+    tokens (rows taken in turn); the time is scaled by the step's total
+    (row x token) work over the sample's."""
+    if rank != 0:
+        return None
+    import dataclasses
+    import oracle
+    w = wl.WORKLOADS[args.workload]
+    P = args.partition_size or w.partition_sizes[0]
+    bc = wl.make(w, device="cpu")
+    T = max(1, args.ref_tokens)
+    sample = dataclasses.replace(bc, seq_lens=bc.seq_lens.clamp(max=T))
+    lens = bc.seq_lens.tolist()
+    total_rows = w.num_seqs * w.num_heads
+    total_work = sum(lens) * w.num_heads
+    times = []
+    for i in range(args.warmup + args.steps):
+        row = (i * 7) % total_rows
+        work = min(lens[row // w.num_heads], T)
+        dt = _oracle_rows(sample, [row])
+        if i >= args.warmup and work > 0:
+            times.append(dt * total_work / work)
+    t = statistics.mean(times)
+    v = round(t * 1e6, 1)
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "partition_size": P},
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"per step one of {total_rows} query-head rows over at most "
+                                   f"{T} tokens, scaled to the step's full row x token work"},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="long_100k", choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--partition-size", type=int, default=0)
+    ap.add_argument("--cpu-rows", type=int, default=24,
+                    help="query-head rows the CPU baseline computes")
+    ap.add_argument("--ref-tokens", type=int, default=4096,
+                    help="tokens of one query-head row per reference-arm step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus:
+        if world == 1 and args.gpus > 1:
+            ap.error("--gpus N > 1 needs torchrun --nproc-per-node N")
+    if args.impl == "reference":
+        if world > 1:
+            torch.distributed.init_process_group("gloo")
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    from paged_attention_decode_v2_gb300 import build
+    if rank == 0 or world == 1:
+        build.build()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=device)
+        torch.distributed.barrier()
+        if rank != 0:
+            build.build()
+    res = run_ours(args, rank, world, device)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,203 @@
+/*
+ * pa.h -- C ABI of libpa: single-token decode attention over a paged KV
+ * cache on one GB300 (sm_103a).
+ *
+ * What the library computes.  For every sequence b < num_seqs and query head
+ * h < num_heads, with G = num_heads / num_kv_heads, kvh = h / G and
+ * L = seq_lens[b]:
+ *
+ *   l_t      = scale * dot(q[b,h,:], K[blk(t), kvh, t % block_size, :]),
+ *              blk(t) = block_tables[b * max_blocks_per_seq + t / block_size]
+ *   out[b,h] = sum_t exp(l_t - max l) V[blk(t), kvh, t % block_size, :]
+ *              / sum_t exp(l_t - max l)                       (t < L)
+ *
+ * Sources (commit pages of the project "project_6"):
+ *   - the paged cache and its block table, and the [blocks, kv_heads,
+ *     block_size, head_dim] layout both caches use: commit 4eb83a7e
+ *     "qwen3_6_scripts", paragraph "Hardware testing confirmed";
+ *   - the V2 split-KV scheme (per-partition QK^T, softmax and weighted V sum
+ *     into tmp_output / exp_sums / max_logits, then a cross-partition
+ *     log-sum-exp reduction): same page, paragraph "Implementation
+ *     (paged_attention_v2_pytorch.py)", and commit 1a4e1005 "paged_attn.py",
+ *     paragraph "Architecture follows CCCL's two-pass dispatch";
+ *   - the V1 single pass and the 8192-token dispatch threshold: commit
+ *     1a4e1005 "paged_attn.py", change 1 "Restore V1/V2 adaptive dispatch",
+ *     and commit 4eb83a7e "qwen3_6_scripts", paragraph "forward_decode: V2
+ *     enabled via original heuristic";
+ *   - the preallocated V2 workspace: commit 1a4e1005 "paged_attn.py",
+ *     change 2 "Pre-allocate V2 intermediate tensors".
+ *
+ * Conventions shared by every entry point:
+ *   - Every tensor pointer is a DEVICE pointer, owned by the caller, valid
+ *     for the whole asynchronous execution of the call.  The library never
+ *     allocates, frees, synchronises or logs (pa_read_device_status is the
+ *     one call that waits on the stream, and it says so).
+ *   - All work is enqueued on `stream` and returns before it runs.  The
+ *     decode calls make no allocation and no host synchronisation.
+ *   - Host-side checks run before anything is enqueued; a failing check
+ *     returns its status and enqueues nothing.
+ *   - q, k_cache, v_cache and out must be 16-byte aligned; block_tables and
+ *     seq_lens 4-byte aligned; the workspace 256-byte aligned.
+ *   - The caller promises 0 <= seq_lens[b] <= max_seq_len and valid block ids
+ *     for every token t < seq_lens[b].  A violation is caught on the device:
+ *     the offending output row is written as NaN, no out-of-range memory is
+ *     touched, and (for calls given a workspace) the status word records it.
+ *   - A sequence of length 0 gets an all-zero output row.
+ *   - The library keeps no per-call state; calls are thread-safe.
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pa_status {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1,         /* null pointer, bad shape or size          */
+  PA_ERR_UNSUPPORTED = 2,         /* valid but not built: dtype, head_dim ... */
+  PA_ERR_MISALIGNED = 3,          /* pointer alignment rule broken            */
+  PA_ERR_WORKSPACE_TOO_SMALL = 4, /* workspace_bytes < pa_workspace_size()    */
+  PA_ERR_CUDA = 5,                /* a CUDA launch or copy failed             */
+  PA_ERR_DEVICE_TIMEOUT = 6,      /* device status: a bounded wait gave up    */
+  PA_ERR_BAD_BLOCK_ID = 7,        /* device status: block id outside the pool */
+  PA_ERR_BAD_SEQ_LEN = 8          /* device status: seq_len outside 0..max    */
+} pa_status_t;
+
+typedef enum pa_dtype { PA_F32 = 0, PA_BF16 = 1, PA_F16 = 2 } pa_dtype_t;
+
+/* Flags (pa_params_t.flags). */
+#define PA_FLAG_PORTABLE 1 /* use the CUDA-core kernels even where the
+                              TMA / tensor-core kernels apply              */
+
+typedef struct pa_params {
+  int32_t num_seqs;           /* B >= 0                                      */
+  int32_t num_heads;          /* Hq >= 1                                     */
+  int32_t num_kv_heads;       /* Hkv >= 1, divides Hq                        */
+  int32_t head_dim;           /* D: 64, 128 or 256                           */
+  int32_t block_size;         /* BS >= 1 tokens per physical block           */
+  int32_t num_blocks;         /* NB >= 1: blocks in each cache pool          */
+  int32_t max_blocks_per_seq; /* MB: row length of block_tables              */
+  int32_t max_seq_len;        /* host-known upper bound of seq_lens, <= MB*BS */
+  int32_t partition_size;     /* P: V2 tokens per partition, multiple of BS  */
+  int32_t v1_max_seq_len;     /* pa_decode threshold, <= 0 means 8192        */
+  pa_dtype_t kv_dtype;        /* element type of q, k_cache and v_cache      */
+  pa_dtype_t out_dtype;       /* PA_F32, or the same type as kv_dtype        */
+  float scale;                /* logit scale, usually 1/sqrt(head_dim)       */
+  int32_t flags;              /* PA_FLAG_* bits, 0 by default                */
+} pa_params_t;
+
+/*
+ * Tensor layouts (row-major, element type in brackets):
+ *   q            [kv_dtype] [num_seqs, num_heads, head_dim]
+ *   k_cache      [kv_dtype] [num_blocks, num_kv_heads, block_size, head_dim]
+ *   v_cache      [kv_dtype] [num_blocks, num_kv_heads, block_size, head_dim]
+ *   block_tables [int32]    [num_seqs, max_blocks_per_seq]
+ *   seq_lens     [int32]    [num_seqs]
+ *   out          [out_dtype][num_seqs, num_heads, head_dim]
+ *
+ * Workspace (V2 only), NP = ceil(max_seq_len / partition_size), each region
+ * starting on a 256-byte boundary, in this order:
+ *   status       int32 word at offset 0 (then padding to 256 bytes)
+ *   max_logits   float32 [num_seqs, num_heads, NP]   m_p, natural-log units
+ *   exp_sums     float32 [num_seqs, num_heads, NP]   s_p = sum exp(l_t - m_p)
+ *   tmp_output   float32 [num_seqs, num_heads, NP, head_dim]
+ *                o_p = sum exp(l_t - m_p) V_t / s_p
+ * Only partitions p < ceil(seq_lens[b] / P) are written or read; the rest
+ * may hold anything.
+ */
+
+/* Bytes of workspace pa_decode_v2 / pa_decode need for these parameters
+ * (0 if the parameters are invalid).  Depends only on num_seqs, num_heads,
+ * head_dim, max_seq_len and partition_size. */
+PA_API size_t pa_workspace_size(const pa_params_t* params);
+
+/*
+ * V1: one pass per (sequence, KV head) over the whole sequence, normalised
+ * straight into `out`.  No workspace.
+ * Source: commit 1a4e1005 "paged_attn.py", change 1 (V1 single-CTA
+ * iteration); commit 4eb83a7e "qwen3_6_scripts", paragraph "V1
+ * paged_attention (decode <= 8192)".
+ */
+PA_API pa_status_t pa_decode_v1(const pa_params_t* params, const void* q, const void* k_cache,
+                         const void* v_cache, const int32_t* block_tables,
+                         const int32_t* seq_lens, void* out, cudaStream_t stream);
+
+/*
+ * V2: split-KV in two kernels.  Pass 1 runs one CTA per (sequence, KV-head
+ * group, partition of partition_size tokens) and writes max_logits,
+ * exp_sums and tmp_output into the workspace; pass 2 combines a row's
+ * partitions with weights exp(m_p - max_p m_p) * s_p and writes `out`.
+ * `workspace` must hold pa_workspace_size(params) bytes.
+ * Source: commit 4eb83a7e "qwen3_6_scripts", paragraph "Implementation
+ * (paged_attention_v2_pytorch.py)", Phase 1 and Phase 2.
+ */
+PA_API pa_status_t pa_decode_v2(const pa_params_t* params, const void* q, const void* k_cache,
+                         const void* v_cache, const int32_t* block_tables,
+                         const int32_t* seq_lens, void* workspace, size_t workspace_bytes,
+                         void* out, cudaStream_t stream);
+
+/*
+ * The two kernels of pa_decode_v2 as separate calls, for callers that want
+ * to schedule or time them apart.  pa_decode_v2_partitions enqueues pass 1
+ * (writes the workspace); pa_decode_v2_reduce enqueues pass 2 (reads the
+ * workspace, writes `out`) and must follow pass 1 on the same stream with
+ * the same arguments.  pa_decode_v2 is exactly the two in sequence, with
+ * pass 2 launched as a programmatic dependent of pass 1.
+ */
+PA_API pa_status_t pa_decode_v2_partitions(const pa_params_t* params, const void* q,
+                                           const void* k_cache, const void* v_cache,
+                                           const int32_t* block_tables, const int32_t* seq_lens,
+                                           void* workspace, size_t workspace_bytes,
+                                           cudaStream_t stream);
+PA_API pa_status_t pa_decode_v2_reduce(const pa_params_t* params, const int32_t* seq_lens,
+                                       const void* workspace, size_t workspace_bytes, void* out,
+                                       cudaStream_t stream);
+
+/*
+ * Dispatch: V2 when max_seq_len > v1_max_seq_len (8192 by default), else
+ * V1.  The workspace is only touched (and only required) when V2 runs.
+ * Source: commit 1a4e1005 "paged_attn.py", change 1 ("For sequences > 8192
+ * tokens ... V2"), and commit 4eb83a7e "qwen3_6_scripts", paragraph
+ * "forward_decode: V2 enabled via original heuristic".
+ */
+PA_API pa_status_t pa_decode(const pa_params_t* params, const void* q, const void* k_cache,
+                      const void* v_cache, const int32_t* block_tables, const int32_t* seq_lens,
+                      void* workspace, size_t workspace_bytes, void* out, cudaStream_t stream);
+
+/* Which path pa_decode takes for these parameters: 1 (V1), 2 (V2) or 0 if
+ * the parameters are invalid.  Pure host function. */
+PA_API int pa_decode_path(const pa_params_t* params);
+
+/* Static description of a status code (never NULL). */
+PA_API const char* pa_status_string(pa_status_t status);
+
+/* Zero the workspace's status word (enqueued on `stream`).  Call once after
+ * allocating a workspace; device errors then accumulate in it until read. */
+PA_API pa_status_t pa_workspace_init(void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Diagnostic: copy the status word to *status (PA_OK or the last device
+ * error recorded), WAITING for `stream` to finish, then zero it when
+ * `clear` is non-zero.  Not for use inside stream capture. */
+PA_API pa_status_t pa_read_device_status(const void* workspace, int32_t* status, int clear,
+                                  cudaStream_t stream);
+
+/* ABI version: major * 10000 + minor * 100 + patch. */
+PA_API int pa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H */

@@ -1,0 +1,278 @@
+"""Python binding of libpa: paged single-token decode attention on GB300.
+
+Argument marshalling only.  Every step of the computation runs in the CUDA
+kernels of ``libpa.so`` behind the C ABI of ``include/pa.h``; this module
+turns torch tensors into pointers and sizes, passes the current CUDA stream,
+and raises :class:`PaError` on a non-OK status.  There is no fallback: if
+``libpa.so`` has not been built, every call raises.
+
+Functions mirror the C entry points: :func:`workspace_size`,
+:func:`decode_v1`, :func:`decode_v2`, :func:`decode`, :func:`decode_path`,
+:func:`status_string`, :func:`workspace_init`, :func:`read_device_status`.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libpa.so")
+
+PA_OK = 0
+PA_ERR_INVALID_ARG = 1
+PA_ERR_UNSUPPORTED = 2
+PA_ERR_MISALIGNED = 3
+PA_ERR_WORKSPACE_TOO_SMALL = 4
+PA_ERR_CUDA = 5
+PA_ERR_DEVICE_TIMEOUT = 6
+PA_ERR_BAD_BLOCK_ID = 7
+PA_ERR_BAD_SEQ_LEN = 8
+
+PA_F32, PA_BF16, PA_F16 = 0, 1, 2
+PA_FLAG_PORTABLE = 1
+DEFAULT_V1_MAX_SEQ_LEN = 8192
+
+# Every symbol include/pa.h declares.
+EXPORTS = ("pa_workspace_size", "pa_decode_v1", "pa_decode_v2", "pa_decode_v2_partitions",
+           "pa_decode_v2_reduce", "pa_decode", "pa_decode_path", "pa_status_string",
+           "pa_workspace_init", "pa_read_device_status", "pa_version")
+
+
+class PaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+class Params(ctypes.Structure):
+    """Mirror of ``pa_params_t``."""
+    _fields_ = [
+        ("num_seqs", ctypes.c_int32),
+        ("num_heads", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("block_size", ctypes.c_int32),
+        ("num_blocks", ctypes.c_int32),
+        ("max_blocks_per_seq", ctypes.c_int32),
+        ("max_seq_len", ctypes.c_int32),
+        ("partition_size", ctypes.c_int32),
+        ("v1_max_seq_len", ctypes.c_int32),
+        ("kv_dtype", ctypes.c_int32),
+        ("out_dtype", ctypes.c_int32),
+        ("scale", ctypes.c_float),
+        ("flags", ctypes.c_int32),
+    ]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded ``libpa.so``; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it with "
+                    "`python -m paged_attention_decode_v2_gb300.build` (there is no fallback)")
+            L = ctypes.CDLL(LIB_PATH)
+            P = ctypes.c_void_p
+            PP = ctypes.POINTER(Params)
+            L.pa_workspace_size.argtypes = [PP]
+            L.pa_workspace_size.restype = ctypes.c_size_t
+            L.pa_decode_v1.argtypes = [PP, P, P, P, P, P, P, P]
+            L.pa_decode_v1.restype = ctypes.c_int
+            L.pa_decode_v2.argtypes = [PP, P, P, P, P, P, P, ctypes.c_size_t, P, P]
+            L.pa_decode_v2.restype = ctypes.c_int
+            L.pa_decode_v2_partitions.argtypes = [PP, P, P, P, P, P, P, ctypes.c_size_t, P]
+            L.pa_decode_v2_partitions.restype = ctypes.c_int
+            L.pa_decode_v2_reduce.argtypes = [PP, P, P, ctypes.c_size_t, P, P]
+            L.pa_decode_v2_reduce.restype = ctypes.c_int
+            L.pa_decode.argtypes = [PP, P, P, P, P, P, P, ctypes.c_size_t, P, P]
+            L.pa_decode.restype = ctypes.c_int
+            L.pa_decode_path.argtypes = [PP]
+            L.pa_decode_path.restype = ctypes.c_int
+            L.pa_status_string.argtypes = [ctypes.c_int]
+            L.pa_status_string.restype = ctypes.c_char_p
+            L.pa_workspace_init.argtypes = [P, ctypes.c_size_t, P]
+            L.pa_workspace_init.restype = ctypes.c_int
+            L.pa_read_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_int32), ctypes.c_int, P]
+            L.pa_read_device_status.restype = ctypes.c_int
+            L.pa_version.restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().pa_status_string(int(status)).decode()
+
+
+def _dtype_code(dtype) -> int:
+    import torch
+    codes = {torch.float32: PA_F32, torch.bfloat16: PA_BF16, torch.float16: PA_F16}
+    if dtype not in codes:
+        raise PaError(PA_ERR_UNSUPPORTED, f"dtype {dtype}")
+    return codes[dtype]
+
+
+def make_params(q, k_cache, block_tables, *, max_seq_len: int, scale: float,
+                partition_size: int = 512, out_dtype=None,
+                v1_max_seq_len: int = DEFAULT_V1_MAX_SEQ_LEN, portable: bool = False) -> Params:
+    """Fill a :class:`Params` from tensor shapes (no device access)."""
+    num_seqs, num_heads, head_dim = q.shape
+    num_blocks, num_kv_heads, block_size, d2 = k_cache.shape
+    if d2 != head_dim:
+        raise PaError(PA_ERR_INVALID_ARG, "q and k_cache head_dim differ")
+    return Params(num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                  block_tables.shape[1], int(max_seq_len), int(partition_size),
+                  int(v1_max_seq_len), _dtype_code(k_cache.dtype),
+                  _dtype_code(out_dtype if out_dtype is not None else q.dtype), float(scale),
+                  PA_FLAG_PORTABLE if portable else 0)
+
+
+def workspace_size(params: Params) -> int:
+    return int(lib().pa_workspace_size(ctypes.byref(params)))
+
+
+def decode_path(params: Params) -> int:
+    return int(lib().pa_decode_path(ctypes.byref(params)))
+
+
+def _stream(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _check_inputs(q, k_cache, v_cache, block_tables, seq_lens, out):
+    import torch
+    for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache),
+                    ("block_tables", block_tables), ("seq_lens", seq_lens), ("out", out)):
+        if not t.is_cuda:
+            raise PaError(PA_ERR_INVALID_ARG, f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise PaError(PA_ERR_INVALID_ARG, f"{name} must be contiguous")
+    if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise PaError(PA_ERR_INVALID_ARG, "block_tables and seq_lens must be int32")
+    if v_cache.shape != k_cache.shape or v_cache.dtype != k_cache.dtype or q.dtype != k_cache.dtype:
+        raise PaError(PA_ERR_INVALID_ARG, "q, k_cache and v_cache must agree in dtype/shape")
+    if tuple(out.shape) != tuple(q.shape):
+        raise PaError(PA_ERR_INVALID_ARG, "out must have q's shape")
+
+
+def _params_for(q, k_cache, block_tables, out, max_seq_len, scale, partition_size,
+                v1_max_seq_len, portable):
+    return make_params(q, k_cache, block_tables, max_seq_len=max_seq_len, scale=scale,
+                       partition_size=partition_size, out_dtype=out.dtype,
+                       v1_max_seq_len=v1_max_seq_len, portable=portable)
+
+
+def decode_v1(q, k_cache, v_cache, block_tables, seq_lens, out, *, max_seq_len: int,
+              scale: float, portable: bool = False, stream=None):
+    """``pa_decode_v1``: single pass per (sequence, KV head), into ``out``."""
+    _check_inputs(q, k_cache, v_cache, block_tables, seq_lens, out)
+    p = _params_for(q, k_cache, block_tables, out, max_seq_len, scale, 512,
+                    DEFAULT_V1_MAX_SEQ_LEN, portable)
+    st = lib().pa_decode_v1(ctypes.byref(p), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                            _ptr(block_tables), _ptr(seq_lens), _ptr(out), _stream(stream))
+    if st != PA_OK:
+        raise PaError(st, "pa_decode_v1")
+    return out
+
+
+def decode_v2(q, k_cache, v_cache, block_tables, seq_lens, out, workspace, *, max_seq_len: int,
+              scale: float, partition_size: int = 512, portable: bool = False, stream=None):
+    """``pa_decode_v2``: split-KV pass 1 + log-sum-exp reduce, into ``out``.
+
+    ``workspace`` is a CUDA uint8 tensor of at least :func:`workspace_size`
+    bytes, allocated once and reused.
+    """
+    _check_inputs(q, k_cache, v_cache, block_tables, seq_lens, out)
+    p = _params_for(q, k_cache, block_tables, out, max_seq_len, scale, partition_size,
+                    DEFAULT_V1_MAX_SEQ_LEN, portable)
+    st = lib().pa_decode_v2(ctypes.byref(p), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                            _ptr(block_tables), _ptr(seq_lens), _ptr(workspace),
+                            workspace.numel() * workspace.element_size(), _ptr(out),
+                            _stream(stream))
+    if st != PA_OK:
+        raise PaError(st, "pa_decode_v2")
+    return out
+
+
+def decode_v2_partitions(q, k_cache, v_cache, block_tables, seq_lens, workspace, *,
+                         max_seq_len: int, scale: float, partition_size: int = 512,
+                         out_dtype=None, portable: bool = False, stream=None):
+    """``pa_decode_v2_partitions``: V2 pass 1 only (fills the workspace)."""
+    p = make_params(q, k_cache, block_tables, max_seq_len=max_seq_len, scale=scale,
+                    partition_size=partition_size, out_dtype=out_dtype, portable=portable)
+    st = lib().pa_decode_v2_partitions(ctypes.byref(p), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                       _ptr(block_tables), _ptr(seq_lens), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(),
+                                       _stream(stream))
+    if st != PA_OK:
+        raise PaError(st, "pa_decode_v2_partitions")
+
+
+def decode_v2_reduce(params: Params, seq_lens, workspace, out, stream=None):
+    """``pa_decode_v2_reduce``: V2 pass 2 only (workspace -> out)."""
+    st = lib().pa_decode_v2_reduce(ctypes.byref(params), _ptr(seq_lens), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _ptr(out),
+                                   _stream(stream))
+    if st != PA_OK:
+        raise PaError(st, "pa_decode_v2_reduce")
+    return out
+
+
+def decode(q, k_cache, v_cache, block_tables, seq_lens, out, workspace=None, *,
+           max_seq_len: int, scale: float, partition_size: int = 512,
+           v1_max_seq_len: int = DEFAULT_V1_MAX_SEQ_LEN, portable: bool = False, stream=None):
+    """``pa_decode``: V2 when ``max_seq_len > v1_max_seq_len``, else V1."""
+    _check_inputs(q, k_cache, v_cache, block_tables, seq_lens, out)
+    p = _params_for(q, k_cache, block_tables, out, max_seq_len, scale, partition_size,
+                    v1_max_seq_len, portable)
+    nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib().pa_decode(ctypes.byref(p), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                         _ptr(block_tables), _ptr(seq_lens), _ptr(workspace), nbytes, _ptr(out),
+                         _stream(stream))
+    if st != PA_OK:
+        raise PaError(st, "pa_decode")
+    return out
+
+
+def alloc_workspace(params: Params, device=None):
+    """A CUDA uint8 tensor sized for ``params`` (allocated by torch), with its
+    status word zeroed."""
+    import torch
+    n = workspace_size(params)
+    if n == 0:
+        raise PaError(PA_ERR_INVALID_ARG, "pa_workspace_size")
+    ws = torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+    workspace_init(ws)
+    return ws
+
+
+def workspace_init(workspace, stream=None):
+    st = lib().pa_workspace_init(_ptr(workspace), workspace.numel(), _stream(stream))
+    if st != PA_OK:
+        raise PaError(st, "pa_workspace_init")
+
+
+def read_device_status(workspace, clear: bool = True, stream=None) -> int:
+    """The device status word (waits for the stream)."""
+    v = ctypes.c_int32(0)
+    st = lib().pa_read_device_status(_ptr(workspace), ctypes.byref(v), int(clear),
+                                     _stream(stream))
+    if st != PA_OK:
+        raise PaError(st, "pa_read_device_status")
+    return int(v.value)
+
+
+def version() -> int:
+    return int(lib().pa_version())

@@ -1,0 +1,53 @@
+// pa_internal.h -- internal interface between the C ABI (pa_api.cu) and the
+// kernels.  Not installed; users include include/pa.h only.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime_api.h>
+
+#include "pa.h"
+
+namespace pa {
+
+// Everything a kernel needs, passed by value as one kernel parameter.
+struct KernelArgs {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  const int32_t* seq_lens;
+  void* out;            // final output (V1 kernels, V2 reduce)
+  float* max_logits;    // V2 workspace regions
+  float* exp_sums;
+  float* tmp_out;
+  int32_t* status;      // V2 status word, or nullptr (V1)
+  int32_t num_seqs;
+  int32_t num_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t block_size;
+  int32_t num_blocks;
+  int32_t max_blocks_per_seq;
+  int32_t max_seq_len;
+  int32_t partition_size;  // V2: tokens per partition
+  int32_t num_partitions;  // V2: NP = ceil(max_seq_len / partition_size)
+  int32_t group;           // G = num_heads / num_kv_heads
+  int32_t out_dtype;       // pa_dtype_t
+  float scale_log2;        // scale * log2(e): logits are kept in base-2 units
+};
+
+// Launchers return cudaSuccess or the launch error.
+cudaError_t launch_generic_f32(const KernelArgs& a, bool v2, cudaStream_t s);
+cudaError_t launch_generic_bf16(const KernelArgs& a, bool v2, cudaStream_t s);
+cudaError_t launch_generic_f16(const KernelArgs& a, bool v2, cudaStream_t s);
+cudaError_t launch_reduce(const KernelArgs& a, cudaStream_t s, bool pdl);
+
+// Workspace carve-up shared by pa_workspace_size and the V2 launch.
+struct WorkspaceLayout {
+  size_t max_logits_off, exp_sums_off, tmp_out_off, total;
+};
+WorkspaceLayout workspace_layout(int64_t num_seqs, int64_t num_heads, int64_t head_dim,
+                                 int64_t num_partitions);
+
+}  // namespace pa

@@ -1,0 +1,74 @@
+"""Helpers for the GPU parity tests: run the CUDA path through the binding and
+compare with the float64 oracle."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import paged_attention_decode_v2_gb300 as pa
+
+TOL = {torch.float32: 1e-5, torch.bfloat16: 2e-3, torch.float16: 2e-3}
+
+
+def run(batch, path="decode", partition_size=512, portable=False, out_dtype=torch.float32,
+        v1_max_seq_len=pa.DEFAULT_V1_MAX_SEQ_LEN, workspace=None, return_ws=False):
+    """Run one decode step of ``batch`` (already on the GPU); returns out as a
+    float64 numpy array (and the workspace tensor when asked)."""
+    b = batch
+    out = torch.full(tuple(b.q.shape), float("nan"), dtype=out_dtype, device=b.q.device)
+    params = pa.make_params(b.q, b.k_cache, b.block_tables, max_seq_len=b.max_seq_len,
+                            scale=b.scale, partition_size=partition_size, out_dtype=out_dtype,
+                            v1_max_seq_len=v1_max_seq_len, portable=portable)
+    if workspace is None and path in ("v2", "decode"):
+        n = pa.workspace_size(params)
+        workspace = torch.empty(n, dtype=torch.uint8, device=b.q.device)
+        workspace.view(torch.float32)[64:].fill_(float("nan"))   # poison all but the status
+        pa.workspace_init(workspace)
+    kw = dict(max_seq_len=b.max_seq_len, scale=b.scale, portable=portable)
+    if path == "v1":
+        pa.decode_v1(b.q, b.k_cache, b.v_cache, b.block_tables, b.seq_lens, out, **kw)
+    elif path == "v2":
+        pa.decode_v2(b.q, b.k_cache, b.v_cache, b.block_tables, b.seq_lens, out, workspace,
+                     partition_size=partition_size, **kw)
+    else:
+        pa.decode(b.q, b.k_cache, b.v_cache, b.block_tables, b.seq_lens, out, workspace,
+                  partition_size=partition_size, v1_max_seq_len=v1_max_seq_len, **kw)
+    torch.cuda.synchronize()
+    res = out.double().cpu().numpy()
+    return (res, workspace) if return_ws else res
+
+
+def max_err(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    if a.size == 0:
+        return 0.0
+    return float(np.max(np.abs(a - b)))
+
+
+def assert_close(gpu, ref, tol, what=""):
+    gpu = np.asarray(gpu)
+    assert np.all(np.isfinite(gpu)), f"{what}: non-finite output"
+    err = max_err(gpu, ref)
+    assert err <= tol, f"{what}: max abs err {err:.3e} > {tol:.1e}"
+    return err
+
+
+def bf16_round(x: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.asarray(x, dtype=np.float32)).to(torch.bfloat16).double().numpy()
+
+
+def workspace_views(ws, batch, partition_size):
+    """max_logits, exp_sums, tmp_out views of a V2 workspace (layout of pa.h)."""
+    w = batch.workload
+    B, H, D = w.num_seqs, w.num_heads, w.head_dim
+    NP = max(1, -(-batch.max_seq_len // partition_size))
+    r = lambda x: (x + 255) // 256 * 256
+    f = ws.view(torch.float32)
+    o_ml = 256
+    o_es = o_ml + r(B * H * NP * 4)
+    o_to = o_es + r(B * H * NP * 4)
+    ml = f[o_ml // 4:o_ml // 4 + B * H * NP].view(B, H, NP)
+    es = f[o_es // 4:o_es // 4 + B * H * NP].view(B, H, NP)
+    to = f[o_to // 4:o_to // 4 + B * H * NP * D].view(B, H, NP, D)
+    return ml.double().cpu().numpy(), es.double().cpu().numpy(), to.double().cpu().numpy()

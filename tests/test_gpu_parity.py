@@ -1,0 +1,257 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle.
+
+Tolerance (max abs error on float32 output): 2e-3 for bf16/f16 caches with
+float32 accumulation, 1e-5 for float32 caches.  Inputs are NaN-poisoned
+everywhere outside the batch's tokens (unused pool blocks, slots past the
+last token, block-table entries past the last block are -1), and the V2
+workspace is NaN-filled before each call, so reading anything the method
+does not use shows up as NaN.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_attention_decode_v2_gb300 as pa
+from paged_attention_decode_v2_gb300 import workloads as wl
+from gpu_helpers import TOL, assert_close, bf16_round, max_err, run, workspace_views
+from oracle_pins import problem
+
+pytestmark = pytest.mark.gpu
+
+PATH_MODES = [("v1", False), ("v2", False), ("v1", True), ("v2", True)]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from paged_attention_decode_v2_gb300 import build
+    build.build()
+    assert torch.cuda.is_available(), "the gpu tests need a CUDA device"
+
+
+def _ref(batch_cpu):
+    return oracle.decode(batch_cpu.q, batch_cpu.k_cache, batch_cpu.v_cache,
+                         batch_cpu.block_tables, batch_cpu.seq_lens, batch_cpu.scale)
+
+
+# ---------------------------------------------------------------------------
+# small batches with each workload's head shapes: several tiles, ragged tails
+# ---------------------------------------------------------------------------
+SMALL = [
+    ("tiny_fp32_full", wl.WORKLOADS["tiny_fp32"], None, (32, 16, 64)),
+    ("gqa_shape", wl.scaled(wl.WORKLOADS["gqa_8k"], seq_len=1337, pool_blocks=None), None,
+     (512, 64, 1024)),
+    ("mixed_shape", wl.scaled(wl.WORKLOADS["mixed_32"], num_seqs=5, max_len=3000), None,
+     (512, 128)),
+    ("serving_shape", wl.scaled(wl.WORKLOADS["serving_256"], num_seqs=7, max_len=2500), None,
+     (512, 96)),
+    ("f16_gqa", wl.scaled(wl.WORKLOADS["gqa_8k"], seq_len=777, dtype=torch.float16), None,
+     (256,)),
+    ("f32_d128", wl.scaled(wl.WORKLOADS["serving_256"], num_seqs=3, max_len=700,
+                           dtype=torch.float32), None, (64,)),
+]
+
+
+@pytest.mark.parametrize("name,w,_,parts", SMALL, ids=[s[0] for s in SMALL])
+@pytest.mark.parametrize("path,portable", PATH_MODES, ids=[f"{p}{'-portable' if q else ''}"
+                                                           for p, q in PATH_MODES])
+def test_small_parity(name, w, _, parts, path, portable):
+    bc = wl.make(w, poison=True, table_pad=1)
+    ref = _ref(bc)
+    bg = bc.to("cuda")
+    tol = TOL[w.dtype]
+    for P in (parts if path == "v2" else parts[:1]):
+        got = run(bg, path=path, partition_size=P, portable=portable)
+        assert_close(got, ref, tol, f"{name} {path} P={P} portable={portable}")
+
+
+def test_v1_v2_agree():
+    bc = wl.make(wl.scaled(wl.WORKLOADS["gqa_8k"], seq_len=5000), poison=True)
+    bg = bc.to("cuda")
+    o1 = run(bg, path="v1")
+    for P in (64, 512, 1024):
+        o2 = run(bg, path="v2", partition_size=P)
+        assert max_err(o1, o2) <= 2e-3
+
+
+def test_dispatch_boundary():
+    """max_seq_len 8192 runs V1 and 8193 runs V2 (threshold of the pages),
+    both matching the oracle."""
+    for L in (8192, 8193):
+        w = wl.scaled(wl.WORKLOADS["mixed_32"], num_seqs=1, seq_len=L)
+        bc = wl.make(w, poison=True)
+        params = pa.make_params(bc.q, bc.k_cache, bc.block_tables, max_seq_len=L,
+                                scale=bc.scale)
+        assert pa.decode_path(params) == (1 if L == 8192 else 2)
+        got = run(bc.to("cuda"), path="decode")
+        assert_close(got, _ref(bc), 2e-3, f"dispatch L={L}")
+
+
+def test_workspace_intermediates_match_partitioned_oracle():
+    """Pass 1 alone: max_logits, exp_sums and tmp_output of every partition
+    that exists, against the oracle's Phase 1 in double."""
+    bc = wl.make(wl.scaled(wl.WORKLOADS["mixed_32"], num_seqs=4, max_len=2200), poison=True)
+    P = 256
+    _, ml_r, es_r, to_r = oracle.decode_partitioned(bc.q, bc.k_cache, bc.v_cache,
+                                                    bc.block_tables, bc.seq_lens, bc.scale, P,
+                                                    max_partitions=-(-bc.max_seq_len // P))
+    for portable in (False, True):
+        _, ws = run(bc.to("cuda"), path="v2", partition_size=P, portable=portable,
+                    return_ws=True)
+        ml, es, to = workspace_views(ws, bc, P)
+        live = np.isfinite(ml_r)
+        assert np.array_equal(np.isfinite(ml), live) or np.all(np.isfinite(ml[live]))
+        assert max_err(ml[live], ml_r[live]) <= 1e-4 * max(1.0, np.abs(ml_r[live]).max())
+        rel = np.abs(es[live] - es_r[live]) / es_r[live]
+        assert rel.max() <= 1e-4
+        assert max_err(to[live], to_r[live]) <= 2e-3
+
+
+def test_block_permutation_is_bit_identical():
+    bc = wl.make(wl.scaled(wl.WORKLOADS["gqa_8k"], seq_len=3001), poison=False)
+    nb = bc.k_cache.shape[0]
+    perm = torch.randperm(nb, generator=torch.Generator().manual_seed(5))
+    k2 = torch.empty_like(bc.k_cache)
+    v2 = torch.empty_like(bc.v_cache)
+    k2[perm] = bc.k_cache
+    v2[perm] = bc.v_cache
+    bt2 = perm[bc.block_tables.long()].to(torch.int32)
+    b1 = bc.to("cuda")
+    b2 = wl.Batch(bc.workload, bc.q, k2, v2, bt2, bc.seq_lens, bc.max_seq_len).to("cuda")
+    for path, portable in PATH_MODES:
+        o1 = run(b1, path=path, portable=portable)
+        o2 = run(b2, path=path, portable=portable)
+        assert np.array_equal(o1, o2), f"{path} portable={portable}"
+
+
+def test_repeat_runs_are_bit_identical():
+    bg = wl.make(wl.scaled(wl.WORKLOADS["serving_256"], num_seqs=9, max_len=4000)).to("cuda")
+    for path, portable in PATH_MODES:
+        first = run(bg, path=path, portable=portable)
+        for _ in range(3):
+            assert np.array_equal(run(bg, path=path, portable=portable), first)
+
+
+def test_bf16_output():
+    bc = wl.make(wl.scaled(wl.WORKLOADS["gqa_8k"], seq_len=2100), poison=True)
+    ref = _ref(bc)
+    for path in ("v1", "v2"):
+        got = run(bc.to("cuda"), path=path, out_dtype=torch.bfloat16)
+        # float32 result within 2e-3, then one bf16 rounding: half an ulp more
+        ulp_half = np.abs(bf16_round(ref)) * 2.0 ** -8
+        assert np.all(np.abs(got - ref) <= 2e-3 + ulp_half), path
+
+
+# ---------------------------------------------------------------------------
+# edge cases
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("path,portable", PATH_MODES)
+def test_edge_lengths(path, portable):
+    """L = 1, a block boundary, a partition boundary, a partition plus one,
+    and a zero-length sequence (zero row) in one batch."""
+    lens = (1, 16, 512, 513, 0, 1023, 31)
+    bc = problem(dtype=torch.bfloat16, lens=lens, Hq=24, Hkv=4, D=256, BS=16, seed=7)
+    ref = _ref(bc)
+    got = run(bc.to("cuda"), path=path, partition_size=512, portable=portable)
+    assert np.all(got[4] == 0.0)
+    assert_close(got, ref, 2e-3, f"edge lengths {path}")
+
+
+def test_single_key_gives_value_row():
+    bc = problem(dtype=torch.bfloat16, lens=(1, 1, 1), Hq=6, Hkv=1, D=128, BS=32, seed=8)
+    for path, portable in PATH_MODES:
+        got = run(bc.to("cuda"), path=path, portable=portable)
+        for s in range(3):
+            v0 = bc.v_cache[int(bc.block_tables[s, 0]), 0, 0].double().numpy()
+            for h in range(6):
+                assert np.array_equal(got[s, h], v0), (path, portable)
+
+
+def test_partition_larger_than_sequence():
+    bc = problem(dtype=torch.bfloat16, lens=(300, 77), Hq=8, Hkv=2, D=64, BS=16, seed=9)
+    ref = _ref(bc)
+    got = run(bc.to("cuda"), path="v2", partition_size=4096)
+    assert_close(got, ref, 2e-3, "P > L")
+
+
+def test_empty_batch():
+    bc = problem(dtype=torch.bfloat16, lens=(), Hq=8, Hkv=2, D=64, BS=16, seed=10, pool=4)
+    bg = bc.to("cuda")
+    out = torch.empty((0, 8, 64), dtype=torch.float32, device="cuda")
+    pa.decode(bg.q, bg.k_cache, bg.v_cache, bg.block_tables, bg.seq_lens, out, None,
+              max_seq_len=0, scale=bc.scale)
+    torch.cuda.synchronize()
+
+
+def test_large_logits_stay_finite():
+    w = wl.scaled(wl.WORKLOADS["long_100k"], seq_len=20000)
+    bc = wl.make(dataclasses_replace(w, key_outlier_frac=0.002), poison=True)
+    ref = _ref(bc)
+    for path, portable in PATH_MODES:
+        got = run(bc.to("cuda"), path=path, portable=portable)
+        assert_close(got, ref, 2e-3, f"outliers {path} portable={portable}")
+
+
+def dataclasses_replace(w, **kw):
+    import dataclasses
+    return dataclasses.replace(w, **kw)
+
+
+def test_bad_block_id_poisons_the_row_and_sets_status():
+    bc = problem(dtype=torch.bfloat16, lens=(100, 100), Hq=4, Hkv=2, D=64, BS=16, seed=11)
+    bc.block_tables[1, 2] = bc.k_cache.shape[0] + 5          # outside the pool
+    ref = _ref(problem(dtype=torch.bfloat16, lens=(100, 100), Hq=4, Hkv=2, D=64, BS=16, seed=11))
+    bg = bc.to("cuda")
+    for path, portable in PATH_MODES:
+        got, ws = run(bg, path="v2" if path == "v2" else "v1", portable=portable,
+                      partition_size=32, return_ws=True)
+        assert np.all(np.isnan(got[1])), path
+        assert_close(got[0], ref[0], 2e-3, "untouched row")
+        if path == "v2":
+            assert pa.read_device_status(ws) == pa.PA_ERR_BAD_BLOCK_ID
+            assert pa.read_device_status(ws) == pa.PA_OK      # cleared by the read
+
+
+def test_bad_seq_len_poisons_the_row_and_sets_status():
+    bc = problem(dtype=torch.bfloat16, lens=(60, 60), Hq=4, Hkv=2, D=64, BS=16, seed=12)
+    bg = bc.to("cuda")
+    bg.seq_lens[1] = 61                                       # > max_seq_len promised
+    ref = _ref(bc)
+    for path, portable in PATH_MODES:
+        got, ws = run(bg, path=path, portable=portable, partition_size=32, return_ws=True)
+        assert np.all(np.isnan(got[1])), path
+        assert_close(got[0], ref[0], 2e-3, "untouched row")
+        if path == "v2":
+            assert pa.read_device_status(ws) == pa.PA_ERR_BAD_SEQ_LEN
+
+
+# ---------------------------------------------------------------------------
+# the five workloads at full size, in the launch configuration bench.py times
+# ---------------------------------------------------------------------------
+FULL = ["tiny_fp32", "gqa_8k", "long_100k", "mixed_32", "serving_256"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_workload(name):
+    w = wl.WORKLOADS[name]
+    bg = wl.make(w, device="cuda", poison=True)
+    bc = bg.to("cpu")
+    tol = TOL[w.dtype]
+    rows_all = w.num_seqs * w.num_heads
+    if name in ("mixed_32", "serving_256"):
+        # the oracle computes a sample of rows; cover the longest and
+        # shortest sequences and a seeded random set
+        lens = bc.seq_lens.tolist()
+        pick = {int(np.argmax(lens)), int(np.argmin(lens))}
+        g = np.random.default_rng(123)
+        pick |= set(int(x) for x in g.choice(w.num_seqs, size=min(6, w.num_seqs), replace=False))
+        rows = sorted(b * w.num_heads + h for b in pick for h in range(w.num_heads))
+    else:
+        rows = list(range(rows_all))
+    ref = oracle.decode(bc.q, bc.k_cache, bc.v_cache, bc.block_tables, bc.seq_lens, bc.scale,
+                        rows=rows)
+    for P in w.partition_sizes:
+        for path in ("decode", "v2") if bg.max_seq_len <= pa.DEFAULT_V1_MAX_SEQ_LEN else ("decode",):
+            got = run(bg, path=path, partition_size=P).reshape(rows_all, w.head_dim)
+            assert_close(got[rows], ref, tol, f"{name} {path} P={P}")
+            assert np.all(np.isfinite(got)), "every row finite"
