@@ -176,6 +176,36 @@ PA_API pa_status_t pa_decode(const pa_params_t* params, const void* q, const voi
                       const void* v_cache, const int32_t* block_tables, const int32_t* seq_lens,
                       void* workspace, size_t workspace_bytes, void* out, cudaStream_t stream);
 
+/*
+ * pa_decode_v2 for callers that cannot allocate device memory.  The pages
+ * have no counterpart of this call: it exists for callers with no way to
+ * call cudaMalloc or any allocator where they decode (a plugin of a host
+ * runtime that owns every device allocation, a C program linking libpa
+ * without torch, a real-time loop that must not stall on or fail an
+ * allocation).  The caller still passes its inputs and `out`; the V2
+ * workspace is instead a fixed array of PA_STATIC_WORKSPACE_BYTES (16 MiB)
+ * that the library keeps in device memory, which every GPU that loads
+ * libpa.so holds until the process exits.
+ *   - Parameters whose pa_workspace_size() exceeds PA_STATIC_WORKSPACE_BYTES
+ *     are rejected with PA_ERR_WORKSPACE_TOO_SMALL before anything is
+ *     enqueued (16 MiB covers, e.g., one 24-head, head_dim-256 sequence of
+ *     up to about 340K tokens at partition_size 512).
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - All calls on a device share the array, and it keeps the last call's
+ *     contents (nothing in it needs to start at zero).  Calls that overlap on
+ *     the GPU race on it: order them on one stream.
+ *   - It makes no allocation of its own and calls no allocating routine.
+ *   - Device-detected input errors still show as NaN output rows; the status
+ *     word is not reported by this call.
+ */
+#define PA_STATIC_WORKSPACE_BYTES ((size_t)16 << 20)
+PA_API pa_status_t pa_decode_v2_static(const pa_params_t* params, const void* q,
+                                       const void* k_cache, const void* v_cache,
+                                       const int32_t* block_tables, const int32_t* seq_lens,
+                                       void* out, cudaStream_t stream);
+
 /* Which path pa_decode takes for these parameters: 1 (V1), 2 (V2) or 0 if
  * the parameters are invalid.  Pure host function. */
 PA_API int pa_decode_path(const pa_params_t* params);

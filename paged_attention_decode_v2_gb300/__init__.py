@@ -36,7 +36,8 @@ DEFAULT_V1_MAX_SEQ_LEN = 8192
 # Every symbol include/pa.h declares.
 EXPORTS = ("pa_workspace_size", "pa_decode_v1", "pa_decode_v2", "pa_decode_v2_partitions",
            "pa_decode_v2_reduce", "pa_decode", "pa_decode_path", "pa_status_string",
-           "pa_workspace_init", "pa_read_device_status", "pa_version")
+           "pa_workspace_init", "pa_read_device_status", "pa_version", "pa_decode_v2_static")
+PA_STATIC_WORKSPACE_BYTES = 16 << 20
 
 
 class PaError(RuntimeError):
@@ -102,6 +103,8 @@ def lib() -> ctypes.CDLL:
             L.pa_read_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_int32), ctypes.c_int, P]
             L.pa_read_device_status.restype = ctypes.c_int
             L.pa_version.restype = ctypes.c_int
+            L.pa_decode_v2_static.argtypes = [PP, P, P, P, P, P, P, P]
+            L.pa_decode_v2_static.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -243,6 +246,22 @@ def decode(q, k_cache, v_cache, block_tables, seq_lens, out, workspace=None, *,
                          _stream(stream))
     if st != PA_OK:
         raise PaError(st, "pa_decode")
+    return out
+
+
+def decode_v2_static(q, k_cache, v_cache, block_tables, seq_lens, out, *, max_seq_len: int,
+                     scale: float, partition_size: int = 512, portable: bool = False,
+                     stream=None):
+    """``pa_decode_v2_static``: V2 with the library's own fixed 16 MiB device
+    workspace, for callers that cannot allocate one.  Calls on a device share
+    that workspace, so calls that overlap on the GPU race."""
+    _check_inputs(q, k_cache, v_cache, block_tables, seq_lens, out)
+    p = _params_for(q, k_cache, block_tables, out, max_seq_len, scale, partition_size,
+                    DEFAULT_V1_MAX_SEQ_LEN, portable)
+    st = lib().pa_decode_v2_static(ctypes.byref(p), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                   _ptr(block_tables), _ptr(seq_lens), _ptr(out), _stream(stream))
+    if st != PA_OK:
+        raise PaError(st, "pa_decode_v2_static")
     return out
 
 

@@ -1,0 +1,67 @@
+// pa_static.cu -- pa_decode_v2_static: the V2 decode with its workspace in a
+// fixed-size device array that the library holds, for callers that cannot
+// allocate device memory themselves.
+//
+// Some callers have no way to call cudaMalloc (or any allocator) at the
+// point where they decode: a plugin inside a host runtime that owns every
+// device allocation and forbids raw ones, a C program that links libpa
+// without torch or any other allocator, or a real-time loop that must not
+// risk an allocation failure or an allocator stall mid-run.  This entry
+// point lets them run V2 with nothing but their inputs and outputs.
+//
+// The array below lives in the library's device image: every GPU on which
+// libpa.so's code is loaded holds PA_STATIC_WORKSPACE_BYTES of device memory
+// for it until the process exits.  All calls on a device share it and it
+// keeps whatever the last call left there; V2 only reads back what the same
+// call wrote, so nothing in it has to start at zero.  Two calls that overlap
+// on the GPU (different streams, or different host threads, without ordering
+// between them) race on it: order them on one stream.
+#include <mutex>
+
+#include <cuda_runtime_api.h>
+
+#include "pa.h"
+#include "pa_internal.h"
+
+namespace {
+
+static __device__ __align__(256) unsigned char g_static_ws[PA_STATIC_WORKSPACE_BYTES];
+
+constexpr int kMaxDevices = 128;
+std::mutex g_mu;
+void* g_ws_addr[kMaxDevices];  // device address of g_static_ws, per device
+
+// Host code cannot use g_static_ws's address directly (on the host it names
+// a stand-in, not device memory), so look it up once per device, with that
+// device current, and cache it.
+pa_status_t static_ws_address(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_ws_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_ws) != cudaSuccess || !p) return PA_ERR_CUDA;
+    g_ws_addr[dev] = p;
+  }
+  *out = g_ws_addr[dev];
+  return PA_OK;
+}
+
+}  // namespace
+
+extern "C" pa_status_t pa_decode_v2_static(const pa_params_t* params, const void* q,
+                                           const void* k_cache, const void* v_cache,
+                                           const int32_t* block_tables, const int32_t* seq_lens,
+                                           void* out, cudaStream_t stream) {
+  const size_t need = pa_workspace_size(params);
+  if (need == 0)  // invalid parameters: let the regular checks name the problem
+    return pa_decode_v2(params, q, k_cache, v_cache, block_tables, seq_lens, nullptr, 0, out,
+                        stream);
+  if (need > PA_STATIC_WORKSPACE_BYTES) return PA_ERR_WORKSPACE_TOO_SMALL;
+  if (params->num_seqs == 0) return PA_OK;
+  void* ws = nullptr;
+  const pa_status_t st = static_ws_address(&ws);
+  if (st != PA_OK) return st;
+  return pa_decode_v2(params, q, k_cache, v_cache, block_tables, seq_lens, ws,
+                      PA_STATIC_WORKSPACE_BYTES, out, stream);
+}
