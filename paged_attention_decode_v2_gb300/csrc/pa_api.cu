@@ -88,8 +88,9 @@ KernelArgs make_args(const pa_params_t* p, const void* q, const void* k, const v
   return a;
 }
 
-cudaError_t launch_pass(const KernelArgs& a, pa_dtype_t kv, bool v2, cudaStream_t s) {
-  switch (kv) {
+cudaError_t launch_pass(const pa_params_t* p, const KernelArgs& a, bool v2, cudaStream_t s) {
+  if (tc_applicable(p)) return launch_tc(a, p->kv_dtype, v2, s);
+  switch (p->kv_dtype) {
     case PA_F32: return launch_generic_f32(a, v2, s);
     case PA_BF16: return launch_generic_bf16(a, v2, s);
     default: return launch_generic_f16(a, v2, s);
@@ -135,7 +136,7 @@ pa_status_t pa_decode_v1(const pa_params_t* p, const void* q, const void* k_cach
   st = check_tensors(q, k_cache, v_cache, block_tables, seq_lens, out);
   if (st != PA_OK) return st;
   KernelArgs a = make_args(p, q, k_cache, v_cache, block_tables, seq_lens, out);
-  if (launch_pass(a, p->kv_dtype, false, stream) != cudaSuccess) return PA_ERR_CUDA;
+  if (launch_pass(p, a, false, stream) != cudaSuccess) return PA_ERR_CUDA;
   return PA_OK;
 }
 
@@ -187,7 +188,7 @@ pa_status_t pa_decode_v2(const pa_params_t* p, const void* q, const void* k_cach
   pa_status_t st = prepare_v2(p, q, k_cache, v_cache, block_tables, seq_lens, workspace,
                               workspace_bytes, out, true, true, &a);
   if (st != PA_OK || p->num_seqs == 0) return st;
-  if (launch_pass(a, p->kv_dtype, true, stream) != cudaSuccess) return PA_ERR_CUDA;
+  if (launch_pass(p, a, true, stream) != cudaSuccess) return PA_ERR_CUDA;
   if (launch_reduce(a, stream, true) != cudaSuccess) return PA_ERR_CUDA;
   return PA_OK;
 }
@@ -200,7 +201,7 @@ pa_status_t pa_decode_v2_partitions(const pa_params_t* p, const void* q, const v
   pa_status_t st = prepare_v2(p, q, k_cache, v_cache, block_tables, seq_lens, workspace,
                               workspace_bytes, nullptr, true, false, &a);
   if (st != PA_OK || p->num_seqs == 0) return st;
-  if (launch_pass(a, p->kv_dtype, true, stream) != cudaSuccess) return PA_ERR_CUDA;
+  if (launch_pass(p, a, true, stream) != cudaSuccess) return PA_ERR_CUDA;
   return PA_OK;
 }
 

@@ -43,6 +43,11 @@ cudaError_t launch_generic_bf16(const KernelArgs& a, bool v2, cudaStream_t s);
 cudaError_t launch_generic_f16(const KernelArgs& a, bool v2, cudaStream_t s);
 cudaError_t launch_reduce(const KernelArgs& a, cudaStream_t s, bool pdl);
 
+// Tensor-core path (pa_tc_host.cu): whether it serves these parameters on
+// the current device, and its launch (pass 1 for V2, the whole pass for V1).
+bool tc_applicable(const pa_params_t* p);
+cudaError_t launch_tc(const KernelArgs& a, pa_dtype_t kv, bool v2, cudaStream_t s);
+
 // Workspace carve-up shared by pa_workspace_size and the V2 launch.
 struct WorkspaceLayout {
   size_t max_logits_off, exp_sums_off, tmp_out_off, total;

@@ -1,0 +1,524 @@
+// pa_tc.cuh -- tensor-core decode kernel for bf16 / f16 caches on GB300.
+//
+// Same contract as the CUDA-core kernels (pa_generic.cuh): one CTA per
+// (sequence, KV head, token range), the range being one V2 partition or the
+// whole sequence (V1), all G <= 8 query heads of the KV head served at once,
+// so each key/value byte is read once per step.
+//
+// Roles (192 threads, warp-specialised):
+//   warp 4      producer: reads the block table and streams the range's
+//               keys and values into a ring of 16 KB shared-memory stages
+//               with TMA (cp.async.bulk.tensor, 128-byte swizzle);
+//   warp 5      MMA issuer: tcgen05.mma, accumulators in tensor memory;
+//   warps 0-3   softmax + epilogue: read logits from tensor memory, form the
+//               chunk max / exp / sums, write P^T, combine chunks, store.
+//
+// Per chunk of up to 512 tokens (a 512-token partition is one chunk):
+//   QK^T   S^T[t, h] = sum_d K[t, d] q[h, d]    M = 128 tokens, N = 16, K = d
+//          A = K tile (K-major, SW128): a stage holds one 64-element slice of
+//          head_dim for 128 tokens, filled by one TMA copy per KV block;
+//          B = q (K-major, SW128, rows >= G zero); D in tensor memory.
+//   softmax l = S * scale * log2(e); m = chunk max; p = exp2(l - m); sums in
+//          f32; p goes to P^T as a 16-bit hi part (columns 0..7) plus the
+//          rounded remainder p - hi (columns 8..15), so P.V sees ~16
+//          significant bits of p.
+//   P.V    O^T[d, n] = sum_t V[t, d] P^T[t, n]  M = 128 (half of head_dim),
+//          N = 16, K = 16 tokens; A = V (MN-major, SW128), one TMA copy per
+//          KV block; B = P^T (K-major, no swizzle).
+// Chunks are combined in registers with the running max / rescale, so a
+// range of any length (V1) works; within a chunk all logits exist before the
+// max is taken, so nothing is rescaled per block.
+//
+// This is Phase 1 of the V2 scheme in commit 4eb83a7e "qwen3_6_scripts",
+// paragraph "Implementation (paged_attention_v2_pytorch.py)" (per-partition
+// QK^T, softmax and weighted V sum into tmp_output / exp_sums / max_logits),
+// with whole tiles staged by bulk asynchronous copies (the SM90+ tier of the
+// same page's BlockLoadToShared notes) and the dot products on tensor cores.
+//
+// Every wait is bounded.  A wait that gives up sets the status word to
+// PA_ERR_DEVICE_TIMEOUT and an abort flag that ends every other wait at
+// once; in-flight copies and MMAs are drained (again with a bound) before
+// tensor memory is released, and the CTA's outputs become NaN.
+#pragma once
+
+#include <type_traits>
+
+#include <cuda.h>
+
+#include "pa_device.cuh"
+#include "pa_sm100.cuh"
+
+namespace pa {
+
+namespace tc {
+
+constexpr int kThreads = 192;
+constexpr int kChunk = 512;           // tokens per chunk
+constexpr int kTile = 128;            // tokens per QK^T MMA (M)
+constexpr int kStageBytes = 16384;    // one ring stage
+constexpr int kStages = 5;            // ring depth (two CTAs fit one SM)
+constexpr int kTmemCols = 128;        // S: 4 tiles x 16 columns, O^T: 2 x 16
+constexpr int kOCol = 64;             // first tensor-memory column of O^T
+constexpr long long kDefaultWaitBudget = 4000000000LL;  // cycles (about 2 s)
+
+template <int D>
+struct Layout {
+  static constexpr int kSlices = D / 64;                  // 64-element head_dim slices
+  static constexpr int kHalves = D / 128;                 // 128-row halves of head_dim
+  static constexpr int kVTokens = kStageBytes / (D * 2);  // tokens per V stage
+  static constexpr int kQOff = kStages * kStageBytes;     // 1024-aligned
+  static constexpr int kPtOff = kQOff + kSlices * 16 * 128;
+  static constexpr int kCtrlOff = kPtOff + (kChunk / 16) * 512;
+  static constexpr int kBytes = kCtrlOff + 512;
+  static constexpr int kSmem = kBytes + 1024;             // room to align to 1024
+};
+
+struct Ctrl {
+  uint64_t full[kStages];   // stage landed (TMA transaction count)
+  uint64_t empty[kStages];  // stage consumed (MMA commit)
+  uint64_t s_full;          // chunk logits ready in tensor memory
+  uint64_t p_ready;         // P^T written (128 softmax threads arrive)
+  uint64_t o_full;          // chunk O^T ready in tensor memory
+  uint64_t tail;            // last value stage landed and its tail cleared
+  uint64_t drain;           // abort path: all issued MMAs finished
+  uint32_t tmem;
+  int bad;                  // a block id of the range was outside the pool
+  int abort;                // some wait gave up
+  float red[2][4][8];       // cross-warp max / sum of the softmax warps
+};
+static_assert(sizeof(Ctrl) <= 512, "control block");
+
+__device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ void fail(Ctrl& c, int32_t* status) {
+  c.abort = 1;
+  set_status(status, PA_ERR_DEVICE_TIMEOUT);
+}
+
+__device__ __forceinline__ uint16_t bits16(__nv_bfloat16 x) { return __bfloat16_as_ushort(x); }
+__device__ __forceinline__ uint16_t bits16(__half x) { return __half_as_ushort(x); }
+__device__ __forceinline__ __nv_bfloat16 round16(float x, __nv_bfloat16*) {
+  return __float2bfloat16_rn(x);
+}
+__device__ __forceinline__ __half round16(float x, __half*) { return __float2half_rn(x); }
+
+}  // namespace tc
+
+template <typename T, int D, int BS, bool kV2>
+__global__ void __launch_bounds__(tc::kThreads, 2)
+    pa_tc_kernel(const KernelArgs a, const __grid_constant__ CUtensorMap kmap,
+                 const __grid_constant__ CUtensorMap vmap, long long budget) {
+  using namespace tc;
+  using Lay = Layout<D>;
+  static_assert(D == 128 || D == 256, "head_dim");
+  static_assert(BS % 16 == 0 && kTile % BS == 0 && Lay::kVTokens % BS == 0, "block size");
+  constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (sm100::smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* ring = smem;
+  uint8_t* qs = smem + Lay::kQOff;
+  uint8_t* pt = smem + Lay::kPtOff;
+  Ctrl& c = *reinterpret_cast<Ctrl*>(smem + Lay::kCtrlOff);
+
+  // Let the reduce kernel (launched as a programmatic dependent) be
+  // scheduled as soon as every CTA of this grid has started.
+  asm volatile("griddepcontrol.launch_dependents;");
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = blockIdx.z, kvh = blockIdx.y, part = blockIdx.x;
+  const int G = a.group, Hq = a.num_heads;
+  const int64_t row0 = static_cast<int64_t>(b) * Hq + kvh * G;  // first query-head row
+  const int32_t L = a.seq_lens[b];
+
+  if (!seq_len_ok(a, L)) {
+    if (tid == 0 && part == 0) set_status(a.status, PA_ERR_BAD_SEQ_LEN);
+    if (!kV2)
+      for (int i = tid; i < G * D; i += kThreads) store_out(a.out, row0 * D + i, a.out_dtype, qnan());
+    return;
+  }
+  const int32_t t0 = kV2 ? part * a.partition_size : 0;
+  const int32_t t1 = kV2 ? min(L, t0 + a.partition_size) : L;
+  if (t0 >= t1) {
+    if (!kV2)  // V1 of an empty sequence: a zero row
+      for (int i = tid; i < G * D; i += kThreads) store_out(a.out, row0 * D + i, a.out_dtype, 0.f);
+    return;
+  }
+  const int nchunks = (t1 - t0 + kChunk - 1) / kChunk;
+  // the range ends inside a 16-token MMA step: those value rows get cleared
+  const bool tail_fix = (t1 % 16) != 0;
+
+  // ---- set-up -----------------------------------------------------------------
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      sm100::mbar_init(&c.full[s], 1);
+      sm100::mbar_init(&c.empty[s], 1);
+    }
+    sm100::mbar_init(&c.s_full, 1);
+    sm100::mbar_init(&c.p_ready, 128);
+    sm100::mbar_init(&c.o_full, 1);
+    sm100::mbar_init(&c.tail, 1);
+    sm100::mbar_init(&c.drain, 1);
+    c.bad = 0;
+    c.abort = 0;
+  }
+  if (warp == 5) {
+    sm100::tmem_alloc(&c.tmem, kTmemCols);
+    sm100::tmem_relinquish();
+  }
+  if (warp == 4 && lane == 0) {
+    sm100::tma_prefetch_desc(&kmap);
+    sm100::tma_prefetch_desc(&vmap);
+  }
+  if (warp < 4) {
+    // the G query rows of this KV head -> SW128 K-major [slice][16 rows][64]
+    const T* qp = static_cast<const T*>(a.q) + row0 * D;
+    for (int i = tid; i < 16 * (D / 8); i += 128) {
+      const int row = i / (D / 8), d = (i % (D / 8)) * 8;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (row < G) v = *reinterpret_cast<const uint4*>(qp + row * D + d);
+      const int sl = d / 64, ch = (d % 64) / 8;
+      *reinterpret_cast<uint4*>(qs + sl * 2048 + row * 128 + ((ch ^ (row & 7)) << 4)) = v;
+    }
+    sm100::fence_proxy_async_smem();
+  }
+  sm100::tc_fence_before();
+  __syncthreads();
+  sm100::tc_fence_after();
+  const uint32_t tmem = c.tmem;
+  volatile int* abort_flag = &c.abort;
+
+  // softmax-warp state, used by the epilogue
+  float m_run[8], s_run[8], acc[Lay::kHalves][8];
+#pragma unroll
+  for (int h = 0; h < 8; ++h) {
+    m_run[h] = -INFINITY;
+    s_run[h] = 0.f;
+#pragma unroll
+    for (int j = 0; j < Lay::kHalves; ++j) acc[j][h] = 0.f;
+  }
+
+  if (warp == 4) {
+    // ========================= producer ===========================================
+    const int32_t* bt = a.block_tables + static_cast<int64_t>(b) * a.max_blocks_per_seq;
+    uint32_t g = 0;  // ring stages issued so far
+    bool ok = true;
+    for (int ci = 0; ci < nchunks && ok; ++ci) {
+      const int c0 = t0 + ci * kChunk;
+      const int n = min(kChunk, t1 - c0);
+      const int nblk = (n + BS - 1) / BS;  // <= 32: one block id per lane
+      int32_t id = 0;
+      bool bad = false;
+      if (lane < nblk) {
+        id = bt[c0 / BS + lane];
+        bad = id < 0 || id >= a.num_blocks;
+      }
+      if (__any_sync(0xffffffffu, bad) && lane == 0) {
+        c.bad = 1;
+        set_status(a.status, PA_ERR_BAD_BLOCK_ID);
+      }
+      // TMA row of the block's first slot; a bad id becomes a negative row,
+      // which TMA fills with zeros instead of reading memory.
+      const int32_t y = bad ? -BS : (id * a.num_kv_heads + kvh) * BS;
+      const int nt = (n + kTile - 1) / kTile;
+      for (int tt = 0; tt < nt && ok; ++tt) {
+        const int jb0 = tt * kTile / BS;
+        const int jb1 = (min(n, tt * kTile + kTile) + BS - 1) / BS;
+        for (int sl = 0; sl < Lay::kSlices; ++sl) {
+          const int slot = g % kStages;
+          ok = sm100::mbar_wait(&c.empty[slot], ((g / kStages) & 1) ^ 1, budget, abort_flag);
+          if (!ok) break;
+          if (lane == 0) sm100::mbar_arrive_expect_tx(&c.full[slot], (jb1 - jb0) * BS * 128);
+          for (int j = jb0; j < jb1; ++j) {
+            const int32_t yj = __shfl_sync(0xffffffffu, y, j);
+            if (lane == 0)
+              sm100::tma_load_2d(ring + slot * kStageBytes + (j - jb0) * BS * 128, &kmap,
+                                 &c.full[slot], sl * 64, yj);
+          }
+          ++g;
+        }
+      }
+      const int nv = (n + Lay::kVTokens - 1) / Lay::kVTokens;
+      for (int v = 0; v < nv && ok; ++v) {
+        const int jb0 = v * Lay::kVTokens / BS;
+        const int jb1 = (min(n, (v + 1) * Lay::kVTokens) + BS - 1) / BS;
+        const int slot = g % kStages;
+        const uint32_t par = (g / kStages) & 1;
+        ok = sm100::mbar_wait(&c.empty[slot], par ^ 1, budget, abort_flag);
+        if (!ok) break;
+        if (lane == 0) sm100::mbar_arrive_expect_tx(&c.full[slot], (jb1 - jb0) * BS * D * 2);
+        for (int j = jb0; j < jb1; ++j) {
+          const int32_t yj = __shfl_sync(0xffffffffu, y, j);
+          if (lane == 0)
+            sm100::tma_load_3d(ring + slot * kStageBytes + (j - jb0) * BS * D * 2, &vmap,
+                               &c.full[slot], 0, yj, 0);
+        }
+        ++g;
+        if (tail_fix && ci == nchunks - 1 && v == nv - 1) {
+          // Clear the value rows from the range end to the end of its
+          // 16-token step: P^T is zero there, but 0 * NaN would be NaN.
+          ok = sm100::mbar_wait(&c.full[slot], par, budget, abort_flag);
+          if (!ok) break;
+          const int r0 = n - v * Lay::kVTokens;  // first row past the end
+          const int r1 = (r0 + 15) / 16 * 16;    // end of its 16-token step
+          uint8_t* st = ring + slot * kStageBytes;
+          const int pieces = (r1 - r0) * Lay::kSlices * 8;  // 16-byte pieces
+          for (int i = lane; i < pieces; i += 32) {
+            const int line = i / 8, piece = i % 8;
+            const int r = r0 + line / Lay::kSlices, sl = line % Lay::kSlices;
+            *reinterpret_cast<uint4*>(st + (r / BS) * BS * D * 2 + sl * BS * 128 + (r % BS) * 128 +
+                                      piece * 16) = make_uint4(0u, 0u, 0u, 0u);
+          }
+          sm100::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) sm100::mbar_arrive(&c.tail);
+        }
+      }
+    }
+    if (!ok) {
+      if (lane == 0) fail(c, a.status);
+      // Copies already issued must land before the CTA may exit: wait for
+      // the newest use of every slot (older uses completed before it began).
+      for (uint32_t gg = g > kStages ? g - kStages : 0; gg < g; ++gg)
+        sm100::mbar_wait(&c.full[gg % kStages], (gg / kStages) & 1, budget, nullptr);
+    }
+  } else if (warp == 5) {
+    // ========================= MMA issuer =========================================
+    if (lane == 0) {
+      constexpr uint32_t id_qk = sm100::idesc_f16(kBf16, false, false, 128, 16);
+      constexpr uint32_t id_pv = sm100::idesc_f16(kBf16, true, false, 128, 16);
+      const uint32_t q_base = sm100::smem_u32(qs);
+      const uint32_t pt_base = sm100::smem_u32(pt);
+      const uint32_t ring_base = sm100::smem_u32(ring);
+      uint32_t g = 0;
+      bool ok = true;
+      for (int ci = 0; ci < nchunks && ok; ++ci) {
+        const int c0 = t0 + ci * kChunk;
+        const int n = min(kChunk, t1 - c0);
+        const int nt = (n + kTile - 1) / kTile;
+        for (int tt = 0; tt < nt && ok; ++tt) {
+          for (int sl = 0; sl < Lay::kSlices; ++sl) {
+            const int slot = g % kStages;
+            ok = sm100::mbar_wait(&c.full[slot], (g / kStages) & 1, budget, abort_flag);
+            if (!ok) break;
+            sm100::tc_fence_after();
+            const uint32_t st = ring_base + slot * kStageBytes;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t ad = sm100::smem_desc(st + kk * 32, 16, 1024, sm100::kSw128);
+              const uint64_t bd =
+                  sm100::smem_desc(q_base + sl * 2048 + kk * 32, 16, 1024, sm100::kSw128);
+              sm100::mma_f16(tmem + tt * 16, ad, bd, id_qk, (sl | kk) != 0);
+            }
+            sm100::mma_commit(&c.empty[slot]);
+            ++g;
+          }
+        }
+        if (!ok) break;
+        sm100::mma_commit(&c.s_full);
+        ok = sm100::mbar_wait(&c.p_ready, ci & 1, budget, abort_flag);
+        if (!ok) break;
+        sm100::tc_fence_after();
+        const int nv = (n + Lay::kVTokens - 1) / Lay::kVTokens;
+        bool first = true;
+        for (int v = 0; v < nv; ++v) {
+          const int slot = g % kStages;
+          if (tail_fix && ci == nchunks - 1 && v == nv - 1)
+            ok = sm100::mbar_wait(&c.tail, 0, budget, abort_flag);
+          else
+            ok = sm100::mbar_wait(&c.full[slot], (g / kStages) & 1, budget, abort_flag);
+          if (!ok) break;
+          sm100::tc_fence_after();
+          const uint32_t st = ring_base + slot * kStageBytes;
+          const int toks = min(Lay::kVTokens, n - v * Lay::kVTokens);
+          for (int r = 0; r < toks; r += 16) {
+            const int jb = r / BS, s0 = r % BS;
+            const uint64_t bd = sm100::smem_desc(pt_base + ((v * Lay::kVTokens + r) / 16) * 512,
+                                                 256, 128, sm100::kSwNone);
+#pragma unroll
+            for (int j = 0; j < Lay::kHalves; ++j) {
+              const uint64_t ad = sm100::smem_desc(
+                  st + jb * BS * D * 2 + 2 * j * BS * 128 + s0 * 128, BS * 128, 1024, sm100::kSw128);
+              sm100::mma_f16(tmem + kOCol + 16 * j, ad, bd, id_pv, !first);
+            }
+            first = false;
+          }
+          sm100::mma_commit(&c.empty[slot]);
+          ++g;
+        }
+        if (!ok) break;
+        sm100::mma_commit(&c.o_full);
+      }
+      if (!ok) {
+        fail(c, a.status);
+        // no MMA may still be running when tensor memory is released
+        sm100::mma_commit(&c.drain);
+        sm100::mbar_wait(&c.drain, 0, budget, nullptr);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ========================= softmax + combine (warps 0-3) ======================
+    // Every softmax thread runs the same iterations and barriers whatever
+    // happens; a failed wait only marks the abort, which ends later waits.
+    const int r = tid;  // tensor-memory lane: token of a tile, or head_dim row
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const float sl2 = a.scale_log2;
+    for (int ci = 0; ci < nchunks; ++ci) {
+      const int c0 = t0 + ci * kChunk;
+      const int n = min(kChunk, t1 - c0);
+      const int nt = (n + kTile - 1) / kTile;
+      const int n16 = (n + 15) / 16 * 16;
+      if (!sm100::mbar_wait(&c.s_full, ci & 1, budget, abort_flag)) fail(c, a.status);
+      sm100::tc_fence_after();
+      __syncwarp();
+      float mx[8];
+#pragma unroll
+      for (int h = 0; h < 8; ++h) mx[h] = -INFINITY;
+      for (int tt = 0; tt < nt; ++tt) {
+        float s[16];
+        sm100::tmem_ld16(tmem + lane_base + tt * 16, s);
+        sm100::tmem_wait_ld();
+        if (tt * kTile + r < n) {
+#pragma unroll
+          for (int h = 0; h < 8; ++h)
+            if (h < G) mx[h] = fmaxf(mx[h], s[h] * sl2);
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < 8; ++h) {
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], o));
+        if (lane == 0) c.red[0][warp][h] = mx[h];
+      }
+      softmax_sync();
+      float mc[8];
+#pragma unroll
+      for (int h = 0; h < 8; ++h)
+        mc[h] = fmaxf(fmaxf(c.red[0][0][h], c.red[0][1][h]), fmaxf(c.red[0][2][h], c.red[0][3][h]));
+      float sum[8];
+#pragma unroll
+      for (int h = 0; h < 8; ++h) sum[h] = 0.f;
+      for (int tt = 0; tt < nt; ++tt) {
+        float s[16];
+        sm100::tmem_ld16(tmem + lane_base + tt * 16, s);
+        sm100::tmem_wait_ld();
+        const int tok = tt * kTile + r;
+        if (tok < n16) {
+          const bool valid = tok < n;
+          // P^T element (tok, col): step tok/16, core (tok%16)/8, column group
+          // col/8, column col%8, token tok%8 -- no-swizzle K-major core matrices
+          uint8_t* dst = pt + (tok / 16) * 512 + ((tok % 16) / 8) * 256 + (tok % 8) * 2;
+#pragma unroll
+          for (int h = 0; h < 8; ++h) {
+            float p = 0.f;
+            if (valid && h < G) p = exp2f(s[h] * sl2 - mc[h]);
+            sum[h] += p;
+            const T hi = round16(p, static_cast<T*>(nullptr));
+            const T lo = round16(p - to_float(hi), static_cast<T*>(nullptr));
+            *reinterpret_cast<uint16_t*>(dst + h * 16) = bits16(hi);
+            *reinterpret_cast<uint16_t*>(dst + 128 + h * 16) = bits16(lo);
+          }
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < 8; ++h) {
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) sum[h] += __shfl_xor_sync(0xffffffffu, sum[h], o);
+        if (lane == 0) c.red[1][warp][h] = sum[h];
+      }
+      sm100::fence_proxy_async_smem();
+      sm100::tc_fence_before();
+      sm100::mbar_arrive(&c.p_ready);
+      softmax_sync();
+      float f_old[8], f_new[8];
+#pragma unroll
+      for (int h = 0; h < 8; ++h) {
+        const float sc = (c.red[1][0][h] + c.red[1][1][h]) + (c.red[1][2][h] + c.red[1][3][h]);
+        const float m_new = fmaxf(m_run[h], mc[h]);
+        f_old[h] = m_run[h] == -INFINITY ? 0.f : exp2f(m_run[h] - m_new);
+        f_new[h] = mc[h] == -INFINITY ? 0.f : exp2f(mc[h] - m_new);
+        s_run[h] = s_run[h] * f_old[h] + sc * f_new[h];
+        m_run[h] = m_new;
+      }
+      if (!sm100::mbar_wait(&c.o_full, ci & 1, budget, abort_flag)) fail(c, a.status);
+      sm100::tc_fence_after();
+      __syncwarp();
+#pragma unroll
+      for (int j = 0; j < Lay::kHalves; ++j) {
+        float o[16];
+        sm100::tmem_ld16(tmem + lane_base + kOCol + 16 * j, o);
+        sm100::tmem_wait_ld();
+#pragma unroll
+        for (int h = 0; h < 8; ++h) acc[j][h] = acc[j][h] * f_old[h] + (o[h] + o[8 + h]) * f_new[h];
+      }
+      sm100::tc_fence_before();
+    }
+  }
+
+  // ---- epilogue ---------------------------------------------------------------
+  sm100::tc_fence_before();
+  __syncthreads();
+  sm100::tc_fence_after();
+  if (warp == 5) sm100::tmem_dealloc(tmem, kTmemCols);
+  if (warp < 4) {
+    const bool poison = c.bad != 0 || c.abort != 0;
+#pragma unroll
+    for (int j = 0; j < Lay::kHalves; ++j) {
+      const int d = j * 128 + tid;
+#pragma unroll
+      for (int h = 0; h < 8; ++h) {
+        if (h >= G) break;
+        const float o = poison ? qnan() : acc[j][h] / s_run[h];
+        if constexpr (kV2)
+          a.tmp_out[((row0 + h) * a.num_partitions + part) * D + d] = o;
+        else
+          store_out(a.out, (row0 + h) * D + d, a.out_dtype, o);
+      }
+    }
+    if (kV2 && tid < G) {
+      const int64_t w = (row0 + tid) * a.num_partitions + part;
+      float m = m_run[0], s = s_run[0];
+#pragma unroll
+      for (int h = 1; h < 8; ++h)
+        if (h == tid) {
+          m = m_run[h];
+          s = s_run[h];
+        }
+      a.max_logits[w] = poison ? qnan() : m * kLn2;
+      a.exp_sums[w] = s;
+    }
+  }
+}
+
+template <typename T, int D, int BS>
+cudaError_t launch_tc_t(const KernelArgs& a, const CUtensorMap& km, const CUtensorMap& vm,
+                        bool v2, cudaStream_t s) {
+  static bool configured[2][128] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  auto kern = v2 ? pa_tc_kernel<T, D, BS, true> : pa_tc_kernel<T, D, BS, false>;
+  const int smem = tc::Layout<D>::kSmem;
+  if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+  if (!configured[v2][dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured[v2][dev] = true;
+  }
+  const dim3 grid(v2 ? a.num_partitions : 1, a.num_kv_heads, a.num_seqs);
+  kern<<<grid, tc::kThreads, smem, s>>>(a, km, vm, tc::kDefaultWaitBudget);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_tc_dtype(const KernelArgs& a, const CUtensorMap& km, const CUtensorMap& vm,
+                            bool v2, cudaStream_t s) {
+  if (a.head_dim == 256 && a.block_size == 16) return launch_tc_t<T, 256, 16>(a, km, vm, v2, s);
+  if (a.head_dim == 256 && a.block_size == 32) return launch_tc_t<T, 256, 32>(a, km, vm, v2, s);
+  if (a.head_dim == 128 && a.block_size == 16) return launch_tc_t<T, 128, 16>(a, km, vm, v2, s);
+  if (a.head_dim == 128 && a.block_size == 32) return launch_tc_t<T, 128, 32>(a, km, vm, v2, s);
+  if (a.head_dim == 128 && a.block_size == 64) return launch_tc_t<T, 128, 64>(a, km, vm, v2, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace pa

@@ -1,0 +1,12 @@
+// pa_tc_bf16.cu -- instantiates the tensor-core decode kernels for bf16 caches
+// (one translation unit per element type, compiled in parallel).
+#include "pa_tc.cuh"
+
+namespace pa {
+
+cudaError_t launch_tc_bf16(const KernelArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                         bool v2, cudaStream_t s) {
+  return launch_tc_dtype<__nv_bfloat16>(a, kmap, vmap, v2, s);
+}
+
+}  // namespace pa

@@ -1,0 +1,101 @@
+// pa_tc_host.cu -- host side of the tensor-core path: when it applies, and
+// the TMA tensor maps of the two caches.
+//
+// The caches are viewed as rows of head_dim elements, one row per
+// (block, KV head, slot): row = (block * num_kv_heads + kv_head) *
+// block_size + slot.  Keys use a 2-D map (head_dim, rows) with a 64 x
+// block_size box, so one copy brings one 64-element slice of one block;
+// values use a 3-D map (64, rows, head_dim / 64) whose box is a whole block
+// laid out slice-major.  Both use the 128-byte swizzle the MMA descriptors
+// expect.
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "pa_internal.h"
+
+namespace pa {
+
+cudaError_t launch_tc_bf16(const KernelArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                           bool v2, cudaStream_t s);
+cudaError_t launch_tc_f16(const KernelArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                          bool v2, cudaStream_t s);
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 1 if the current device runs the sm_100-family tensor-core kernels.
+bool device_has_tcgen05() {
+  static int cache[128] = {};  // 0 unknown, 1 yes, 2 no
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return false;
+  if (!cache[dev]) {
+    int major = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cache[dev] = major == 10 ? 1 : 2;
+  }
+  return cache[dev] == 1;
+}
+
+}  // namespace
+
+bool tc_applicable(const pa_params_t* p) {
+  if (p->flags & PA_FLAG_PORTABLE) return false;
+  if (p->kv_dtype != PA_BF16 && p->kv_dtype != PA_F16) return false;
+  if (p->num_heads / p->num_kv_heads > 8) return false;
+  const int D = p->head_dim, BS = p->block_size;
+  const bool shape = (D == 256 && (BS == 16 || BS == 32)) ||
+                     (D == 128 && (BS == 16 || BS == 32 || BS == 64));
+  if (!shape) return false;
+  const int64_t rows = static_cast<int64_t>(p->num_blocks) * p->num_kv_heads * BS;
+  if (rows + BS >= (int64_t(1) << 31)) return false;  // TMA row coordinates are int32
+  return encoder() != nullptr && device_has_tcgen05();
+}
+
+cudaError_t launch_tc(const KernelArgs& a, pa_dtype_t kv, bool v2, cudaStream_t s) {
+  auto enc = encoder();
+  if (!enc) return cudaErrorNotSupported;
+  const CUtensorMapDataType dt =
+      kv == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const cuuint64_t D = static_cast<cuuint64_t>(a.head_dim);
+  const cuuint64_t rows = static_cast<cuuint64_t>(a.num_blocks) * a.num_kv_heads * a.block_size;
+  const cuuint32_t BS = static_cast<cuuint32_t>(a.block_size);
+  CUtensorMap kmap, vmap;
+  {
+    const cuuint64_t dims[2] = {D, rows};
+    const cuuint64_t strides[1] = {D * 2};
+    const cuuint32_t box[2] = {64, BS};
+    const cuuint32_t es[2] = {1, 1};
+    if (enc(&kmap, dt, 2, const_cast<void*>(a.k_cache), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[3] = {64, rows, D / 64};
+    const cuuint64_t strides[2] = {D * 2, 128};
+    const cuuint32_t box[3] = {64, BS, static_cast<cuuint32_t>(D / 64)};
+    const cuuint32_t es[3] = {1, 1, 1};
+    if (enc(&vmap, dt, 3, const_cast<void*>(a.v_cache), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  return kv == PA_BF16 ? launch_tc_bf16(a, kmap, vmap, v2, s) : launch_tc_f16(a, kmap, vmap, v2, s);
+}
+
+}  // namespace pa
