@@ -36,7 +36,7 @@ pa_status_t check_params(const pa_params_t* p, bool v2) {
     return PA_ERR_UNSUPPORTED;
   if (p->out_dtype != PA_F32 && p->out_dtype != p->kv_dtype) return PA_ERR_UNSUPPORTED;
   if (p->head_dim != 64 && p->head_dim != 128 && p->head_dim != 256) return PA_ERR_UNSUPPORTED;
-  if (p->num_heads > 65535 * 8 || p->num_kv_heads > 65535 || p->num_seqs > 65535)
+  if (p->num_heads > 65535 || p->num_kv_heads > 65535 || p->num_seqs > 65535)
     return PA_ERR_UNSUPPORTED;
   if (v2) {
     if (p->partition_size < 1 || p->partition_size % p->block_size) return PA_ERR_INVALID_ARG;

@@ -1,33 +1,32 @@
-// pa_tc.cuh -- tensor-core decode kernel for bf16 / f16 caches on GB300.
+// pa_tc.cuh -- persistent tensor-core decode kernel for bf16 / f16 caches.
 //
-// Same contract as the CUDA-core kernels (pa_generic.cuh): one CTA per
-// (sequence, KV head, token range), the range being one V2 partition or the
-// whole sequence (V1), all G <= 8 query heads of the KV head served at once,
-// so each key/value byte is read once per step.
+// Work items.  A work item is one (sequence, KV head, token range), the
+// range being one V2 partition or the whole sequence (V1); all G <= 8 query
+// heads of the KV head are served together, so each key/value byte is read
+// once per step.  The grid is persistent (about two CTAs per SM); CTA c
+// takes items c, c + gridDim.x, ... in partition-major order and skips the
+// ones a sequence does not have.  The shared-memory ring keeps streaming
+// from one item into the next, so a CTA never stops loading between items.
 //
 // Roles (192 threads, warp-specialised):
-//   warp 4      producer: reads the block table and streams the range's
-//               keys and values into a ring of 16 KB shared-memory stages
-//               with TMA (cp.async.bulk.tensor, 128-byte swizzle);
+//   warp 4      producer: streams q, keys and values into shared memory with
+//               TMA (cp.async.bulk.tensor, 128-byte swizzle): keys as one
+//               64-element head_dim slice of 128 tokens per 16 KB stage,
+//               values as whole KV blocks;
 //   warp 5      MMA issuer: tcgen05.mma, accumulators in tensor memory;
-//   warps 0-3   softmax + epilogue: read logits from tensor memory, form the
-//               chunk max / exp / sums, write P^T, combine chunks, store.
+//   warps 0-3   softmax + epilogue.
 //
-// Per chunk of up to 512 tokens (a 512-token partition is one chunk):
+// Per chunk of up to 512 tokens of an item:
 //   QK^T   S^T[t, h] = sum_d K[t, d] q[h, d]    M = 128 tokens, N = 16, K = d
-//          A = K tile (K-major, SW128): a stage holds one 64-element slice of
-//          head_dim for 128 tokens, filled by one TMA copy per KV block;
-//          B = q (K-major, SW128, rows >= G zero); D in tensor memory.
 //   softmax l = S * scale * log2(e); m = chunk max; p = exp2(l - m); sums in
 //          f32; p goes to P^T as a 16-bit hi part (columns 0..7) plus the
 //          rounded remainder p - hi (columns 8..15), so P.V sees ~16
 //          significant bits of p.
 //   P.V    O^T[d, n] = sum_t V[t, d] P^T[t, n]  M = 128 (half of head_dim),
-//          N = 16, K = 16 tokens; A = V (MN-major, SW128), one TMA copy per
-//          KV block; B = P^T (K-major, no swizzle).
-// Chunks are combined in registers with the running max / rescale, so a
-// range of any length (V1) works; within a chunk all logits exist before the
-// max is taken, so nothing is rescaled per block.
+//          N = 16, K = 16 tokens; V is the MN-major operand.
+// Chunks of one item are combined in registers with the running max and
+// rescale (V1 ranges of any length); within a chunk all logits exist before
+// the max is taken, so nothing is rescaled per block.
 //
 // This is Phase 1 of the V2 scheme in commit 4eb83a7e "qwen3_6_scripts",
 // paragraph "Implementation (paged_attention_v2_pytorch.py)" (per-partition
@@ -37,8 +36,8 @@
 //
 // Every wait is bounded.  A wait that gives up sets the status word to
 // PA_ERR_DEVICE_TIMEOUT and an abort flag that ends every other wait at
-// once; in-flight copies and MMAs are drained (again with a bound) before
-// tensor memory is released, and the CTA's outputs become NaN.
+// once; issued copies and MMAs are drained (again with a bound) before
+// tensor memory is released, and the outputs the CTA writes become NaN.
 #pragma once
 
 #include <type_traits>
@@ -56,9 +55,10 @@ constexpr int kThreads = 192;
 constexpr int kChunk = 512;           // tokens per chunk
 constexpr int kTile = 128;            // tokens per QK^T MMA (M)
 constexpr int kStageBytes = 16384;    // one ring stage
-constexpr int kStages = 5;            // ring depth (two CTAs fit one SM)
+constexpr int kStages = 5;            // ring depth (two CTAs share one SM)
 constexpr int kTmemCols = 128;        // S: 4 tiles x 16 columns, O^T: 2 x 16
 constexpr int kOCol = 64;             // first tensor-memory column of O^T
+constexpr int kCtasPerSm = 2;
 constexpr long long kDefaultWaitBudget = 4000000000LL;  // cycles (about 2 s)
 
 template <int D>
@@ -66,27 +66,50 @@ struct Layout {
   static constexpr int kSlices = D / 64;                  // 64-element head_dim slices
   static constexpr int kHalves = D / 128;                 // 128-row halves of head_dim
   static constexpr int kVTokens = kStageBytes / (D * 2);  // tokens per V stage
-  static constexpr int kQOff = kStages * kStageBytes;     // 1024-aligned
-  static constexpr int kPtOff = kQOff + kSlices * 16 * 128;
+  static constexpr int kQOff = kStages * kStageBytes;     // 2 q buffers x slices x 1 KB
+  static constexpr int kPtOff = kQOff + 2 * kSlices * 1024;
   static constexpr int kCtrlOff = kPtOff + (kChunk / 16) * 512;
   static constexpr int kBytes = kCtrlOff + 512;
-  static constexpr int kSmem = kBytes + 1024;             // room to align to 1024
+  static constexpr int kSmem = kBytes + 1024;  // room to align to 1024
 };
 
 struct Ctrl {
   uint64_t full[kStages];   // stage landed (TMA transaction count)
   uint64_t empty[kStages];  // stage consumed (MMA commit)
+  uint64_t qfull[2];        // q buffer landed
+  uint64_t qempty[2];       // q buffer no longer read by MMAs
   uint64_t s_full;          // chunk logits ready in tensor memory
   uint64_t p_ready;         // P^T written (128 softmax threads arrive)
   uint64_t o_full;          // chunk O^T ready in tensor memory
-  uint64_t tail;            // last value stage landed and its tail cleared
+  uint64_t tail;            // producer-private: a tail value stage landed
   uint64_t drain;           // abort path: all issued MMAs finished
   uint32_t tmem;
-  int bad;                  // a block id of the range was outside the pool
   int abort;                // some wait gave up
   float red[2][4][8];       // cross-warp max / sum of the softmax warps
 };
 static_assert(sizeof(Ctrl) <= 512, "control block");
+
+// One work item, decoded the same way by every role.
+struct Item {
+  int b, kvh, part;
+  int32_t t0, t1;  // token range; empty when t0 >= t1
+  bool len_ok;     // 0 <= seq_len <= max_seq_len
+};
+
+__device__ __forceinline__ Item decode_item(const KernelArgs& a, int64_t k, bool v2) {
+  Item it;
+  const int64_t per_part = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads;
+  it.part = v2 ? static_cast<int>(k / per_part) : 0;
+  const int64_t rem = v2 ? k % per_part : k;
+  it.b = static_cast<int>(rem / a.num_kv_heads);
+  it.kvh = static_cast<int>(rem % a.num_kv_heads);
+  const int32_t L = __ldg(a.seq_lens + it.b);
+  it.len_ok = seq_len_ok(a, L);
+  it.t0 = v2 ? it.part * a.partition_size : 0;
+  it.t1 = v2 ? min(L, it.t0 + a.partition_size) : L;
+  if (!it.len_ok) it.t1 = it.t0;
+  return it;
+}
 
 __device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
@@ -105,9 +128,10 @@ __device__ __forceinline__ __half round16(float x, __half*) { return __float2hal
 }  // namespace tc
 
 template <typename T, int D, int BS, bool kV2>
-__global__ void __launch_bounds__(tc::kThreads, 2)
+__global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
     pa_tc_kernel(const KernelArgs a, const __grid_constant__ CUtensorMap kmap,
-                 const __grid_constant__ CUtensorMap vmap, long long budget) {
+                 const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap qmap,
+                 int64_t total_items, long long budget) {
   using namespace tc;
   using Lay = Layout<D>;
   static_assert(D == 128 || D == 256, "head_dim");
@@ -121,32 +145,14 @@ __global__ void __launch_bounds__(tc::kThreads, 2)
   uint8_t* pt = smem + Lay::kPtOff;
   Ctrl& c = *reinterpret_cast<Ctrl*>(smem + Lay::kCtrlOff);
 
-  // Let the reduce kernel (launched as a programmatic dependent) be
-  // scheduled as soon as every CTA of this grid has started.
-  asm volatile("griddepcontrol.launch_dependents;");
-
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int b = blockIdx.z, kvh = blockIdx.y, part = blockIdx.x;
   const int G = a.group, Hq = a.num_heads;
-  const int64_t row0 = static_cast<int64_t>(b) * Hq + kvh * G;  // first query-head row
-  const int32_t L = a.seq_lens[b];
+  const int64_t stride = gridDim.x;
 
-  if (!seq_len_ok(a, L)) {
-    if (tid == 0 && part == 0) set_status(a.status, PA_ERR_BAD_SEQ_LEN);
-    if (!kV2)
-      for (int i = tid; i < G * D; i += kThreads) store_out(a.out, row0 * D + i, a.out_dtype, qnan());
-    return;
-  }
-  const int32_t t0 = kV2 ? part * a.partition_size : 0;
-  const int32_t t1 = kV2 ? min(L, t0 + a.partition_size) : L;
-  if (t0 >= t1) {
-    if (!kV2)  // V1 of an empty sequence: a zero row
-      for (int i = tid; i < G * D; i += kThreads) store_out(a.out, row0 * D + i, a.out_dtype, 0.f);
-    return;
-  }
-  const int nchunks = (t1 - t0 + kChunk - 1) / kChunk;
-  // the range ends inside a 16-token MMA step: those value rows get cleared
-  const bool tail_fix = (t1 % 16) != 0;
+  // The grid is persistent, so every CTA starts at once: let the reduce
+  // kernel (a programmatic dependent) be scheduled now; it waits for this
+  // grid's results before reading them.
+  asm volatile("griddepcontrol.launch_dependents;");
 
   // ---- set-up -----------------------------------------------------------------
   if (tid == 0) {
@@ -154,12 +160,15 @@ __global__ void __launch_bounds__(tc::kThreads, 2)
       sm100::mbar_init(&c.full[s], 1);
       sm100::mbar_init(&c.empty[s], 1);
     }
+    for (int s = 0; s < 2; ++s) {
+      sm100::mbar_init(&c.qfull[s], 1);
+      sm100::mbar_init(&c.qempty[s], 1);
+    }
     sm100::mbar_init(&c.s_full, 1);
     sm100::mbar_init(&c.p_ready, 128);
     sm100::mbar_init(&c.o_full, 1);
     sm100::mbar_init(&c.tail, 1);
     sm100::mbar_init(&c.drain, 1);
-    c.bad = 0;
     c.abort = 0;
   }
   if (warp == 5) {
@@ -169,18 +178,7 @@ __global__ void __launch_bounds__(tc::kThreads, 2)
   if (warp == 4 && lane == 0) {
     sm100::tma_prefetch_desc(&kmap);
     sm100::tma_prefetch_desc(&vmap);
-  }
-  if (warp < 4) {
-    // the G query rows of this KV head -> SW128 K-major [slice][16 rows][64]
-    const T* qp = static_cast<const T*>(a.q) + row0 * D;
-    for (int i = tid; i < 16 * (D / 8); i += 128) {
-      const int row = i / (D / 8), d = (i % (D / 8)) * 8;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (row < G) v = *reinterpret_cast<const uint4*>(qp + row * D + d);
-      const int sl = d / 64, ch = (d % 64) / 8;
-      *reinterpret_cast<uint4*>(qs + sl * 2048 + row * 128 + ((ch ^ (row & 7)) << 4)) = v;
-    }
-    sm100::fence_proxy_async_smem();
+    sm100::tma_prefetch_desc(&qmap);
   }
   sm100::tc_fence_before();
   __syncthreads();
@@ -188,90 +186,107 @@ __global__ void __launch_bounds__(tc::kThreads, 2)
   const uint32_t tmem = c.tmem;
   volatile int* abort_flag = &c.abort;
 
-  // softmax-warp state, used by the epilogue
-  float m_run[8], s_run[8], acc[Lay::kHalves][8];
-#pragma unroll
-  for (int h = 0; h < 8; ++h) {
-    m_run[h] = -INFINITY;
-    s_run[h] = 0.f;
-#pragma unroll
-    for (int j = 0; j < Lay::kHalves; ++j) acc[j][h] = 0.f;
-  }
-
   if (warp == 4) {
     // ========================= producer ===========================================
-    const int32_t* bt = a.block_tables + static_cast<int64_t>(b) * a.max_blocks_per_seq;
-    uint32_t g = 0;  // ring stages issued so far
+    const uint64_t stream_once = sm100::l2_evict_first_policy();  // keys and values
+    uint64_t keep;                                                // q: default priority
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(keep));
+    uint32_t g = 0, qn = 0, tn = 0;  // ring stages / q buffers / tail stages so far
+    int tail_pending = -1;           // slot of a tail stage still landing
     bool ok = true;
-    for (int ci = 0; ci < nchunks && ok; ++ci) {
-      const int c0 = t0 + ci * kChunk;
-      const int n = min(kChunk, t1 - c0);
-      const int nblk = (n + BS - 1) / BS;  // <= 32: one block id per lane
-      int32_t id = 0;
-      bool bad = false;
-      if (lane < nblk) {
-        id = bt[c0 / BS + lane];
-        bad = id < 0 || id >= a.num_blocks;
+    for (int64_t k = blockIdx.x; k < total_items && ok; k += stride) {
+      const Item it = decode_item(a, k, kV2);
+      if (it.t0 >= it.t1) continue;
+      const int32_t* bt = a.block_tables + static_cast<int64_t>(it.b) * a.max_blocks_per_seq;
+      // q rows of the item's query heads (8 rows; rows past G are ignored)
+      {
+        const int qb = qn & 1;
+        ok = sm100::mbar_wait(&c.qempty[qb], ((qn >> 1) & 1) ^ 1, budget, abort_flag);
+        if (!ok) break;
+        if (lane == 0) {
+          sm100::mbar_arrive_expect_tx(&c.qfull[qb], Lay::kSlices * 1024);
+          const int32_t qrow = it.b * Hq + it.kvh * G;
+          for (int sl = 0; sl < Lay::kSlices; ++sl)
+            sm100::tma_load_2d(qs + (qb * Lay::kSlices + sl) * 1024, &qmap, &c.qfull[qb], sl * 64,
+                               qrow, keep);
+        }
+        ++qn;
       }
-      if (__any_sync(0xffffffffu, bad) && lane == 0) {
-        c.bad = 1;
-        set_status(a.status, PA_ERR_BAD_BLOCK_ID);
-      }
-      // TMA row of the block's first slot; a bad id becomes a negative row,
-      // which TMA fills with zeros instead of reading memory.
-      const int32_t y = bad ? -BS : (id * a.num_kv_heads + kvh) * BS;
-      const int nt = (n + kTile - 1) / kTile;
-      for (int tt = 0; tt < nt && ok; ++tt) {
-        const int jb0 = tt * kTile / BS;
-        const int jb1 = (min(n, tt * kTile + kTile) + BS - 1) / BS;
-        for (int sl = 0; sl < Lay::kSlices; ++sl) {
+      const int nchunks = (it.t1 - it.t0 + kChunk - 1) / kChunk;
+      const bool tail_fix = (it.t1 % 16) != 0;
+      for (int ci = 0; ci < nchunks && ok; ++ci) {
+        const int c0 = it.t0 + ci * kChunk;
+        const int n = min(kChunk, it.t1 - c0);
+        const int nblk = (n + BS - 1) / BS;  // <= 32: one block id per lane
+        int32_t id = 0;
+        bool bad = false;
+        if (lane < nblk) {
+          id = __ldg(bt + c0 / BS + lane);
+          bad = id < 0 || id >= a.num_blocks;
+        }
+        if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(a.status, PA_ERR_BAD_BLOCK_ID);
+        // TMA row of the block's first slot; a bad id becomes a negative row,
+        // which TMA fills with zeros instead of reading memory.
+        const int32_t y = bad ? -BS : (id * a.num_kv_heads + it.kvh) * BS;
+        const int nt = (n + kTile - 1) / kTile;
+        for (int tt = 0; tt < nt && ok; ++tt) {
+          const int jb0 = tt * kTile / BS;
+          const int jb1 = (min(n, tt * kTile + kTile) + BS - 1) / BS;
+          for (int sl = 0; sl < Lay::kSlices; ++sl) {
+            const int slot = g % kStages;
+            ok = sm100::mbar_wait(&c.empty[slot], ((g / kStages) & 1) ^ 1, budget, abort_flag);
+            if (!ok) break;
+            if (lane == 0) sm100::mbar_arrive_expect_tx(&c.full[slot], (jb1 - jb0) * BS * 128);
+            for (int j = jb0; j < jb1; ++j) {
+              const int32_t yj = __shfl_sync(0xffffffffu, y, j);
+              if (lane == 0)
+                sm100::tma_load_2d(ring + slot * kStageBytes + (j - jb0) * BS * 128, &kmap,
+                                   &c.full[slot], sl * 64, yj, stream_once);
+            }
+            ++g;
+          }
+        }
+        const int nv = (n + Lay::kVTokens - 1) / Lay::kVTokens;
+        for (int v = 0; v < nv && ok; ++v) {
+          const int jb0 = v * Lay::kVTokens / BS;
+          const int jb1 = (min(n, (v + 1) * Lay::kVTokens) + BS - 1) / BS;
           const int slot = g % kStages;
           ok = sm100::mbar_wait(&c.empty[slot], ((g / kStages) & 1) ^ 1, budget, abort_flag);
           if (!ok) break;
-          if (lane == 0) sm100::mbar_arrive_expect_tx(&c.full[slot], (jb1 - jb0) * BS * 128);
+          // The stage holding the range end, when that end falls inside a
+          // 16-token MMA step, lands on the producer's own barrier first:
+          // the rows past the end are cleared (P^T is zero there, but 0 * NaN
+          // would be NaN) and only then is the stage handed to the MMA warp.
+          const bool tail = tail_fix && ci == nchunks - 1 && v == nv - 1;
+          uint64_t* land = tail ? &c.tail : &c.full[slot];
+          if (lane == 0) sm100::mbar_arrive_expect_tx(land, (jb1 - jb0) * BS * D * 2);
           for (int j = jb0; j < jb1; ++j) {
             const int32_t yj = __shfl_sync(0xffffffffu, y, j);
             if (lane == 0)
-              sm100::tma_load_2d(ring + slot * kStageBytes + (j - jb0) * BS * 128, &kmap,
-                                 &c.full[slot], sl * 64, yj);
+              sm100::tma_load_3d(ring + slot * kStageBytes + (j - jb0) * BS * D * 2, &vmap, land, 0,
+                                 yj, 0, stream_once);
           }
           ++g;
-        }
-      }
-      const int nv = (n + Lay::kVTokens - 1) / Lay::kVTokens;
-      for (int v = 0; v < nv && ok; ++v) {
-        const int jb0 = v * Lay::kVTokens / BS;
-        const int jb1 = (min(n, (v + 1) * Lay::kVTokens) + BS - 1) / BS;
-        const int slot = g % kStages;
-        const uint32_t par = (g / kStages) & 1;
-        ok = sm100::mbar_wait(&c.empty[slot], par ^ 1, budget, abort_flag);
-        if (!ok) break;
-        if (lane == 0) sm100::mbar_arrive_expect_tx(&c.full[slot], (jb1 - jb0) * BS * D * 2);
-        for (int j = jb0; j < jb1; ++j) {
-          const int32_t yj = __shfl_sync(0xffffffffu, y, j);
-          if (lane == 0)
-            sm100::tma_load_3d(ring + slot * kStageBytes + (j - jb0) * BS * D * 2, &vmap,
-                               &c.full[slot], 0, yj, 0);
-        }
-        ++g;
-        if (tail_fix && ci == nchunks - 1 && v == nv - 1) {
-          // Clear the value rows from the range end to the end of its
-          // 16-token step: P^T is zero there, but 0 * NaN would be NaN.
-          ok = sm100::mbar_wait(&c.full[slot], par, budget, abort_flag);
-          if (!ok) break;
-          const int r0 = n - v * Lay::kVTokens;  // first row past the end
-          const int r1 = (r0 + 15) / 16 * 16;    // end of its 16-token step
-          uint8_t* st = ring + slot * kStageBytes;
-          const int pieces = (r1 - r0) * Lay::kSlices * 8;  // 16-byte pieces
-          for (int i = lane; i < pieces; i += 32) {
-            const int line = i / 8, piece = i % 8;
-            const int r = r0 + line / Lay::kSlices, sl = line % Lay::kSlices;
-            *reinterpret_cast<uint4*>(st + (r / BS) * BS * D * 2 + sl * BS * 128 + (r % BS) * 128 +
-                                      piece * 16) = make_uint4(0u, 0u, 0u, 0u);
+          if (tail) {
+            tail_pending = slot;
+            ok = sm100::mbar_wait(&c.tail, tn & 1, budget, abort_flag);
+            if (!ok) break;
+            ++tn;
+            tail_pending = -1;
+            const int r0 = n - v * Lay::kVTokens;  // first row past the end
+            const int r1 = (r0 + 15) / 16 * 16;    // end of its 16-token step
+            uint8_t* st = ring + slot * kStageBytes;
+            const int pieces = (r1 - r0) * Lay::kSlices * 8;  // 16-byte pieces
+            for (int i = lane; i < pieces; i += 32) {
+              const int line = i / 8, piece = i % 8;
+              const int r = r0 + line / Lay::kSlices, sl = line % Lay::kSlices;
+              *reinterpret_cast<uint4*>(st + (r / BS) * BS * D * 2 + sl * BS * 128 +
+                                        (r % BS) * 128 + piece * 16) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            sm100::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) sm100::mbar_arrive(&c.full[slot]);  // no bytes: the data is there
           }
-          sm100::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) sm100::mbar_arrive(&c.tail);
         }
       }
     }
@@ -280,7 +295,11 @@ __global__ void __launch_bounds__(tc::kThreads, 2)
       // Copies already issued must land before the CTA may exit: wait for
       // the newest use of every slot (older uses completed before it began).
       for (uint32_t gg = g > kStages ? g - kStages : 0; gg < g; ++gg)
-        sm100::mbar_wait(&c.full[gg % kStages], (gg / kStages) & 1, budget, nullptr);
+        if (static_cast<int>(gg % kStages) != tail_pending)
+          sm100::mbar_wait(&c.full[gg % kStages], (gg / kStages) & 1, budget, nullptr);
+      if (tail_pending >= 0) sm100::mbar_wait(&c.tail, tn & 1, budget, nullptr);
+      for (uint32_t qq = qn > 2 ? qn - 2 : 0; qq < qn; ++qq)
+        sm100::mbar_wait(&c.qfull[qq & 1], (qq >> 1) & 1, budget, nullptr);
     }
   } else if (warp == 5) {
     // ========================= MMA issuer =========================================
@@ -290,64 +309,73 @@ __global__ void __launch_bounds__(tc::kThreads, 2)
       const uint32_t q_base = sm100::smem_u32(qs);
       const uint32_t pt_base = sm100::smem_u32(pt);
       const uint32_t ring_base = sm100::smem_u32(ring);
-      uint32_t g = 0;
+      uint32_t g = 0, qn = 0, cc = 0;
       bool ok = true;
-      for (int ci = 0; ci < nchunks && ok; ++ci) {
-        const int c0 = t0 + ci * kChunk;
-        const int n = min(kChunk, t1 - c0);
-        const int nt = (n + kTile - 1) / kTile;
-        for (int tt = 0; tt < nt && ok; ++tt) {
-          for (int sl = 0; sl < Lay::kSlices; ++sl) {
+      for (int64_t k = blockIdx.x; k < total_items && ok; k += stride) {
+        const Item it = decode_item(a, k, kV2);
+        if (it.t0 >= it.t1) continue;
+        const int qb = qn & 1;
+        ok = sm100::mbar_wait(&c.qfull[qb], (qn >> 1) & 1, budget, abort_flag);
+        if (!ok) break;
+        ++qn;
+        const uint32_t qbuf = q_base + qb * Lay::kSlices * 1024;
+        const int nchunks = (it.t1 - it.t0 + kChunk - 1) / kChunk;
+        for (int ci = 0; ci < nchunks && ok; ++ci, ++cc) {
+          const int c0 = it.t0 + ci * kChunk;
+          const int n = min(kChunk, it.t1 - c0);
+          const int nt = (n + kTile - 1) / kTile;
+          for (int tt = 0; tt < nt && ok; ++tt) {
+            for (int sl = 0; sl < Lay::kSlices; ++sl) {
+              const int slot = g % kStages;
+              ok = sm100::mbar_wait(&c.full[slot], (g / kStages) & 1, budget, abort_flag);
+              if (!ok) break;
+              sm100::tc_fence_after();
+              const uint32_t st = ring_base + slot * kStageBytes;
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t ad = sm100::smem_desc(st + kk * 32, 16, 1024, sm100::kSw128);
+                const uint64_t bd =
+                    sm100::smem_desc(qbuf + sl * 1024 + kk * 32, 16, 1024, sm100::kSw128);
+                sm100::mma_f16(tmem + tt * 16, ad, bd, id_qk, (sl | kk) != 0);
+              }
+              sm100::mma_commit(&c.empty[slot]);
+              ++g;
+            }
+          }
+          if (!ok) break;
+          if (ci == nchunks - 1) sm100::mma_commit(&c.qempty[qb]);
+          sm100::mma_commit(&c.s_full);
+          ok = sm100::mbar_wait(&c.p_ready, cc & 1, budget, abort_flag);
+          if (!ok) break;
+          sm100::tc_fence_after();
+          const int nv = (n + Lay::kVTokens - 1) / Lay::kVTokens;
+          bool first = true;
+          for (int v = 0; v < nv; ++v) {
             const int slot = g % kStages;
             ok = sm100::mbar_wait(&c.full[slot], (g / kStages) & 1, budget, abort_flag);
             if (!ok) break;
             sm100::tc_fence_after();
             const uint32_t st = ring_base + slot * kStageBytes;
+            const int toks = min(Lay::kVTokens, n - v * Lay::kVTokens);
+            for (int r = 0; r < toks; r += 16) {
+              const int jb = r / BS, s0 = r % BS;
+              const uint64_t bd = sm100::smem_desc(pt_base + ((v * Lay::kVTokens + r) / 16) * 512,
+                                                   256, 128, sm100::kSwNone);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t ad = sm100::smem_desc(st + kk * 32, 16, 1024, sm100::kSw128);
-              const uint64_t bd =
-                  sm100::smem_desc(q_base + sl * 2048 + kk * 32, 16, 1024, sm100::kSw128);
-              sm100::mma_f16(tmem + tt * 16, ad, bd, id_qk, (sl | kk) != 0);
+              for (int j = 0; j < Lay::kHalves; ++j) {
+                const uint64_t ad =
+                    sm100::smem_desc(st + jb * BS * D * 2 + 2 * j * BS * 128 + s0 * 128, BS * 128,
+                                     1024, sm100::kSw128);
+                sm100::mma_f16(tmem + kOCol + 16 * j, ad, bd, id_pv, !first);
+              }
+              first = false;
             }
             sm100::mma_commit(&c.empty[slot]);
             ++g;
           }
-        }
-        if (!ok) break;
-        sm100::mma_commit(&c.s_full);
-        ok = sm100::mbar_wait(&c.p_ready, ci & 1, budget, abort_flag);
-        if (!ok) break;
-        sm100::tc_fence_after();
-        const int nv = (n + Lay::kVTokens - 1) / Lay::kVTokens;
-        bool first = true;
-        for (int v = 0; v < nv; ++v) {
-          const int slot = g % kStages;
-          if (tail_fix && ci == nchunks - 1 && v == nv - 1)
-            ok = sm100::mbar_wait(&c.tail, 0, budget, abort_flag);
-          else
-            ok = sm100::mbar_wait(&c.full[slot], (g / kStages) & 1, budget, abort_flag);
           if (!ok) break;
-          sm100::tc_fence_after();
-          const uint32_t st = ring_base + slot * kStageBytes;
-          const int toks = min(Lay::kVTokens, n - v * Lay::kVTokens);
-          for (int r = 0; r < toks; r += 16) {
-            const int jb = r / BS, s0 = r % BS;
-            const uint64_t bd = sm100::smem_desc(pt_base + ((v * Lay::kVTokens + r) / 16) * 512,
-                                                 256, 128, sm100::kSwNone);
-#pragma unroll
-            for (int j = 0; j < Lay::kHalves; ++j) {
-              const uint64_t ad = sm100::smem_desc(
-                  st + jb * BS * D * 2 + 2 * j * BS * 128 + s0 * 128, BS * 128, 1024, sm100::kSw128);
-              sm100::mma_f16(tmem + kOCol + 16 * j, ad, bd, id_pv, !first);
-            }
-            first = false;
-          }
-          sm100::mma_commit(&c.empty[slot]);
-          ++g;
+          sm100::mma_commit(&c.o_full);
         }
-        if (!ok) break;
-        sm100::mma_commit(&c.o_full);
       }
       if (!ok) {
         fail(c, a.status);
@@ -358,142 +386,178 @@ __global__ void __launch_bounds__(tc::kThreads, 2)
     }
     __syncwarp();
   } else {
-    // ========================= softmax + combine (warps 0-3) ======================
+    // ========================= softmax + epilogue (warps 0-3) =====================
     // Every softmax thread runs the same iterations and barriers whatever
     // happens; a failed wait only marks the abort, which ends later waits.
     const int r = tid;  // tensor-memory lane: token of a tile, or head_dim row
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     const float sl2 = a.scale_log2;
-    for (int ci = 0; ci < nchunks; ++ci) {
-      const int c0 = t0 + ci * kChunk;
-      const int n = min(kChunk, t1 - c0);
-      const int nt = (n + kTile - 1) / kTile;
-      const int n16 = (n + 15) / 16 * 16;
-      if (!sm100::mbar_wait(&c.s_full, ci & 1, budget, abort_flag)) fail(c, a.status);
-      sm100::tc_fence_after();
-      __syncwarp();
-      float mx[8];
-#pragma unroll
-      for (int h = 0; h < 8; ++h) mx[h] = -INFINITY;
-      for (int tt = 0; tt < nt; ++tt) {
-        float s[16];
-        sm100::tmem_ld16(tmem + lane_base + tt * 16, s);
-        sm100::tmem_wait_ld();
-        if (tt * kTile + r < n) {
-#pragma unroll
-          for (int h = 0; h < 8; ++h)
-            if (h < G) mx[h] = fmaxf(mx[h], s[h] * sl2);
+    uint32_t cc = 0;
+    for (int64_t k = blockIdx.x; k < total_items; k += stride) {
+      const Item it = decode_item(a, k, kV2);
+      const int64_t row0 = static_cast<int64_t>(it.b) * Hq + it.kvh * G;
+      if (it.t0 >= it.t1) {
+        if (!it.len_ok && it.part == 0 && it.kvh == 0 && tid == 0)
+          set_status(a.status, PA_ERR_BAD_SEQ_LEN);
+        if (!kV2) {  // V1 row of a sequence with nothing to attend to
+          const float v = it.len_ok ? 0.f : qnan();
+          for (int i = tid; i < G * D; i += 128) store_out(a.out, row0 * D + i, a.out_dtype, v);
         }
+        continue;
       }
+      const int32_t* bt = a.block_tables + static_cast<int64_t>(it.b) * a.max_blocks_per_seq;
+      float m_run[8], s_run[8], acc[Lay::kHalves][8];
 #pragma unroll
       for (int h = 0; h < 8; ++h) {
+        m_run[h] = -INFINITY;
+        s_run[h] = 0.f;
 #pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], o));
-        if (lane == 0) c.red[0][warp][h] = mx[h];
+        for (int j = 0; j < Lay::kHalves; ++j) acc[j][h] = 0.f;
       }
-      softmax_sync();
-      float mc[8];
+      bool bad = false;
+      const int nchunks = (it.t1 - it.t0 + kChunk - 1) / kChunk;
+      for (int ci = 0; ci < nchunks; ++ci, ++cc) {
+        const int c0 = it.t0 + ci * kChunk;
+        const int n = min(kChunk, it.t1 - c0);
+        const int nt = (n + kTile - 1) / kTile;
+        const int n16 = (n + 15) / 16 * 16;
+        {  // block ids of the chunk: any outside the pool poisons the item
+          const int nblk = (n + BS - 1) / BS;
+          bool bl = false;
+          if (lane < nblk) {
+            const int32_t id = __ldg(bt + c0 / BS + lane);
+            bl = id < 0 || id >= a.num_blocks;
+          }
+          bad |= __any_sync(0xffffffffu, bl);
+        }
+        if (!sm100::mbar_wait(&c.s_full, cc & 1, budget, abort_flag)) fail(c, a.status);
+        sm100::tc_fence_after();
+        __syncwarp();
+        float mx[8];
 #pragma unroll
-      for (int h = 0; h < 8; ++h)
-        mc[h] = fmaxf(fmaxf(c.red[0][0][h], c.red[0][1][h]), fmaxf(c.red[0][2][h], c.red[0][3][h]));
-      float sum[8];
+        for (int h = 0; h < 8; ++h) mx[h] = -INFINITY;
+        for (int tt = 0; tt < nt; ++tt) {
+          float s[16];
+          sm100::tmem_ld16(tmem + lane_base + tt * 16, s);
+          sm100::tmem_wait_ld();
+          if (tt * kTile + r < n) {
 #pragma unroll
-      for (int h = 0; h < 8; ++h) sum[h] = 0.f;
-      for (int tt = 0; tt < nt; ++tt) {
-        float s[16];
-        sm100::tmem_ld16(tmem + lane_base + tt * 16, s);
-        sm100::tmem_wait_ld();
-        const int tok = tt * kTile + r;
-        if (tok < n16) {
-          const bool valid = tok < n;
-          // P^T element (tok, col): step tok/16, core (tok%16)/8, column group
-          // col/8, column col%8, token tok%8 -- no-swizzle K-major core matrices
-          uint8_t* dst = pt + (tok / 16) * 512 + ((tok % 16) / 8) * 256 + (tok % 8) * 2;
-#pragma unroll
-          for (int h = 0; h < 8; ++h) {
-            float p = 0.f;
-            if (valid && h < G) p = exp2f(s[h] * sl2 - mc[h]);
-            sum[h] += p;
-            const T hi = round16(p, static_cast<T*>(nullptr));
-            const T lo = round16(p - to_float(hi), static_cast<T*>(nullptr));
-            *reinterpret_cast<uint16_t*>(dst + h * 16) = bits16(hi);
-            *reinterpret_cast<uint16_t*>(dst + 128 + h * 16) = bits16(lo);
+            for (int h = 0; h < 8; ++h)
+              if (h < G) mx[h] = fmaxf(mx[h], s[h] * sl2);
           }
         }
-      }
 #pragma unroll
-      for (int h = 0; h < 8; ++h) {
+        for (int h = 0; h < 8; ++h) {
 #pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) sum[h] += __shfl_xor_sync(0xffffffffu, sum[h], o);
-        if (lane == 0) c.red[1][warp][h] = sum[h];
-      }
-      sm100::fence_proxy_async_smem();
-      sm100::tc_fence_before();
-      sm100::mbar_arrive(&c.p_ready);
-      softmax_sync();
-      float f_old[8], f_new[8];
+          for (int o = 16; o >= 1; o >>= 1)
+            mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], o));
+          if (lane == 0) c.red[0][warp][h] = mx[h];
+        }
+        softmax_sync();
+        float mc[8];
 #pragma unroll
-      for (int h = 0; h < 8; ++h) {
-        const float sc = (c.red[1][0][h] + c.red[1][1][h]) + (c.red[1][2][h] + c.red[1][3][h]);
-        const float m_new = fmaxf(m_run[h], mc[h]);
-        f_old[h] = m_run[h] == -INFINITY ? 0.f : exp2f(m_run[h] - m_new);
-        f_new[h] = mc[h] == -INFINITY ? 0.f : exp2f(mc[h] - m_new);
-        s_run[h] = s_run[h] * f_old[h] + sc * f_new[h];
-        m_run[h] = m_new;
+        for (int h = 0; h < 8; ++h)
+          mc[h] = fmaxf(fmaxf(c.red[0][0][h], c.red[0][1][h]), fmaxf(c.red[0][2][h], c.red[0][3][h]));
+        float sum[8];
+#pragma unroll
+        for (int h = 0; h < 8; ++h) sum[h] = 0.f;
+        for (int tt = 0; tt < nt; ++tt) {
+          float s[16];
+          sm100::tmem_ld16(tmem + lane_base + tt * 16, s);
+          sm100::tmem_wait_ld();
+          const int tok = tt * kTile + r;
+          if (tok < n16) {
+            const bool valid = tok < n;
+            // P^T element (tok, col): 16-token step, 8-token core, column
+            // group col / 8, column col % 8, token tok % 8 (no-swizzle
+            // K-major core matrices of 8 x 16 bytes)
+            uint8_t* dst = pt + (tok / 16) * 512 + ((tok % 16) / 8) * 256 + (tok % 8) * 2;
+#pragma unroll
+            for (int h = 0; h < 8; ++h) {
+              float p = 0.f;
+              if (valid && h < G) p = exp2f(s[h] * sl2 - mc[h]);
+              sum[h] += p;
+              const T hi = round16(p, static_cast<T*>(nullptr));
+              const T lo = round16(p - to_float(hi), static_cast<T*>(nullptr));
+              *reinterpret_cast<uint16_t*>(dst + h * 16) = bits16(hi);
+              *reinterpret_cast<uint16_t*>(dst + 128 + h * 16) = bits16(lo);
+            }
+          }
+        }
+#pragma unroll
+        for (int h = 0; h < 8; ++h) {
+#pragma unroll
+          for (int o = 16; o >= 1; o >>= 1) sum[h] += __shfl_xor_sync(0xffffffffu, sum[h], o);
+          if (lane == 0) c.red[1][warp][h] = sum[h];
+        }
+        sm100::fence_proxy_async_smem();
+        sm100::tc_fence_before();
+        sm100::mbar_arrive(&c.p_ready);
+        softmax_sync();
+        float f_old[8], f_new[8];
+#pragma unroll
+        for (int h = 0; h < 8; ++h) {
+          const float sc = (c.red[1][0][h] + c.red[1][1][h]) + (c.red[1][2][h] + c.red[1][3][h]);
+          const float m_new = fmaxf(m_run[h], mc[h]);
+          f_old[h] = m_run[h] == -INFINITY ? 0.f : exp2f(m_run[h] - m_new);
+          f_new[h] = mc[h] == -INFINITY ? 0.f : exp2f(mc[h] - m_new);
+          s_run[h] = s_run[h] * f_old[h] + sc * f_new[h];
+          m_run[h] = m_new;
+        }
+        if (!sm100::mbar_wait(&c.o_full, cc & 1, budget, abort_flag)) fail(c, a.status);
+        sm100::tc_fence_after();
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < Lay::kHalves; ++j) {
+          float o[16];
+          sm100::tmem_ld16(tmem + lane_base + kOCol + 16 * j, o);
+          sm100::tmem_wait_ld();
+#pragma unroll
+          for (int h = 0; h < 8; ++h)
+            acc[j][h] = acc[j][h] * f_old[h] + (o[h] + o[8 + h]) * f_new[h];
+        }
+        sm100::tc_fence_before();
       }
-      if (!sm100::mbar_wait(&c.o_full, ci & 1, budget, abort_flag)) fail(c, a.status);
-      sm100::tc_fence_after();
-      __syncwarp();
+      // ---- epilogue of the item ------------------------------------------------
+      const bool poison = bad || *abort_flag != 0;
 #pragma unroll
       for (int j = 0; j < Lay::kHalves; ++j) {
-        float o[16];
-        sm100::tmem_ld16(tmem + lane_base + kOCol + 16 * j, o);
-        sm100::tmem_wait_ld();
+        const int d = j * 128 + tid;
 #pragma unroll
-        for (int h = 0; h < 8; ++h) acc[j][h] = acc[j][h] * f_old[h] + (o[h] + o[8 + h]) * f_new[h];
+        for (int h = 0; h < 8; ++h) {
+          if (h >= G) break;
+          const float o = poison ? qnan() : acc[j][h] / s_run[h];
+          if constexpr (kV2)
+            a.tmp_out[((row0 + h) * a.num_partitions + it.part) * D + d] = o;
+          else
+            store_out(a.out, (row0 + h) * D + d, a.out_dtype, o);
+        }
       }
-      sm100::tc_fence_before();
+      if (kV2 && tid < G) {
+        const int64_t w = (row0 + tid) * a.num_partitions + it.part;
+        float m = m_run[0], s = s_run[0];
+#pragma unroll
+        for (int h = 1; h < 8; ++h)
+          if (h == tid) {
+            m = m_run[h];
+            s = s_run[h];
+          }
+        a.max_logits[w] = poison ? qnan() : m * kLn2;
+        a.exp_sums[w] = s;
+      }
     }
   }
 
-  // ---- epilogue ---------------------------------------------------------------
+  // ---- teardown -------------------------------------------------------------------
   sm100::tc_fence_before();
   __syncthreads();
   sm100::tc_fence_after();
   if (warp == 5) sm100::tmem_dealloc(tmem, kTmemCols);
-  if (warp < 4) {
-    const bool poison = c.bad != 0 || c.abort != 0;
-#pragma unroll
-    for (int j = 0; j < Lay::kHalves; ++j) {
-      const int d = j * 128 + tid;
-#pragma unroll
-      for (int h = 0; h < 8; ++h) {
-        if (h >= G) break;
-        const float o = poison ? qnan() : acc[j][h] / s_run[h];
-        if constexpr (kV2)
-          a.tmp_out[((row0 + h) * a.num_partitions + part) * D + d] = o;
-        else
-          store_out(a.out, (row0 + h) * D + d, a.out_dtype, o);
-      }
-    }
-    if (kV2 && tid < G) {
-      const int64_t w = (row0 + tid) * a.num_partitions + part;
-      float m = m_run[0], s = s_run[0];
-#pragma unroll
-      for (int h = 1; h < 8; ++h)
-        if (h == tid) {
-          m = m_run[h];
-          s = s_run[h];
-        }
-      a.max_logits[w] = poison ? qnan() : m * kLn2;
-      a.exp_sums[w] = s;
-    }
-  }
 }
 
 template <typename T, int D, int BS>
 cudaError_t launch_tc_t(const KernelArgs& a, const CUtensorMap& km, const CUtensorMap& vm,
-                        bool v2, cudaStream_t s) {
+                        const CUtensorMap& qm, bool v2, int num_sms, cudaStream_t s) {
   static bool configured[2][128] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -505,19 +569,28 @@ cudaError_t launch_tc_t(const KernelArgs& a, const CUtensorMap& km, const CUtens
     if (e != cudaSuccess) return e;
     configured[v2][dev] = true;
   }
-  const dim3 grid(v2 ? a.num_partitions : 1, a.num_kv_heads, a.num_seqs);
-  kern<<<grid, tc::kThreads, smem, s>>>(a, km, vm, tc::kDefaultWaitBudget);
+  const int64_t items = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads *
+                        (v2 ? a.num_partitions : 1);
+  const int64_t slots = static_cast<int64_t>(num_sms) * tc::kCtasPerSm;
+  const unsigned grid = static_cast<unsigned>(items < slots ? items : slots);
+  if (grid == 0) return cudaSuccess;
+  kern<<<grid, tc::kThreads, smem, s>>>(a, km, vm, qm, items, tc::kDefaultWaitBudget);
   return cudaGetLastError();
 }
 
 template <typename T>
 cudaError_t launch_tc_dtype(const KernelArgs& a, const CUtensorMap& km, const CUtensorMap& vm,
-                            bool v2, cudaStream_t s) {
-  if (a.head_dim == 256 && a.block_size == 16) return launch_tc_t<T, 256, 16>(a, km, vm, v2, s);
-  if (a.head_dim == 256 && a.block_size == 32) return launch_tc_t<T, 256, 32>(a, km, vm, v2, s);
-  if (a.head_dim == 128 && a.block_size == 16) return launch_tc_t<T, 128, 16>(a, km, vm, v2, s);
-  if (a.head_dim == 128 && a.block_size == 32) return launch_tc_t<T, 128, 32>(a, km, vm, v2, s);
-  if (a.head_dim == 128 && a.block_size == 64) return launch_tc_t<T, 128, 64>(a, km, vm, v2, s);
+                            const CUtensorMap& qm, bool v2, int num_sms, cudaStream_t s) {
+  if (a.head_dim == 256 && a.block_size == 16)
+    return launch_tc_t<T, 256, 16>(a, km, vm, qm, v2, num_sms, s);
+  if (a.head_dim == 256 && a.block_size == 32)
+    return launch_tc_t<T, 256, 32>(a, km, vm, qm, v2, num_sms, s);
+  if (a.head_dim == 128 && a.block_size == 16)
+    return launch_tc_t<T, 128, 16>(a, km, vm, qm, v2, num_sms, s);
+  if (a.head_dim == 128 && a.block_size == 32)
+    return launch_tc_t<T, 128, 32>(a, km, vm, qm, v2, num_sms, s);
+  if (a.head_dim == 128 && a.block_size == 64)
+    return launch_tc_t<T, 128, 64>(a, km, vm, qm, v2, num_sms, s);
   return cudaErrorInvalidValue;
 }
 

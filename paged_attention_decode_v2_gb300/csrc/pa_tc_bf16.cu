@@ -5,8 +5,8 @@
 namespace pa {
 
 cudaError_t launch_tc_bf16(const KernelArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                         bool v2, cudaStream_t s) {
-  return launch_tc_dtype<__nv_bfloat16>(a, kmap, vmap, v2, s);
+                         const CUtensorMap& qmap, bool v2, int num_sms, cudaStream_t s) {
+  return launch_tc_dtype<__nv_bfloat16>(a, kmap, vmap, qmap, v2, num_sms, s);
 }
 
 }  // namespace pa

@@ -6,8 +6,9 @@
 // block_size + slot.  Keys use a 2-D map (head_dim, rows) with a 64 x
 // block_size box, so one copy brings one 64-element slice of one block;
 // values use a 3-D map (64, rows, head_dim / 64) whose box is a whole block
-// laid out slice-major.  Both use the 128-byte swizzle the MMA descriptors
-// expect.
+// laid out slice-major; q is viewed as (head_dim, num_seqs * num_heads)
+// rows with an 8-row box (one KV head's query rows).  All use the 128-byte
+// swizzle the MMA descriptors expect.
 #include <mutex>
 
 #include <cuda.h>
@@ -18,9 +19,9 @@
 namespace pa {
 
 cudaError_t launch_tc_bf16(const KernelArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                           bool v2, cudaStream_t s);
+                           const CUtensorMap& qmap, bool v2, int num_sms, cudaStream_t s);
 cudaError_t launch_tc_f16(const KernelArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                          bool v2, cudaStream_t s);
+                          const CUtensorMap& qmap, bool v2, int num_sms, cudaStream_t s);
 
 namespace {
 
@@ -38,17 +39,25 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   return fn;
 }
 
-// 1 if the current device runs the sm_100-family tensor-core kernels.
-bool device_has_tcgen05() {
-  static int cache[128] = {};  // 0 unknown, 1 yes, 2 no
+struct DeviceInfo {
+  int state = 0;  // 0 unknown, 1 runs the sm_100-family kernels, 2 does not
+  int num_sms = 0;
+};
+
+const DeviceInfo& device_info() {
+  static DeviceInfo cache[128];
+  static const DeviceInfo none;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return false;
-  if (!cache[dev]) {
-    int major = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return none;
+  DeviceInfo& d = cache[dev];
+  if (!d.state) {
+    int major = 0, sms = 0;
     cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
-    cache[dev] = major == 10 ? 1 : 2;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    d.num_sms = sms;
+    d.state = (major == 10 && sms > 0) ? 1 : 2;
   }
-  return cache[dev] == 1;
+  return d;
 }
 
 }  // namespace
@@ -63,7 +72,8 @@ bool tc_applicable(const pa_params_t* p) {
   if (!shape) return false;
   const int64_t rows = static_cast<int64_t>(p->num_blocks) * p->num_kv_heads * BS;
   if (rows + BS >= (int64_t(1) << 31)) return false;  // TMA row coordinates are int32
-  return encoder() != nullptr && device_has_tcgen05();
+  if (static_cast<int64_t>(p->num_seqs) * p->num_heads + 8 >= (int64_t(1) << 31)) return false;
+  return encoder() != nullptr && device_info().state == 1;
 }
 
 cudaError_t launch_tc(const KernelArgs& a, pa_dtype_t kv, bool v2, cudaStream_t s) {
@@ -95,7 +105,20 @@ cudaError_t launch_tc(const KernelArgs& a, pa_dtype_t kv, bool v2, cudaStream_t 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  return kv == PA_BF16 ? launch_tc_bf16(a, kmap, vmap, v2, s) : launch_tc_f16(a, kmap, vmap, v2, s);
+  CUtensorMap qmap;
+  {
+    const cuuint64_t dims[2] = {D, static_cast<cuuint64_t>(a.num_seqs) * a.num_heads};
+    const cuuint64_t strides[1] = {D * 2};
+    const cuuint32_t box[2] = {64, 8};
+    const cuuint32_t es[2] = {1, 1};
+    if (enc(&qmap, dt, 2, const_cast<void*>(a.q), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  const int sms = device_info().num_sms;
+  return kv == PA_BF16 ? launch_tc_bf16(a, kmap, vmap, qmap, v2, sms, s)
+                       : launch_tc_f16(a, kmap, vmap, qmap, v2, sms, s);
 }
 
 }  // namespace pa

@@ -11,9 +11,12 @@ TOL = {torch.float32: 1e-5, torch.bfloat16: 2e-3, torch.float16: 2e-3}
 
 
 def run(batch, path="decode", partition_size=512, portable=False, out_dtype=torch.float32,
-        v1_max_seq_len=pa.DEFAULT_V1_MAX_SEQ_LEN, workspace=None, return_ws=False):
+        v1_max_seq_len=pa.DEFAULT_V1_MAX_SEQ_LEN, workspace=None, return_ws=False,
+        check_status=True):
     """Run one decode step of ``batch`` (already on the GPU); returns out as a
-    float64 numpy array (and the workspace tensor when asked)."""
+    float64 numpy array (and the workspace tensor when asked).  When a
+    workspace was used, its device status word must read OK afterwards
+    (unless ``check_status`` is False)."""
     b = batch
     out = torch.full(tuple(b.q.shape), float("nan"), dtype=out_dtype, device=b.q.device)
     params = pa.make_params(b.q, b.k_cache, b.block_tables, max_seq_len=b.max_seq_len,
@@ -34,6 +37,9 @@ def run(batch, path="decode", partition_size=512, portable=False, out_dtype=torc
         pa.decode(b.q, b.k_cache, b.v_cache, b.block_tables, b.seq_lens, out, workspace,
                   partition_size=partition_size, v1_max_seq_len=v1_max_seq_len, **kw)
     torch.cuda.synchronize()
+    if check_status and workspace is not None and path in ("v2", "decode"):
+        st = pa.read_device_status(workspace, clear=False)
+        assert st == pa.PA_OK, f"device status {st}: {pa.status_string(st)}"
     res = out.double().cpu().numpy()
     return (res, workspace) if return_ws else res
 

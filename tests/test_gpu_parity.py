@@ -204,7 +204,7 @@ def test_bad_block_id_poisons_the_row_and_sets_status():
     bg = bc.to("cuda")
     for path, portable in PATH_MODES:
         got, ws = run(bg, path="v2" if path == "v2" else "v1", portable=portable,
-                      partition_size=32, return_ws=True)
+                      partition_size=32, return_ws=True, check_status=False)
         assert np.all(np.isnan(got[1])), path
         assert_close(got[0], ref[0], 2e-3, "untouched row")
         if path == "v2":
@@ -218,7 +218,8 @@ def test_bad_seq_len_poisons_the_row_and_sets_status():
     bg.seq_lens[1] = 61                                       # > max_seq_len promised
     ref = _ref(bc)
     for path, portable in PATH_MODES:
-        got, ws = run(bg, path=path, portable=portable, partition_size=32, return_ws=True)
+        got, ws = run(bg, path=path, portable=portable, partition_size=32, return_ws=True,
+                      check_status=False)
         assert np.all(np.isnan(got[1])), path
         assert_close(got[0], ref[0], 2e-3, "untouched row")
         if path == "v2":
