@@ -50,7 +50,10 @@ L2_FLUSH_BYTES = 256 << 20
 # DRAM bytes (read + write) per launch of the dominant kernel, from one ncu
 # capture, keyed by a hash of the kernel sources it was taken on.  A source
 # change makes the figure stale, and the bench then reports null.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # (kernel source hash, workload, partition size): bytes per launch
+    ("589e810ec5dc24a8", "long_100k", 512): 409_728_256 + 4_928_000,
+}
 
 
 def kernel_source_hash() -> str:
@@ -154,7 +157,10 @@ def run_ours(args, rank, world, device):
     params = pa.make_params(batch.q, batch.k_cache, batch.block_tables,
                             max_seq_len=batch.max_seq_len, scale=batch.scale, partition_size=P,
                             out_dtype=torch.float32)
-    path = pa.decode_path(params)
+    path = pa.decode_path(params) if args.path == "decode" else (1 if args.path == "v1" else 2)
+    family = pa.decode_kernel(params)
+    kname = ("pa_tc_kernel" if family == 2 else "pa_generic_kernel") + \
+        (" (V2 pass 1)" if path == 2 else " (V1)")
     ws = pa.alloc_workspace(params, device=device)
     out = torch.empty(tuple(batch.q.shape), dtype=torch.float32, device=device)
     flush_buf = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=device)
@@ -170,8 +176,15 @@ def run_ours(args, rank, world, device):
     kw = dict(max_seq_len=batch.max_seq_len, scale=batch.scale, partition_size=P)
 
     def step():
-        pa.decode(batch.q, batch.k_cache, batch.v_cache, batch.block_tables, batch.seq_lens, out,
-                  ws, **kw)
+        if args.path == "decode":
+            pa.decode(batch.q, batch.k_cache, batch.v_cache, batch.block_tables, batch.seq_lens,
+                      out, ws, **kw)
+        elif args.path == "v1":
+            pa.decode_v1(batch.q, batch.k_cache, batch.v_cache, batch.block_tables,
+                         batch.seq_lens, out, max_seq_len=batch.max_seq_len, scale=batch.scale)
+        else:
+            pa.decode_v2(batch.q, batch.k_cache, batch.v_cache, batch.block_tables,
+                         batch.seq_lens, out, ws, **kw)
 
     kv_bytes = batch.kv_bytes()
     alg_bytes = kv_bytes + batch.q_bytes()
@@ -238,7 +251,13 @@ def run_ours(args, rank, world, device):
         q_d.copy_(q_h, non_blocking=True)
         bt_d.copy_(bt_h, non_blocking=True)
         sl_d.copy_(sl_h, non_blocking=True)
-        pa.decode(q_d, batch.k_cache, batch.v_cache, bt_d, sl_d, out, ws, **kw)
+        if args.path == "v1":
+            pa.decode_v1(q_d, batch.k_cache, batch.v_cache, bt_d, sl_d, out,
+                         max_seq_len=batch.max_seq_len, scale=batch.scale)
+        elif args.path == "v2":
+            pa.decode_v2(q_d, batch.k_cache, batch.v_cache, bt_d, sl_d, out, ws, **kw)
+        else:
+            pa.decode(q_d, batch.k_cache, batch.v_cache, bt_d, sl_d, out, ws, **kw)
         out_h.copy_(out, non_blocking=True)
         torch.cuda.synchronize(device)
         if i >= args.warmup:
@@ -281,7 +300,8 @@ def run_ours(args, rank, world, device):
                         f"{w.num_heads} q / {w.num_kv_heads} kv heads, head_dim {w.head_dim}, "
                         f"{str(w.dtype).replace('torch.', '')} KV, block {w.block_size}",
             "partition_size": P,
-            "path": "V2 (partition kernel + LSE reduce)" if path == 2 else "V1 single pass",
+            "path": ("V2 (partition kernel + LSE reduce)" if path == 2 else "V1 single pass") +
+                    (" via pa_decode" if args.path == "decode" else " forced"),
             "accumulate": "f32",
             "l2": f"inputs larger than L2 (KV {kv_bytes / 1e6:.1f} MB > 129 MB), and a 256 MiB "
                   "read sweep evicts L2 before every timed step",
@@ -291,7 +311,7 @@ def run_ours(args, rank, world, device):
         "hbm_frac_of_step": round(alg_bytes / (t_step * 1e-3) / 1e9 / peak, 4),
         "roofline": {
             "bound": "hbm",
-            "kernel": "pa_generic_kernel (V2 pass 1)" if path == 2 else "pa_generic_kernel (V1)",
+            "kernel": kname,
             "achieved": round(achieved, 1),
             "peak": peak,
             "peak_source": f"{peak_kind} hbm_gbs (copy)",
@@ -385,6 +405,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="long_100k", choices=sorted(wl.WORKLOADS))
     ap.add_argument("--partition-size", type=int, default=0)
+    ap.add_argument("--path", choices=("decode", "v1", "v2"), default="decode",
+                    help="pa_decode (threshold dispatch), or force V1 / V2")
     ap.add_argument("--cpu-rows", type=int, default=24,
                     help="query-head rows the CPU baseline computes")
     ap.add_argument("--ref-tokens", type=int, default=4096,

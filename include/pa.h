@@ -210,6 +210,14 @@ PA_API pa_status_t pa_decode_v2_static(const pa_params_t* params, const void* q,
  * the parameters are invalid.  Pure host function. */
 PA_API int pa_decode_path(const pa_params_t* params);
 
+/* Which kernels the decode calls use for these parameters on the current
+ * device: 2 = tensor-core kernels (TMA + tcgen05; bf16 / f16 caches, at most
+ * 8 query heads per KV head, head_dim 128 or 256 with block_size 16 or 32,
+ * or head_dim 128 with block_size 64), 1 = CUDA-core kernels (every other
+ * valid case, or PA_FLAG_PORTABLE), 0 = invalid parameters.  Host function;
+ * it queries the current device's compute capability. */
+PA_API int pa_decode_kernel(const pa_params_t* params);
+
 /* Static description of a status code (never NULL). */
 PA_API const char* pa_status_string(pa_status_t status);
 

@@ -36,7 +36,8 @@ DEFAULT_V1_MAX_SEQ_LEN = 8192
 # Every symbol include/pa.h declares.
 EXPORTS = ("pa_workspace_size", "pa_decode_v1", "pa_decode_v2", "pa_decode_v2_partitions",
            "pa_decode_v2_reduce", "pa_decode", "pa_decode_path", "pa_status_string",
-           "pa_workspace_init", "pa_read_device_status", "pa_version", "pa_decode_v2_static")
+           "pa_workspace_init", "pa_read_device_status", "pa_version", "pa_decode_v2_static",
+           "pa_decode_kernel")
 PA_STATIC_WORKSPACE_BYTES = 16 << 20
 
 
@@ -94,6 +95,8 @@ def lib() -> ctypes.CDLL:
             L.pa_decode_v2_reduce.restype = ctypes.c_int
             L.pa_decode.argtypes = [PP, P, P, P, P, P, P, ctypes.c_size_t, P, P]
             L.pa_decode.restype = ctypes.c_int
+            L.pa_decode_kernel.argtypes = [PP]
+            L.pa_decode_kernel.restype = ctypes.c_int
             L.pa_decode_path.argtypes = [PP]
             L.pa_decode_path.restype = ctypes.c_int
             L.pa_status_string.argtypes = [ctypes.c_int]
@@ -142,6 +145,11 @@ def workspace_size(params: Params) -> int:
 
 def decode_path(params: Params) -> int:
     return int(lib().pa_decode_path(ctypes.byref(params)))
+
+
+def decode_kernel(params: Params) -> int:
+    """2: tensor-core kernels, 1: CUDA-core kernels, 0: invalid parameters."""
+    return int(lib().pa_decode_kernel(ctypes.byref(params)))
 
 
 def _stream(stream):

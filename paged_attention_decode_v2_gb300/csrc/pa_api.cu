@@ -227,6 +227,11 @@ pa_status_t pa_decode(const pa_params_t* p, const void* q, const void* k_cache,
   return pa_decode_v1(p, q, k_cache, v_cache, block_tables, seq_lens, out, stream);
 }
 
+int pa_decode_kernel(const pa_params_t* p) {
+  if (check_params(p, false) != PA_OK) return 0;
+  return tc_applicable(p) ? 2 : 1;
+}
+
 const char* pa_status_string(pa_status_t s) {
   switch (s) {
     case PA_OK: return "ok";

@@ -157,3 +157,13 @@ def test_workspace_helpers_check_arguments(L):
     v = ctypes.c_int32(0)
     assert L.pa_read_device_status(V(0), ctypes.byref(v), 0, V(0)) == pa.PA_ERR_INVALID_ARG
     assert L.pa_version() >= 100
+
+
+def test_decode_kernel_query(L):
+    # 0 for invalid parameters; the CUDA-core family whenever asked for, or
+    # for float32 caches; otherwise whatever the device supports
+    assert pa.decode_kernel(params(num_kv_heads=5)) == 0
+    assert pa.decode_kernel(params(flags=pa.PA_FLAG_PORTABLE)) == 1
+    assert pa.decode_kernel(params(kv_dtype=pa.PA_F32)) == 1
+    assert pa.decode_kernel(params(num_heads=36, num_kv_heads=4)) == 1   # group 9 > 8
+    assert pa.decode_kernel(params()) in (1, 2)
