@@ -65,6 +65,18 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
+def max_over_ranks(values, world, device=None):
+    """Element-wise max of `values` over all ranks (identity when world == 1).
+    The tensor lives on `device` for NCCL and on the CPU for gloo."""
+    if world <= 1:
+        return list(values)
+    dist = torch.distributed
+    on_cpu = dist.get_backend() == "gloo" or device is None
+    t = torch.tensor(values, dtype=torch.float64, device="cpu" if on_cpu else device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
 def measured_hbm_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -271,13 +283,9 @@ def run_ours(args, rank, world, device):
     assert torch.isfinite(out).all().item(), "non-finite output"
 
     # reduce over ranks: max of times
-    t_step = statistics.mean(step_ms)
-    t_dom = statistics.mean(dom_ms)
-    t_e2e = statistics.mean(e2e_s) * 1e3
-    if world > 1:
-        tt = torch.tensor([t_step, t_dom, t_e2e], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        t_step, t_dom, t_e2e = tt.tolist()
+    t_step, t_dom, t_e2e = max_over_ranks(
+        [statistics.mean(step_ms), statistics.mean(dom_ms), statistics.mean(e2e_s) * 1e3], world,
+        device)
 
     peak, peak_kind = measured_hbm_peak()
     achieved = alg_bytes / (t_dom * 1e-3) / 1e9

@@ -31,6 +31,7 @@ PA_ERR_BAD_SEQ_LEN = 8
 
 PA_F32, PA_BF16, PA_F16 = 0, 1, 2
 PA_FLAG_PORTABLE = 1
+PA_FLAG_SELFTEST_STALL = 2
 DEFAULT_V1_MAX_SEQ_LEN = 8192
 
 # Every symbol include/pa.h declares.
@@ -126,7 +127,8 @@ def _dtype_code(dtype) -> int:
 
 def make_params(q, k_cache, block_tables, *, max_seq_len: int, scale: float,
                 partition_size: int = 512, out_dtype=None,
-                v1_max_seq_len: int = DEFAULT_V1_MAX_SEQ_LEN, portable: bool = False) -> Params:
+                v1_max_seq_len: int = DEFAULT_V1_MAX_SEQ_LEN, portable: bool = False,
+                flags: int = 0) -> Params:
     """Fill a :class:`Params` from tensor shapes (no device access)."""
     num_seqs, num_heads, head_dim = q.shape
     num_blocks, num_kv_heads, block_size, d2 = k_cache.shape
@@ -136,7 +138,7 @@ def make_params(q, k_cache, block_tables, *, max_seq_len: int, scale: float,
                   block_tables.shape[1], int(max_seq_len), int(partition_size),
                   int(v1_max_seq_len), _dtype_code(k_cache.dtype),
                   _dtype_code(out_dtype if out_dtype is not None else q.dtype), float(scale),
-                  PA_FLAG_PORTABLE if portable else 0)
+                  (PA_FLAG_PORTABLE if portable else 0) | int(flags))
 
 
 def workspace_size(params: Params) -> int:
@@ -179,10 +181,10 @@ def _check_inputs(q, k_cache, v_cache, block_tables, seq_lens, out):
 
 
 def _params_for(q, k_cache, block_tables, out, max_seq_len, scale, partition_size,
-                v1_max_seq_len, portable):
+                v1_max_seq_len, portable, flags=0):
     return make_params(q, k_cache, block_tables, max_seq_len=max_seq_len, scale=scale,
                        partition_size=partition_size, out_dtype=out.dtype,
-                       v1_max_seq_len=v1_max_seq_len, portable=portable)
+                       v1_max_seq_len=v1_max_seq_len, portable=portable, flags=flags)
 
 
 def decode_v1(q, k_cache, v_cache, block_tables, seq_lens, out, *, max_seq_len: int,
@@ -199,7 +201,8 @@ def decode_v1(q, k_cache, v_cache, block_tables, seq_lens, out, *, max_seq_len: 
 
 
 def decode_v2(q, k_cache, v_cache, block_tables, seq_lens, out, workspace, *, max_seq_len: int,
-              scale: float, partition_size: int = 512, portable: bool = False, stream=None):
+              scale: float, partition_size: int = 512, portable: bool = False, stream=None,
+              flags: int = 0):
     """``pa_decode_v2``: split-KV pass 1 + log-sum-exp reduce, into ``out``.
 
     ``workspace`` is a CUDA uint8 tensor of at least :func:`workspace_size`
@@ -207,7 +210,7 @@ def decode_v2(q, k_cache, v_cache, block_tables, seq_lens, out, workspace, *, ma
     """
     _check_inputs(q, k_cache, v_cache, block_tables, seq_lens, out)
     p = _params_for(q, k_cache, block_tables, out, max_seq_len, scale, partition_size,
-                    DEFAULT_V1_MAX_SEQ_LEN, portable)
+                    DEFAULT_V1_MAX_SEQ_LEN, portable, flags)
     st = lib().pa_decode_v2(ctypes.byref(p), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                             _ptr(block_tables), _ptr(seq_lens), _ptr(workspace),
                             workspace.numel() * workspace.element_size(), _ptr(out),

@@ -35,6 +35,7 @@ struct KernelArgs {
   int32_t group;           // G = num_heads / num_kv_heads
   int32_t out_dtype;       // pa_dtype_t
   float scale_log2;        // scale * log2(e): logits are kept in base-2 units
+  int32_t selftest_stall;  // PA_FLAG_SELFTEST_STALL was given
 };
 
 // Launchers return cudaSuccess or the launch error.

@@ -60,6 +60,7 @@ constexpr int kTmemCols = 128;        // S: 4 tiles x 16 columns, O^T: 2 x 16
 constexpr int kOCol = 64;             // first tensor-memory column of O^T
 constexpr int kCtasPerSm = 2;
 constexpr long long kDefaultWaitBudget = 4000000000LL;  // cycles (about 2 s)
+constexpr long long kSelftestWaitBudget = 20000000LL;   // cycles (about 10 ms)
 
 template <int D>
 struct Layout {
@@ -83,6 +84,7 @@ struct Ctrl {
   uint64_t o_full;          // chunk O^T ready in tensor memory
   uint64_t tail;            // producer-private: a tail value stage landed
   uint64_t drain;           // abort path: all issued MMAs finished
+  uint64_t never;           // self-test: nothing ever arrives here
   uint32_t tmem;
   int abort;                // some wait gave up
   float red[2][4][8];       // cross-warp max / sum of the softmax warps
@@ -169,6 +171,7 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
     sm100::mbar_init(&c.o_full, 1);
     sm100::mbar_init(&c.tail, 1);
     sm100::mbar_init(&c.drain, 1);
+    sm100::mbar_init(&c.never, 1);
     c.abort = 0;
   }
   if (warp == 5) {
@@ -311,6 +314,9 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
       const uint32_t ring_base = sm100::smem_u32(ring);
       uint32_t g = 0, qn = 0, cc = 0;
       bool ok = true;
+      // diagnostic: wait for an event that never happens, so the bounded
+      // wait runs out and the abort path is exercised
+      if (a.selftest_stall) ok = sm100::mbar_wait(&c.never, 0, budget, abort_flag);
       for (int64_t k = blockIdx.x; k < total_items && ok; k += stride) {
         const Item it = decode_item(a, k, kV2);
         if (it.t0 >= it.t1) continue;
@@ -574,7 +580,8 @@ cudaError_t launch_tc_t(const KernelArgs& a, const CUtensorMap& km, const CUtens
   const int64_t slots = static_cast<int64_t>(num_sms) * tc::kCtasPerSm;
   const unsigned grid = static_cast<unsigned>(items < slots ? items : slots);
   if (grid == 0) return cudaSuccess;
-  kern<<<grid, tc::kThreads, smem, s>>>(a, km, vm, qm, items, tc::kDefaultWaitBudget);
+  const long long budget = a.selftest_stall ? tc::kSelftestWaitBudget : tc::kDefaultWaitBudget;
+  kern<<<grid, tc::kThreads, smem, s>>>(a, km, vm, qm, items, budget);
   return cudaGetLastError();
 }
 

@@ -130,6 +130,7 @@ def test_host_checks_reject_bad_arguments(L):
     assert _call_v2(L, params(max_seq_len=100001, max_blocks_per_seq=6250)) == pa.PA_ERR_INVALID_ARG
     assert _call_v2(L, params(num_blocks=0)) == pa.PA_ERR_INVALID_ARG
     assert _call_v2(L, params(flags=8)) == pa.PA_ERR_INVALID_ARG
+    assert _call_v2(L, params(flags=4)) == pa.PA_ERR_INVALID_ARG
     assert L.pa_decode_v2(None, None, None, None, None, None, None, 0, None, None) == \
         pa.PA_ERR_INVALID_ARG
     V = ctypes.c_void_p

@@ -1,0 +1,45 @@
+"""Failure detection on the GPU without a fault.
+
+Every wait in the tensor-core kernel is bounded.  PA_FLAG_SELFTEST_STALL makes
+the kernel wait for an event that never happens (with a ~10 ms bound): the
+wait runs out, the kernel drains what it had in flight, releases its tensor
+memory and returns; the host then reads PA_ERR_DEVICE_TIMEOUT from the status
+word, the outputs are NaN, and the same CUDA context decodes correctly
+afterwards.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_attention_decode_v2_gb300 as pa
+from paged_attention_decode_v2_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+def test_wait_that_runs_out_reports_timeout_and_context_survives():
+    from paged_attention_decode_v2_gb300 import build
+    build.build()
+    bc = wl.make(wl.scaled(wl.WORKLOADS["gqa_8k"], seq_len=3000), poison=True)
+    bg = bc.to("cuda")
+    P = 512
+    params = pa.make_params(bg.q, bg.k_cache, bg.block_tables, max_seq_len=bg.max_seq_len,
+                            scale=bg.scale, partition_size=P, out_dtype=torch.float32)
+    assert pa.decode_kernel(params) == 2, "the self-test needs the tensor-core path"
+    ws = pa.alloc_workspace(params)
+    kw = dict(max_seq_len=bg.max_seq_len, scale=bg.scale, partition_size=P)
+
+    out = torch.zeros(tuple(bg.q.shape), dtype=torch.float32, device="cuda")
+    pa.decode_v2(bg.q, bg.k_cache, bg.v_cache, bg.block_tables, bg.seq_lens, out, ws,
+                 flags=pa.PA_FLAG_SELFTEST_STALL, **kw)
+    torch.cuda.synchronize()
+    assert pa.read_device_status(ws) == pa.PA_ERR_DEVICE_TIMEOUT
+    assert torch.isnan(out).all().item()
+
+    # the context is still usable: a normal call succeeds and is correct
+    pa.decode_v2(bg.q, bg.k_cache, bg.v_cache, bg.block_tables, bg.seq_lens, out, ws, **kw)
+    torch.cuda.synchronize()
+    assert pa.read_device_status(ws) == pa.PA_OK
+    ref = oracle.decode(bc.q, bc.k_cache, bc.v_cache, bc.block_tables, bc.seq_lens, bc.scale)
+    assert float(np.max(np.abs(out.double().cpu().numpy() - ref))) <= 2e-3
