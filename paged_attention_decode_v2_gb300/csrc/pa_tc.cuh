@@ -3,10 +3,15 @@
 // Work items.  A work item is one (sequence, KV head, token range), the
 // range being one V2 partition or the whole sequence (V1); all G <= 8 query
 // heads of the KV head are served together, so each key/value byte is read
-// once per step.  The grid is persistent (about two CTAs per SM); CTA c
-// takes items c, c + gridDim.x, ... in partition-major order and skips the
-// ones a sequence does not have.  The shared-memory ring keeps streaming
-// from one item into the next, so a CTA never stops loading between items.
+// once per step.  The grid is persistent (two CTAs per SM, or one CTA with a
+// deeper ring per item when there are fewer items than SMs); CTA c takes
+// items c, c + gridDim.x, ...  For V2 batches of up to 1024 sequences every
+// CTA first builds a compact work list (a prefix sum of the sequences'
+// partition counts in shared memory), so only existing (sequence, partition,
+// KV head) items are enumerated; otherwise the full space is walked in
+// partition-major order and empty ranges are skipped.  The shared-memory ring
+// keeps streaming from one item into the next (the producer loads the next
+// chunk's block ids while the current one streams).
 //
 // Roles (192 threads, warp-specialised):
 //   warp 4      producer: streams q, keys and values into shared memory with
@@ -55,41 +60,47 @@ constexpr int kThreads = 192;
 constexpr int kChunk = 512;           // tokens per chunk
 constexpr int kTile = 128;            // tokens per QK^T MMA (M)
 constexpr int kStageBytes = 16384;    // one ring stage
-constexpr int kStages = 5;            // ring depth (two CTAs share one SM)
 constexpr int kTmemCols = 128;        // S: 4 tiles x 16 columns, O^T: 2 x 16
 constexpr int kOCol = 64;             // first tensor-memory column of O^T
-constexpr int kCtasPerSm = 2;
+constexpr int kMaxStages = 12;
+constexpr int kMaxCompactSeqs = 1024; // V2 batches up to this size use a compact work list
 constexpr long long kDefaultWaitBudget = 4000000000LL;  // cycles (about 2 s)
 constexpr long long kSelftestWaitBudget = 20000000LL;   // cycles (about 10 ms)
 
-template <int D>
+// Two shapes of the same kernel: a 5-stage ring with two CTAs per SM for
+// large grids, and a 12-stage (192 KB) ring with one CTA per SM when there
+// are fewer work items than SMs, so each CTA keeps more bytes in flight.
+template <int D, int NST>
 struct Layout {
   static constexpr int kSlices = D / 64;                  // 64-element head_dim slices
   static constexpr int kHalves = D / 128;                 // 128-row halves of head_dim
   static constexpr int kVTokens = kStageBytes / (D * 2);  // tokens per V stage
-  static constexpr int kQOff = kStages * kStageBytes;     // 2 q buffers x slices x 1 KB
+  static constexpr int kQOff = NST * kStageBytes;         // 2 q buffers x slices x 1 KB
   static constexpr int kPtOff = kQOff + 2 * kSlices * 1024;
-  static constexpr int kCtrlOff = kPtOff + (kChunk / 16) * 512;
-  static constexpr int kBytes = kCtrlOff + 512;
+  static constexpr int kPrefixOff = kPtOff + (kChunk / 16) * 512;
+  static constexpr int kCtrlOff = kPrefixOff + ((kMaxCompactSeqs + 1) * 4 + 63) / 64 * 64;
+  static constexpr int kBytes = kCtrlOff + 1024;
   static constexpr int kSmem = kBytes + 1024;  // room to align to 1024
 };
 
 struct Ctrl {
-  uint64_t full[kStages];   // stage landed (TMA transaction count)
-  uint64_t empty[kStages];  // stage consumed (MMA commit)
-  uint64_t qfull[2];        // q buffer landed
-  uint64_t qempty[2];       // q buffer no longer read by MMAs
-  uint64_t s_full;          // chunk logits ready in tensor memory
-  uint64_t p_ready;         // P^T written (128 softmax threads arrive)
-  uint64_t o_full;          // chunk O^T ready in tensor memory
-  uint64_t tail;            // producer-private: a tail value stage landed
-  uint64_t drain;           // abort path: all issued MMAs finished
-  uint64_t never;           // self-test: nothing ever arrives here
+  uint64_t full[kMaxStages];   // stage landed (TMA transaction count)
+  uint64_t empty[kMaxStages];  // stage consumed (MMA commit)
+  uint64_t qfull[2];           // q buffer landed
+  uint64_t qempty[2];          // q buffer no longer read by MMAs
+  uint64_t s_full;             // chunk logits ready in tensor memory
+  uint64_t p_ready;            // P^T written (128 softmax threads arrive)
+  uint64_t o_full;             // chunk O^T ready in tensor memory
+  uint64_t tail;               // producer-private: a tail value stage landed
+  uint64_t drain;              // abort path: all issued MMAs finished
+  uint64_t never;              // self-test: nothing ever arrives here
+  int64_t total_items;         // work items to enumerate
   uint32_t tmem;
-  int abort;                // some wait gave up
-  float red[2][4][8];       // cross-warp max / sum of the softmax warps
+  int abort;                   // some wait gave up
+  int scan[8];                 // per-warp totals of the work-list scan
+  float red[2][4][8];          // cross-warp max / sum of the softmax warps
 };
-static_assert(sizeof(Ctrl) <= 512, "control block");
+static_assert(sizeof(Ctrl) <= 1024, "control block");
 
 // One work item, decoded the same way by every role.
 struct Item {
@@ -98,13 +109,31 @@ struct Item {
   bool len_ok;     // 0 <= seq_len <= max_seq_len
 };
 
-__device__ __forceinline__ Item decode_item(const KernelArgs& a, int64_t k, bool v2) {
+// Item k.  With a compact work list (prefix[b] = partitions of sequences
+// before b, kept in shared memory) k runs over existing (sequence, partition,
+// KV head) triples only; otherwise over the full B x Hkv (x NP) space,
+// partition-major, where ranges past a sequence's end come out empty.
+__device__ __forceinline__ Item item_at(const KernelArgs& a, const int32_t* prefix, int64_t k,
+                                        bool v2) {
   Item it;
-  const int64_t per_part = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads;
-  it.part = v2 ? static_cast<int>(k / per_part) : 0;
-  const int64_t rem = v2 ? k % per_part : k;
-  it.b = static_cast<int>(rem / a.num_kv_heads);
-  it.kvh = static_cast<int>(rem % a.num_kv_heads);
+  if (prefix) {
+    const int64_t j = k / a.num_kv_heads;
+    it.kvh = static_cast<int>(k % a.num_kv_heads);
+    int lo = 0, hi = a.num_seqs;  // largest lo with prefix[lo] <= j
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (prefix[mid] <= j) lo = mid;
+      else hi = mid;
+    }
+    it.b = lo;
+    it.part = static_cast<int>(j - prefix[lo]);
+  } else {
+    const int64_t per_part = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads;
+    it.part = v2 ? static_cast<int>(k / per_part) : 0;
+    const int64_t rem = v2 ? k % per_part : k;
+    it.b = static_cast<int>(rem / a.num_kv_heads);
+    it.kvh = static_cast<int>(rem % a.num_kv_heads);
+  }
   const int32_t L = __ldg(a.seq_lens + it.b);
   it.len_ok = seq_len_ok(a, L);
   it.t0 = v2 ? it.part * a.partition_size : 0;
@@ -129,15 +158,16 @@ __device__ __forceinline__ __half round16(float x, __half*) { return __float2hal
 
 }  // namespace tc
 
-template <typename T, int D, int BS, bool kV2>
-__global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
+template <typename T, int D, int BS, bool kV2, int NST, int CPS>
+__global__ void __launch_bounds__(tc::kThreads, CPS)
     pa_tc_kernel(const KernelArgs a, const __grid_constant__ CUtensorMap kmap,
                  const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap qmap,
-                 int64_t total_items, long long budget) {
+                 int64_t grid_items, int compact, long long budget) {
   using namespace tc;
-  using Lay = Layout<D>;
+  using Lay = Layout<D, NST>;
   static_assert(D == 128 || D == 256, "head_dim");
   static_assert(BS % 16 == 0 && kTile % BS == 0 && Lay::kVTokens % BS == 0, "block size");
+  static_assert(NST <= kMaxStages, "ring depth");
   constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
 
   extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -145,6 +175,7 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
   uint8_t* ring = smem;
   uint8_t* qs = smem + Lay::kQOff;
   uint8_t* pt = smem + Lay::kPtOff;
+  int32_t* prefix_s = reinterpret_cast<int32_t*>(smem + Lay::kPrefixOff);
   Ctrl& c = *reinterpret_cast<Ctrl*>(smem + Lay::kCtrlOff);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -158,7 +189,7 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
 
   // ---- set-up -----------------------------------------------------------------
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < NST; ++s) {
       sm100::mbar_init(&c.full[s], 1);
       sm100::mbar_init(&c.empty[s], 1);
     }
@@ -183,10 +214,53 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
     sm100::tma_prefetch_desc(&vmap);
     sm100::tma_prefetch_desc(&qmap);
   }
+  const int32_t* prefix = nullptr;
+  if (compact) {
+    // Compact work list: prefix[b] = partitions of the sequences before b.
+    // A sequence whose length is outside 0..max_seq_len contributes none
+    // (the reduce kernel writes its NaN rows).
+    int carry = 0;
+    for (int base = 0; base < a.num_seqs; base += kThreads) {
+      const int b = base + tid;
+      int n = 0;
+      if (b < a.num_seqs) {
+        const int32_t L = __ldg(a.seq_lens + b);
+        if (seq_len_ok(a, L))
+          n = (L + a.partition_size - 1) / a.partition_size;
+        else if (blockIdx.x == 0)
+          set_status(a.status, PA_ERR_BAD_SEQ_LEN);
+      }
+      int x = n;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (lane == 31) c.scan[warp] = x;
+      __syncthreads();
+      int off = 0, round_total = 0;
+#pragma unroll
+      for (int w = 0; w < kThreads / 32; ++w) {
+        off += w < warp ? c.scan[w] : 0;
+        round_total += c.scan[w];
+      }
+      if (b < a.num_seqs) prefix_s[b + 1] = carry + off + x;
+      carry += round_total;
+      __syncthreads();
+    }
+    if (tid == 0) {
+      prefix_s[0] = 0;
+      c.total_items = static_cast<int64_t>(carry) * a.num_kv_heads;
+    }
+    prefix = prefix_s;
+  } else if (tid == 0) {
+    c.total_items = grid_items;
+  }
   sm100::tc_fence_before();
   __syncthreads();
   sm100::tc_fence_after();
   const uint32_t tmem = c.tmem;
+  const int64_t total_items = c.total_items;
   volatile int* abort_flag = &c.abort;
 
   if (warp == 4) {
@@ -197,12 +271,55 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
     uint32_t g = 0, qn = 0, tn = 0;  // ring stages / q buffers / tail stages so far
     int tail_pending = -1;           // slot of a tail stage still landing
     bool ok = true;
-    for (int64_t k = blockIdx.x; k < total_items && ok; k += stride) {
-      const Item it = decode_item(a, k, kV2);
-      if (it.t0 >= it.t1) continue;
-      const int32_t* bt = a.block_tables + static_cast<int64_t>(it.b) * a.max_blocks_per_seq;
-      // q rows of the item's query heads (8 rows; rows past G are ignored)
-      {
+
+    // Chunks are visited in order (item k, chunk ci); the block ids of the
+    // next chunk are loaded while the current one streams.
+    auto next_active = [&](int64_t k, Item& it) -> int64_t {
+      for (; k < total_items; k += stride) {
+        it = item_at(a, prefix, k, kV2);
+        if (it.t0 < it.t1) return k;
+      }
+      return total_items;
+    };
+    auto load_ids = [&](const Item& it, int ci, int32_t& y, bool& badl) {
+      const int c0 = it.t0 + ci * kChunk;
+      const int n = min(kChunk, it.t1 - c0);
+      const int nblk = (n + BS - 1) / BS;  // <= 32: one block id per lane
+      int32_t id = 0;
+      badl = false;
+      if (lane < nblk) {
+        id = __ldg(a.block_tables + static_cast<int64_t>(it.b) * a.max_blocks_per_seq + c0 / BS +
+                   lane);
+        badl = id < 0 || id >= a.num_blocks;
+      }
+      // TMA row of the block's first slot; a bad id becomes a negative row,
+      // which TMA fills with zeros instead of reading memory.
+      y = badl ? -BS : (id * a.num_kv_heads + it.kvh) * BS;
+    };
+
+    Item it;
+    int64_t k = next_active(blockIdx.x, it);
+    int ci = 0;
+    int32_t y = 0;
+    bool badl = false;
+    if (k < total_items) load_ids(it, 0, y, badl);
+    while (k < total_items && ok) {
+      const int nchunks = (it.t1 - it.t0 + kChunk - 1) / kChunk;
+      // look ahead: the next chunk and its block ids
+      Item it2 = it;
+      int64_t k2 = k;
+      int ci2 = ci + 1;
+      if (ci2 >= nchunks) {
+        k2 = next_active(k + stride, it2);
+        ci2 = 0;
+      }
+      int32_t y2 = 0;
+      bool bad2 = false;
+      if (k2 < total_items) load_ids(it2, ci2, y2, bad2);
+
+      if (__any_sync(0xffffffffu, badl) && lane == 0) set_status(a.status, PA_ERR_BAD_BLOCK_ID);
+      if (ci == 0) {
+        // q rows of the item's query heads (8 rows; rows past G are ignored)
         const int qb = qn & 1;
         ok = sm100::mbar_wait(&c.qempty[qb], ((qn >> 1) & 1) ^ 1, budget, abort_flag);
         if (!ok) break;
@@ -215,91 +332,82 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
         }
         ++qn;
       }
-      const int nchunks = (it.t1 - it.t0 + kChunk - 1) / kChunk;
       const bool tail_fix = (it.t1 % 16) != 0;
-      for (int ci = 0; ci < nchunks && ok; ++ci) {
-        const int c0 = it.t0 + ci * kChunk;
-        const int n = min(kChunk, it.t1 - c0);
-        const int nblk = (n + BS - 1) / BS;  // <= 32: one block id per lane
-        int32_t id = 0;
-        bool bad = false;
-        if (lane < nblk) {
-          id = __ldg(bt + c0 / BS + lane);
-          bad = id < 0 || id >= a.num_blocks;
-        }
-        if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(a.status, PA_ERR_BAD_BLOCK_ID);
-        // TMA row of the block's first slot; a bad id becomes a negative row,
-        // which TMA fills with zeros instead of reading memory.
-        const int32_t y = bad ? -BS : (id * a.num_kv_heads + it.kvh) * BS;
-        const int nt = (n + kTile - 1) / kTile;
-        for (int tt = 0; tt < nt && ok; ++tt) {
-          const int jb0 = tt * kTile / BS;
-          const int jb1 = (min(n, tt * kTile + kTile) + BS - 1) / BS;
-          for (int sl = 0; sl < Lay::kSlices; ++sl) {
-            const int slot = g % kStages;
-            ok = sm100::mbar_wait(&c.empty[slot], ((g / kStages) & 1) ^ 1, budget, abort_flag);
-            if (!ok) break;
-            if (lane == 0) sm100::mbar_arrive_expect_tx(&c.full[slot], (jb1 - jb0) * BS * 128);
-            for (int j = jb0; j < jb1; ++j) {
-              const int32_t yj = __shfl_sync(0xffffffffu, y, j);
-              if (lane == 0)
-                sm100::tma_load_2d(ring + slot * kStageBytes + (j - jb0) * BS * 128, &kmap,
-                                   &c.full[slot], sl * 64, yj, stream_once);
-            }
-            ++g;
-          }
-        }
-        const int nv = (n + Lay::kVTokens - 1) / Lay::kVTokens;
-        for (int v = 0; v < nv && ok; ++v) {
-          const int jb0 = v * Lay::kVTokens / BS;
-          const int jb1 = (min(n, (v + 1) * Lay::kVTokens) + BS - 1) / BS;
-          const int slot = g % kStages;
-          ok = sm100::mbar_wait(&c.empty[slot], ((g / kStages) & 1) ^ 1, budget, abort_flag);
+      const int c0 = it.t0 + ci * kChunk;
+      const int n = min(kChunk, it.t1 - c0);
+      const int nt = (n + kTile - 1) / kTile;
+      for (int tt = 0; tt < nt && ok; ++tt) {
+        const int jb0 = tt * kTile / BS;
+        const int jb1 = (min(n, tt * kTile + kTile) + BS - 1) / BS;
+        for (int sl = 0; sl < Lay::kSlices; ++sl) {
+          const int slot = g % NST;
+          ok = sm100::mbar_wait(&c.empty[slot], ((g / NST) & 1) ^ 1, budget, abort_flag);
           if (!ok) break;
-          // The stage holding the range end, when that end falls inside a
-          // 16-token MMA step, lands on the producer's own barrier first:
-          // the rows past the end are cleared (P^T is zero there, but 0 * NaN
-          // would be NaN) and only then is the stage handed to the MMA warp.
-          const bool tail = tail_fix && ci == nchunks - 1 && v == nv - 1;
-          uint64_t* land = tail ? &c.tail : &c.full[slot];
-          if (lane == 0) sm100::mbar_arrive_expect_tx(land, (jb1 - jb0) * BS * D * 2);
+          if (lane == 0) sm100::mbar_arrive_expect_tx(&c.full[slot], (jb1 - jb0) * BS * 128);
           for (int j = jb0; j < jb1; ++j) {
             const int32_t yj = __shfl_sync(0xffffffffu, y, j);
             if (lane == 0)
-              sm100::tma_load_3d(ring + slot * kStageBytes + (j - jb0) * BS * D * 2, &vmap, land, 0,
-                                 yj, 0, stream_once);
+              sm100::tma_load_2d(ring + slot * kStageBytes + (j - jb0) * BS * 128, &kmap,
+                                 &c.full[slot], sl * 64, yj, stream_once);
           }
           ++g;
-          if (tail) {
-            tail_pending = slot;
-            ok = sm100::mbar_wait(&c.tail, tn & 1, budget, abort_flag);
-            if (!ok) break;
-            ++tn;
-            tail_pending = -1;
-            const int r0 = n - v * Lay::kVTokens;  // first row past the end
-            const int r1 = (r0 + 15) / 16 * 16;    // end of its 16-token step
-            uint8_t* st = ring + slot * kStageBytes;
-            const int pieces = (r1 - r0) * Lay::kSlices * 8;  // 16-byte pieces
-            for (int i = lane; i < pieces; i += 32) {
-              const int line = i / 8, piece = i % 8;
-              const int r = r0 + line / Lay::kSlices, sl = line % Lay::kSlices;
-              *reinterpret_cast<uint4*>(st + (r / BS) * BS * D * 2 + sl * BS * 128 +
-                                        (r % BS) * 128 + piece * 16) = make_uint4(0u, 0u, 0u, 0u);
-            }
-            sm100::fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) sm100::mbar_arrive(&c.full[slot]);  // no bytes: the data is there
-          }
         }
       }
+      const int nv = (n + Lay::kVTokens - 1) / Lay::kVTokens;
+      for (int v = 0; v < nv && ok; ++v) {
+        const int jb0 = v * Lay::kVTokens / BS;
+        const int jb1 = (min(n, (v + 1) * Lay::kVTokens) + BS - 1) / BS;
+        const int slot = g % NST;
+        ok = sm100::mbar_wait(&c.empty[slot], ((g / NST) & 1) ^ 1, budget, abort_flag);
+        if (!ok) break;
+        // The stage holding the range end, when that end falls inside a
+        // 16-token MMA step, lands on the producer's own barrier first: the
+        // rows past the end are cleared (P^T is zero there, but 0 * NaN
+        // would be NaN) and only then is the stage handed to the MMA warp.
+        const bool tail = tail_fix && ci == nchunks - 1 && v == nv - 1;
+        uint64_t* land = tail ? &c.tail : &c.full[slot];
+        if (lane == 0) sm100::mbar_arrive_expect_tx(land, (jb1 - jb0) * BS * D * 2);
+        for (int j = jb0; j < jb1; ++j) {
+          const int32_t yj = __shfl_sync(0xffffffffu, y, j);
+          if (lane == 0)
+            sm100::tma_load_3d(ring + slot * kStageBytes + (j - jb0) * BS * D * 2, &vmap, land, 0,
+                               yj, 0, stream_once);
+        }
+        ++g;
+        if (tail) {
+          tail_pending = slot;
+          ok = sm100::mbar_wait(&c.tail, tn & 1, budget, abort_flag);
+          if (!ok) break;
+          ++tn;
+          tail_pending = -1;
+          const int r0 = n - v * Lay::kVTokens;  // first row past the end
+          const int r1 = (r0 + 15) / 16 * 16;    // end of its 16-token step
+          uint8_t* st = ring + slot * kStageBytes;
+          const int pieces = (r1 - r0) * Lay::kSlices * 8;  // 16-byte pieces
+          for (int i = lane; i < pieces; i += 32) {
+            const int line = i / 8, piece = i % 8;
+            const int r = r0 + line / Lay::kSlices, sl = line % Lay::kSlices;
+            *reinterpret_cast<uint4*>(st + (r / BS) * BS * D * 2 + sl * BS * 128 + (r % BS) * 128 +
+                                      piece * 16) = make_uint4(0u, 0u, 0u, 0u);
+          }
+          sm100::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) sm100::mbar_arrive(&c.full[slot]);  // no bytes: the data is there
+        }
+      }
+      k = k2;
+      ci = ci2;
+      it = it2;
+      y = y2;
+      badl = bad2;
     }
     if (!ok) {
       if (lane == 0) fail(c, a.status);
       // Copies already issued must land before the CTA may exit: wait for
       // the newest use of every slot (older uses completed before it began).
-      for (uint32_t gg = g > kStages ? g - kStages : 0; gg < g; ++gg)
-        if (static_cast<int>(gg % kStages) != tail_pending)
-          sm100::mbar_wait(&c.full[gg % kStages], (gg / kStages) & 1, budget, nullptr);
+      for (uint32_t gg = g > NST ? g - NST : 0; gg < g; ++gg)
+        if (static_cast<int>(gg % NST) != tail_pending)
+          sm100::mbar_wait(&c.full[gg % NST], (gg / NST) & 1, budget, nullptr);
       if (tail_pending >= 0) sm100::mbar_wait(&c.tail, tn & 1, budget, nullptr);
       for (uint32_t qq = qn > 2 ? qn - 2 : 0; qq < qn; ++qq)
         sm100::mbar_wait(&c.qfull[qq & 1], (qq >> 1) & 1, budget, nullptr);
@@ -318,7 +426,7 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
       // wait runs out and the abort path is exercised
       if (a.selftest_stall) ok = sm100::mbar_wait(&c.never, 0, budget, abort_flag);
       for (int64_t k = blockIdx.x; k < total_items && ok; k += stride) {
-        const Item it = decode_item(a, k, kV2);
+        const Item it = item_at(a, prefix, k, kV2);
         if (it.t0 >= it.t1) continue;
         const int qb = qn & 1;
         ok = sm100::mbar_wait(&c.qfull[qb], (qn >> 1) & 1, budget, abort_flag);
@@ -332,8 +440,8 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
           const int nt = (n + kTile - 1) / kTile;
           for (int tt = 0; tt < nt && ok; ++tt) {
             for (int sl = 0; sl < Lay::kSlices; ++sl) {
-              const int slot = g % kStages;
-              ok = sm100::mbar_wait(&c.full[slot], (g / kStages) & 1, budget, abort_flag);
+              const int slot = g % NST;
+              ok = sm100::mbar_wait(&c.full[slot], (g / NST) & 1, budget, abort_flag);
               if (!ok) break;
               sm100::tc_fence_after();
               const uint32_t st = ring_base + slot * kStageBytes;
@@ -357,8 +465,8 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
           const int nv = (n + Lay::kVTokens - 1) / Lay::kVTokens;
           bool first = true;
           for (int v = 0; v < nv; ++v) {
-            const int slot = g % kStages;
-            ok = sm100::mbar_wait(&c.full[slot], (g / kStages) & 1, budget, abort_flag);
+            const int slot = g % NST;
+            ok = sm100::mbar_wait(&c.full[slot], (g / NST) & 1, budget, abort_flag);
             if (!ok) break;
             sm100::tc_fence_after();
             const uint32_t st = ring_base + slot * kStageBytes;
@@ -400,7 +508,7 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
     const float sl2 = a.scale_log2;
     uint32_t cc = 0;
     for (int64_t k = blockIdx.x; k < total_items; k += stride) {
-      const Item it = decode_item(a, k, kV2);
+      const Item it = item_at(a, prefix, k, kV2);
       const int64_t row0 = static_cast<int64_t>(it.b) * Hq + it.kvh * G;
       if (it.t0 >= it.t1) {
         if (!it.len_ok && it.part == 0 && it.kvh == 0 && tid == 0)
@@ -561,28 +669,42 @@ __global__ void __launch_bounds__(tc::kThreads, tc::kCtasPerSm)
   if (warp == 5) sm100::tmem_dealloc(tmem, kTmemCols);
 }
 
+template <typename T, int D, int BS, bool V2, int NST, int CPS>
+cudaError_t launch_tc_variant(const KernelArgs& a, const CUtensorMap& km, const CUtensorMap& vm,
+                              const CUtensorMap& qm, int64_t items, unsigned grid, int compact,
+                              cudaStream_t s) {
+  static bool configured[128] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+  auto kern = pa_tc_kernel<T, D, BS, V2, NST, CPS>;
+  const int smem = tc::Layout<D, NST>::kSmem;
+  if (!configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  const long long budget = a.selftest_stall ? tc::kSelftestWaitBudget : tc::kDefaultWaitBudget;
+  kern<<<grid, tc::kThreads, smem, s>>>(a, km, vm, qm, items, compact, budget);
+  return cudaGetLastError();
+}
+
 template <typename T, int D, int BS>
 cudaError_t launch_tc_t(const KernelArgs& a, const CUtensorMap& km, const CUtensorMap& vm,
                         const CUtensorMap& qm, bool v2, int num_sms, cudaStream_t s) {
-  static bool configured[2][128] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  auto kern = v2 ? pa_tc_kernel<T, D, BS, true> : pa_tc_kernel<T, D, BS, false>;
-  const int smem = tc::Layout<D>::kSmem;
-  if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
-  if (!configured[v2][dev]) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    configured[v2][dev] = true;
-  }
+  // upper bound of the work items: every (sequence, KV head[, partition])
   const int64_t items = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads *
                         (v2 ? a.num_partitions : 1);
-  const int64_t slots = static_cast<int64_t>(num_sms) * tc::kCtasPerSm;
+  if (items == 0) return cudaSuccess;
+  const int compact = (v2 && a.num_seqs > 1 && a.num_seqs <= tc::kMaxCompactSeqs) ? 1 : 0;
+  if (items < num_sms) {  // few items: one deep-ring CTA each
+    const unsigned grid = static_cast<unsigned>(items);
+    return v2 ? launch_tc_variant<T, D, BS, true, 12, 1>(a, km, vm, qm, items, grid, compact, s)
+              : launch_tc_variant<T, D, BS, false, 12, 1>(a, km, vm, qm, items, grid, compact, s);
+  }
+  const int64_t slots = static_cast<int64_t>(num_sms) * 2;
   const unsigned grid = static_cast<unsigned>(items < slots ? items : slots);
-  if (grid == 0) return cudaSuccess;
-  const long long budget = a.selftest_stall ? tc::kSelftestWaitBudget : tc::kDefaultWaitBudget;
-  kern<<<grid, tc::kThreads, smem, s>>>(a, km, vm, qm, items, budget);
-  return cudaGetLastError();
+  return v2 ? launch_tc_variant<T, D, BS, true, 5, 2>(a, km, vm, qm, items, grid, compact, s)
+            : launch_tc_variant<T, D, BS, false, 5, 2>(a, km, vm, qm, items, grid, compact, s);
 }
 
 template <typename T>
