@@ -323,13 +323,11 @@ __global__ void __launch_bounds__(tc::kThreads, CPS)
         const int qb = qn & 1;
         ok = sm100::mbar_wait(&c.qempty[qb], ((qn >> 1) & 1) ^ 1, budget, abort_flag);
         if (!ok) break;
-        if (lane == 0) {
-          sm100::mbar_arrive_expect_tx(&c.qfull[qb], Lay::kSlices * 1024);
-          const int32_t qrow = it.b * Hq + it.kvh * G;
-          for (int sl = 0; sl < Lay::kSlices; ++sl)
-            sm100::tma_load_2d(qs + (qb * Lay::kSlices + sl) * 1024, &qmap, &c.qfull[qb], sl * 64,
-                               qrow, keep);
-        }
+        if (lane == 0) sm100::mbar_arrive_expect_tx(&c.qfull[qb], Lay::kSlices * 1024);
+        __syncwarp();
+        if (lane < Lay::kSlices)  // one lane per slice
+          sm100::tma_load_2d(qs + (qb * Lay::kSlices + lane) * 1024, &qmap, &c.qfull[qb], lane * 64,
+                             it.b * Hq + it.kvh * G, keep);
         ++qn;
       }
       const bool tail_fix = (it.t1 % 16) != 0;
@@ -344,12 +342,12 @@ __global__ void __launch_bounds__(tc::kThreads, CPS)
           ok = sm100::mbar_wait(&c.empty[slot], ((g / NST) & 1) ^ 1, budget, abort_flag);
           if (!ok) break;
           if (lane == 0) sm100::mbar_arrive_expect_tx(&c.full[slot], (jb1 - jb0) * BS * 128);
-          for (int j = jb0; j < jb1; ++j) {
-            const int32_t yj = __shfl_sync(0xffffffffu, y, j);
-            if (lane == 0)
-              sm100::tma_load_2d(ring + slot * kStageBytes + (j - jb0) * BS * 128, &kmap,
-                                 &c.full[slot], sl * 64, yj, stream_once);
-          }
+          __syncwarp();
+          // one lane per block: the whole stage is issued by one warp instruction
+          const int32_t yj = __shfl_sync(0xffffffffu, y, (jb0 + lane) & 31);
+          if (jb0 + lane < jb1)
+            sm100::tma_load_2d(ring + slot * kStageBytes + lane * BS * 128, &kmap, &c.full[slot],
+                               sl * 64, yj, stream_once);
           ++g;
         }
       }
@@ -367,12 +365,11 @@ __global__ void __launch_bounds__(tc::kThreads, CPS)
         const bool tail = tail_fix && ci == nchunks - 1 && v == nv - 1;
         uint64_t* land = tail ? &c.tail : &c.full[slot];
         if (lane == 0) sm100::mbar_arrive_expect_tx(land, (jb1 - jb0) * BS * D * 2);
-        for (int j = jb0; j < jb1; ++j) {
-          const int32_t yj = __shfl_sync(0xffffffffu, y, j);
-          if (lane == 0)
-            sm100::tma_load_3d(ring + slot * kStageBytes + (j - jb0) * BS * D * 2, &vmap, land, 0,
-                               yj, 0, stream_once);
-        }
+        __syncwarp();
+        const int32_t yj = __shfl_sync(0xffffffffu, y, (jb0 + lane) & 31);
+        if (jb0 + lane < jb1)
+          sm100::tma_load_3d(ring + slot * kStageBytes + lane * BS * D * 2, &vmap, land, 0, yj, 0,
+                             stream_once);
         ++g;
         if (tail) {
           tail_pending = slot;
