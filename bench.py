@@ -182,6 +182,10 @@ def run_ours(args, rank, world, device):
         def zero_(self):
             # a read sweep larger than L2: evicts it without leaving dirty lines
             torch.amax(flush_buf, dim=0, out=flush_sink)
+            # then keep the GPU busy for ~100 us so the host has enqueued the
+            # step (and its events) before the GPU reaches the start event:
+            # the event window then holds device time only
+            torch.cuda._sleep(200_000)
 
     flush = _Flush()
     stream = torch.cuda.current_stream(device)

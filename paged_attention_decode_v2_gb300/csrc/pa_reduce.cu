@@ -42,10 +42,12 @@ __global__ void __launch_bounds__(kNT) pa_reduce_kernel(const KernelArgs a) {
   const int64_t row = static_cast<int64_t>(b) * a.num_heads + h;
   const int d0 = x * kSlice;
 
+  // seq_lens is an input, not a pass-1 result: read it before waiting.
+  const int32_t L = a.seq_lens[b];
+
   // Wait for pass 1 (a no-op unless launched as a programmatic dependent).
   cudaGridDependencySynchronize();
 
-  const int32_t L = a.seq_lens[b];
   if (!seq_len_ok(a, L) || L == 0) {
     const float v = L == 0 ? 0.f : qnan();
     if (tid < kSlice) store_out(a.out, row * D + d0 + tid, a.out_dtype, v);

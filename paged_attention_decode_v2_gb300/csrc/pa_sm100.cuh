@@ -81,6 +81,20 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   return pol;
 }
 
+// L2 policy for data written now and read back soon (the V2 partials, read
+// by the reduce right after pass 1): evict it last.
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// Global store with an L2 cache policy.
+__device__ __forceinline__ void st_f32_policy(float* p, float v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(v), "l"(policy)
+               : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, uint64_t* bar, int32_t x,
                                             int32_t y, uint64_t policy) {
   asm volatile(

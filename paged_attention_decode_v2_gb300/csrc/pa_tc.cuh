@@ -77,10 +77,11 @@ struct Layout {
   static constexpr int kVTokens = kStageBytes / (D * 2);  // tokens per V stage
   static constexpr int kQOff = NST * kStageBytes;         // 2 q buffers x slices x 1 KB
   static constexpr int kPtOff = kQOff + 2 * kSlices * 1024;
-  static constexpr int kPrefixOff = kPtOff + (kChunk / 16) * 512;
-  static constexpr int kCtrlOff = kPrefixOff + ((kMaxCompactSeqs + 1) * 4 + 63) / 64 * 64;
-  static constexpr int kBytes = kCtrlOff + 1024;
-  static constexpr int kSmem = kBytes + 1024;  // room to align to 1024
+  static constexpr int kCtrlOff = kPtOff + (kChunk / 16) * 512;
+  static constexpr int kPrefixOff = kCtrlOff + 1024;  // only when the work list is compact
+  static constexpr int kPrefixBytes = ((kMaxCompactSeqs + 1) * 4 + 63) / 64 * 64;
+  static constexpr int kSmem = kPrefixOff + 1024;     // + room to align to 1024
+  static constexpr int kSmemCompact = kSmem + kPrefixBytes;
 };
 
 struct Ctrl {
@@ -630,6 +631,9 @@ __global__ void __launch_bounds__(tc::kThreads, CPS)
         sm100::tc_fence_before();
       }
       // ---- epilogue of the item ------------------------------------------------
+      // partials are read back by the reduce right after this kernel: keep
+      // them in L2 (the key / value stream is marked evict-first)
+      const uint64_t keep_l2 = sm100::l2_evict_last_policy();
       const bool poison = bad || *abort_flag != 0;
 #pragma unroll
       for (int j = 0; j < Lay::kHalves; ++j) {
@@ -639,7 +643,8 @@ __global__ void __launch_bounds__(tc::kThreads, CPS)
           if (h >= G) break;
           const float o = poison ? qnan() : acc[j][h] / s_run[h];
           if constexpr (kV2)
-            a.tmp_out[((row0 + h) * a.num_partitions + it.part) * D + d] = o;
+            sm100::st_f32_policy(a.tmp_out + ((row0 + h) * a.num_partitions + it.part) * D + d, o,
+                               keep_l2);
           else
             store_out(a.out, (row0 + h) * D + d, a.out_dtype, o);
         }
@@ -653,8 +658,8 @@ __global__ void __launch_bounds__(tc::kThreads, CPS)
             m = m_run[h];
             s = s_run[h];
           }
-        a.max_logits[w] = poison ? qnan() : m * kLn2;
-        a.exp_sums[w] = s;
+        sm100::st_f32_policy(a.max_logits + w, poison ? qnan() : m * kLn2, keep_l2);
+        sm100::st_f32_policy(a.exp_sums + w, s, keep_l2);
       }
     }
   }
@@ -674,9 +679,13 @@ cudaError_t launch_tc_variant(const KernelArgs& a, const CUtensorMap& km, const 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
   auto kern = pa_tc_kernel<T, D, BS, V2, NST, CPS>;
-  const int smem = tc::Layout<D, NST>::kSmem;
+  using Lay = tc::Layout<D, NST>;
+  // the compact work list's prefix table only takes shared memory when used,
+  // which leaves room on each SM for the reduce kernel's waiting CTAs
+  const int smem = compact ? Lay::kSmemCompact : Lay::kSmem;
   if (!configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmemCompact);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
@@ -698,8 +707,17 @@ cudaError_t launch_tc_t(const KernelArgs& a, const CUtensorMap& km, const CUtens
     return v2 ? launch_tc_variant<T, D, BS, true, 12, 1>(a, km, vm, qm, items, grid, compact, s)
               : launch_tc_variant<T, D, BS, false, 12, 1>(a, km, vm, qm, items, grid, compact, s);
   }
+  // Persistent grid: at most two CTAs per SM.  When the items are all the
+  // same size (not a compact work list) the grid is sized so every CTA does
+  // the same number of rounds, e.g. 392 items -> 196 CTAs x 2 rounds instead
+  // of 304 CTAs of which only 88 do a second round.
   const int64_t slots = static_cast<int64_t>(num_sms) * 2;
-  const unsigned grid = static_cast<unsigned>(items < slots ? items : slots);
+  int64_t grid64 = items < slots ? items : slots;
+  if (!compact && items > slots) {
+    const int64_t rounds = (items + slots - 1) / slots;
+    grid64 = (items + rounds - 1) / rounds;
+  }
+  const unsigned grid = static_cast<unsigned>(grid64);
   return v2 ? launch_tc_variant<T, D, BS, true, 5, 2>(a, km, vm, qm, items, grid, compact, s)
             : launch_tc_variant<T, D, BS, false, 5, 2>(a, km, vm, qm, items, grid, compact, s);
 }
