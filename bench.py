@@ -52,7 +52,7 @@ L2_FLUSH_BYTES = 256 << 20
 # change makes the figure stale, and the bench then reports null.
 NCU_TRAFFIC = {
     # (kernel source hash, workload, partition size): bytes per launch
-    ("589e810ec5dc24a8", "long_100k", 512): 409_728_256 + 4_928_000,
+    ("6766f9fbc4ffca86", "long_100k", 512): 409_721_088 + 3_597_312,
 }
 
 
@@ -341,7 +341,7 @@ def run_ours(args, rank, world, device):
     if rank == 0:
         result["clocks"] = sampler.summary(t_start, t_end)
         if world == 1 and not args.no_cpu_baseline:
-            result["cpu_baseline"] = cpu_baseline(batch, args.cpu_rows)
+            result["cpu_baseline"] = cpu_baseline(batch, args.cpu_rows, args.cpu_seconds)
     return result
 
 
@@ -356,18 +356,24 @@ def _oracle_rows(batch_cpu, rows):
     return time.perf_counter() - t0
 
 
-def cpu_baseline(batch, nrows):
+def cpu_baseline(batch, nrows, seconds):
+    """The oracle timed on the host cores: the first ``nrows`` query-head rows
+    of the step, repeated until ``seconds`` of CPU work have run, scaled to
+    one full step."""
     import oracle
     bc = batch.to("cpu")
     w = bc.workload
     total_rows = w.num_seqs * w.num_heads
     rows = list(range(min(nrows, total_rows)))
-    dt = _oracle_rows(bc, rows)
-    per_step_us = dt * 1e6 * total_rows / len(rows)
+    spent, reps = 0.0, 0
+    while reps == 0 or spent < seconds:
+        spent += _oracle_rows(bc, rows)
+        reps += 1
+    per_step_us = spent / reps * 1e6 * total_rows / len(rows)
     return {"value": round(per_step_us, 1), "unit": UNIT, "cores": oracle.max_threads(),
             "kind": "oracle",
-            "sample": f"{len(rows)} of {total_rows} query-head rows of one step "
-                      f"({dt:.1f} s), scaled to the full step"}
+            "sample": f"{len(rows)} of {total_rows} query-head rows of one step, "
+                      f"{reps} repetitions ({spent:.1f} s), scaled to the full step"}
 
 
 def run_reference(args, rank, world):
@@ -419,6 +425,8 @@ def main():
     ap.add_argument("--partition-size", type=int, default=0)
     ap.add_argument("--path", choices=("decode", "v1", "v2"), default="decode",
                     help="pa_decode (threshold dispatch), or force V1 / V2")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="host time the oracle baseline runs for (whole repetitions)")
     ap.add_argument("--cpu-rows", type=int, default=24,
                     help="query-head rows the CPU baseline computes")
     ap.add_argument("--ref-tokens", type=int, default=4096,
