@@ -63,6 +63,84 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, long l
   }
 }
 
+// ---- thread-block clusters ------------------------------------------------------
+
+// Every thread of every CTA of the cluster arrives and waits: memory
+// operations before it are visible cluster-wide after it.  Only used where
+// every thread is known to reach it (set-up and exit).
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+
+// Loads from shared memory of a CTA of the cluster (address from
+// mapa_shared).  No memory clobber, so independent loads issue back to back;
+// being volatile they stay after the barrier wait that precedes them.
+__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t caddr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(caddr));
+  return v;
+}
+__device__ __forceinline__ float4 ld_shared_cluster_v4(uint32_t caddr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(caddr));
+  return v;
+}
+
+// Store 16 bytes into shared memory of a CTA of the cluster and count them as
+// a completed transaction on that CTA's mbarrier `cbar` (both addresses from
+// mapa_shared, for the same CTA; the data address 16-byte aligned).
+__device__ __forceinline__ void st_async_v4(uint32_t caddr, float4 v, uint32_t cbar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, "
+      "[%5];" ::"r"(caddr),
+      "r"(__float_as_uint(v.x)), "r"(__float_as_uint(v.y)), "r"(__float_as_uint(v.z)),
+      "r"(__float_as_uint(v.w)), "r"(cbar)
+      : "memory");
+}
+
+// Arrive on an mbarrier of another CTA of the cluster (address from
+// mapa_shared), releasing this thread's earlier writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t caddr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr)
+               : "memory");
+}
+
+// Bounded parity wait that acquires at cluster scope (pairs with
+// mbar_arrive_cluster of other CTAs).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, long long budget,
+                                                  const volatile int* abort) {
+  auto try_wait = [&]() {
+    uint32_t ok;
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+  };
+  if (try_wait()) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (try_wait()) return true;
+    if (abort && *abort) return false;
+    if (clock64() - t0 > budget) return false;
+  }
+}
+
 // ---- proxy fences -------------------------------------------------------------
 
 // Make this thread's generic-proxy shared-memory writes visible to the async

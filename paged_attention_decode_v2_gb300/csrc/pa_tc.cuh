@@ -45,6 +45,7 @@
 // tensor memory is released, and the outputs the CTA writes become NaN.
 #pragma once
 
+#include <algorithm>
 #include <type_traits>
 
 #include <cuda.h>
@@ -62,14 +63,16 @@ constexpr int kTile = 128;            // tokens per QK^T MMA (M)
 constexpr int kStageBytes = 16384;    // one ring stage
 constexpr int kTmemCols = 128;        // S: 4 tiles x 16 columns, O^T: 2 x 16
 constexpr int kOCol = 64;             // first tensor-memory column of O^T
-constexpr int kMaxStages = 12;
+constexpr int kMaxStages = 12;        // barrier slots in the control block
+constexpr int kDeepStages = 11;       // ring of the one-CTA-per-SM shape
 constexpr int kMaxCompactSeqs = 1024; // V2 batches up to this size use a compact work list
 constexpr long long kDefaultWaitBudget = 4000000000LL;  // cycles (about 2 s)
 constexpr long long kSelftestWaitBudget = 20000000LL;   // cycles (about 10 ms)
 
 // Two shapes of the same kernel: a 5-stage ring with two CTAs per SM for
-// large grids, and a 12-stage (192 KB) ring with one CTA per SM when there
-// are fewer work items than SMs, so each CTA keeps more bytes in flight.
+// large grids, and an 11-stage (176 KB) ring with one CTA per SM when there
+// are fewer work items than SMs, so each CTA keeps more bytes in flight; the
+// latter also holds the receive buffer of the cluster combine.
 template <int D, int NST>
 struct Layout {
   static constexpr int kSlices = D / 64;                  // 64-element head_dim slices
@@ -77,7 +80,11 @@ struct Layout {
   static constexpr int kVTokens = kStageBytes / (D * 2);  // tokens per V stage
   static constexpr int kQOff = NST * kStageBytes;         // 2 q buffers x slices x 1 KB
   static constexpr int kPtOff = kQOff + 2 * kSlices * 1024;
-  static constexpr int kCtrlOff = kPtOff + (kChunk / 16) * 512;
+  static constexpr int kCombOff = kPtOff + (kChunk / 16) * 512;
+  // cluster combine receive buffer: sums [cs][8][D / cs], statistics [16][20]
+  static constexpr int kCombBytes =
+      NST == kDeepStages ? ((8 * D + 16 * 20) * 4 + 1023) / 1024 * 1024 : 0;
+  static constexpr int kCtrlOff = kCombOff + kCombBytes;
   static constexpr int kPrefixOff = kCtrlOff + 1024;  // only when the work list is compact
   static constexpr int kPrefixBytes = ((kMaxCompactSeqs + 1) * 4 + 63) / 64 * 64;
   static constexpr int kSmem = kPrefixOff + 1024;     // + room to align to 1024
@@ -95,6 +102,7 @@ struct Ctrl {
   uint64_t tail;               // producer-private: a tail value stage landed
   uint64_t drain;              // abort path: all issued MMAs finished
   uint64_t never;              // self-test: nothing ever arrives here
+  uint64_t comb_ready;         // cluster: every CTA's partial sums have landed here
   int64_t total_items;         // work items to enumerate
   uint32_t tmem;
   int abort;                   // some wait gave up
@@ -106,16 +114,18 @@ static_assert(sizeof(Ctrl) <= 1024, "control block");
 // One work item, decoded the same way by every role.
 struct Item {
   int b, kvh, part;
-  int32_t t0, t1;  // token range; empty when t0 >= t1
+  int32_t t0, t1;  // this CTA's token range; empty when t0 >= t1
   bool len_ok;     // 0 <= seq_len <= max_seq_len
+  bool any;        // the item's whole range (over all CTAs of a cluster) has tokens
 };
 
-// Item k.  With a compact work list (prefix[b] = partitions of sequences
-// before b, kept in shared memory) k runs over existing (sequence, partition,
-// KV head) triples only; otherwise over the full B x Hkv (x NP) space,
-// partition-major, where ranges past a sequence's end come out empty.
-__device__ __forceinline__ Item item_at(const KernelArgs& a, const int32_t* prefix, int64_t k,
-                                        bool v2) {
+// Coordinates of item k (no global memory read).  With a compact work list
+// (prefix[b] = partitions of sequences before b, kept in shared memory) k runs
+// over existing (sequence, partition, KV head) triples only; otherwise over
+// the full B x Hkv (x NP) space, partition-major, where ranges past a
+// sequence's end come out empty.
+__device__ __forceinline__ Item item_coords(const KernelArgs& a, const int32_t* prefix, int64_t k,
+                                            bool v2) {
   Item it;
   if (prefix) {
     const int64_t j = k / a.num_kv_heads;
@@ -135,12 +145,45 @@ __device__ __forceinline__ Item item_at(const KernelArgs& a, const int32_t* pref
     it.b = static_cast<int>(rem / a.num_kv_heads);
     it.kvh = static_cast<int>(rem % a.num_kv_heads);
   }
-  const int32_t L = __ldg(a.seq_lens + it.b);
-  it.len_ok = seq_len_ok(a, L);
   it.t0 = v2 ? it.part * a.partition_size : 0;
-  it.t1 = v2 ? min(L, it.t0 + a.partition_size) : L;
-  if (!it.len_ok) it.t1 = it.t0;
+  it.t1 = it.t0;
+  it.len_ok = false;
+  it.any = false;
   return it;
+}
+
+// The item's token range, given its sequence's length L, and the share of
+// it that CTA `rank` of a cluster of `cs` CTAs streams: a balanced run of
+// the range's 128-token tiles (the whole range when cs == 1).
+__device__ __forceinline__ void item_range(const KernelArgs& a, Item& it, int32_t L, bool v2,
+                                           int rank, int cs) {
+  it.len_ok = seq_len_ok(a, L);
+  it.t1 = !it.len_ok ? it.t0 : (v2 ? min(L, it.t0 + a.partition_size) : L);
+  it.any = it.t0 < it.t1;
+  if (cs > 1 && it.any) {
+    const int ntiles = (it.t1 - it.t0 + kTile - 1) / kTile;
+    const int lo = rank * ntiles / cs, hi = (rank + 1) * ntiles / cs;
+    it.t1 = min(it.t1, it.t0 + hi * kTile);
+    it.t0 += lo * kTile;  // lo < ntiles, so t0 <= t1 (empty when lo == hi)
+  }
+}
+
+__device__ __forceinline__ Item item_at(const KernelArgs& a, const int32_t* prefix, int64_t k,
+                                        bool v2, int rank, int cs) {
+  Item it = item_coords(a, prefix, k, v2);
+  item_range(a, it, __ldg(a.seq_lens + it.b), v2, rank, cs);
+  return it;
+}
+
+// Block-table entry (chunk start c0) / BS + lane of sequence b, for any lane
+// whose entry lies inside the table row (so it may be read before the
+// sequence's length is known; lanes past the chunk are masked afterwards).
+template <int BS>
+__device__ __forceinline__ int32_t load_block_id(const KernelArgs& a, int b, int c0, int lane) {
+  const int idx = c0 / BS + lane;
+  return idx < a.max_blocks_per_seq
+             ? __ldg(a.block_tables + static_cast<int64_t>(b) * a.max_blocks_per_seq + idx)
+             : 0;
 }
 
 __device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
@@ -163,7 +206,7 @@ template <typename T, int D, int BS, bool kV2, int NST, int CPS>
 __global__ void __launch_bounds__(tc::kThreads, CPS)
     pa_tc_kernel(const KernelArgs a, const __grid_constant__ CUtensorMap kmap,
                  const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap qmap,
-                 int64_t grid_items, int compact, long long budget) {
+                 int64_t grid_items, int compact, int cluster, long long budget) {
   using namespace tc;
   using Lay = Layout<D, NST>;
   static_assert(D == 128 || D == 256, "head_dim");
@@ -181,7 +224,16 @@ __global__ void __launch_bounds__(tc::kThreads, CPS)
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = a.group, Hq = a.num_heads;
-  const int64_t stride = gridDim.x;
+  // Clusters of cs CTAs (cs == 1: none) share each work item: cluster cid
+  // takes items cid, cid + clusters, ...; CTA `rank` streams its share of the
+  // item's tokens and the partial results are merged through distributed
+  // shared memory.  Only the one-CTA-per-SM shape is launched in clusters;
+  // the persistent two-CTA shape compiles without any of it.
+  constexpr bool kClusters = NST == kDeepStages;
+  const int cs = kClusters ? cluster : 1;
+  const int rank = kClusters ? static_cast<int>(blockIdx.x % cs) : 0;
+  const int64_t cid = kClusters ? blockIdx.x / cs : blockIdx.x;
+  const int64_t stride = kClusters ? gridDim.x / cs : gridDim.x;
 
   // The grid is persistent, so every CTA starts at once: let the reduce
   // kernel (a programmatic dependent) be scheduled now; it waits for this
@@ -204,6 +256,7 @@ __global__ void __launch_bounds__(tc::kThreads, CPS)
     sm100::mbar_init(&c.tail, 1);
     sm100::mbar_init(&c.drain, 1);
     sm100::mbar_init(&c.never, 1);
+    if (kClusters) sm100::mbar_init(&c.comb_ready, 1);
     c.abort = 0;
   }
   if (warp == 5) {
@@ -260,6 +313,8 @@ __global__ void __launch_bounds__(tc::kThreads, CPS)
   sm100::tc_fence_before();
   __syncthreads();
   sm100::tc_fence_after();
+  // peers' barriers must be initialised before any CTA signals them
+  if (cs > 1) sm100::cluster_sync_all();
   const uint32_t tmem = c.tmem;
   const int64_t total_items = c.total_items;
   volatile int* abort_flag = &c.abort;
@@ -277,47 +332,44 @@ __global__ void __launch_bounds__(tc::kThreads, CPS)
     // next chunk are loaded while the current one streams.
     auto next_active = [&](int64_t k, Item& it) -> int64_t {
       for (; k < total_items; k += stride) {
-        it = item_at(a, prefix, k, kV2);
+        it = item_at(a, prefix, k, kV2, rank, cs);
         if (it.t0 < it.t1) return k;
       }
       return total_items;
     };
-    auto load_ids = [&](const Item& it, int ci, int32_t& y, bool& badl) {
-      const int c0 = it.t0 + ci * kChunk;
-      const int n = min(kChunk, it.t1 - c0);
-      const int nblk = (n + BS - 1) / BS;  // <= 32: one block id per lane
-      int32_t id = 0;
-      badl = false;
-      if (lane < nblk) {
-        id = __ldg(a.block_tables + static_cast<int64_t>(it.b) * a.max_blocks_per_seq + c0 / BS +
-                   lane);
-        badl = id < 0 || id >= a.num_blocks;
-      }
-      // TMA row of the block's first slot; a bad id becomes a negative row,
-      // which TMA fills with zeros instead of reading memory.
-      y = badl ? -BS : (id * a.num_kv_heads + it.kvh) * BS;
+    // TMA row of each lane's block of chunk ci (lanes past the chunk: row 0,
+    // never used); a bad id becomes a negative row, which TMA fills with
+    // zeros instead of reading memory.
+    auto block_rows = [&](const Item& it, int ci, int32_t id, int32_t& y, bool& badl) {
+      const int n = min(kChunk, it.t1 - (it.t0 + ci * kChunk));
+      const int nblk = (n + BS - 1) / BS;  // <= 32: one block per lane
+      badl = lane < nblk && (id < 0 || id >= a.num_blocks);
+      y = lane >= nblk ? 0 : badl ? -BS : (id * a.num_kv_heads + it.kvh) * BS;
     };
 
+    // First item: its length and its first chunk's block ids are loaded
+    // together (one memory latency before the first copy, not two).
     Item it;
-    int64_t k = next_active(blockIdx.x, it);
+    int64_t k = cid;
+    int32_t raw = 0;
+    if (k < total_items) {
+      it = item_coords(a, prefix, k, kV2);
+      const int32_t L = __ldg(a.seq_lens + it.b);
+      const int32_t t_spec = it.t0;
+      raw = load_block_id<BS>(a, it.b, t_spec, lane);
+      item_range(a, it, L, kV2, rank, cs);
+      if (it.t0 < it.t1 && it.t0 != t_spec) raw = load_block_id<BS>(a, it.b, it.t0, lane);
+      if (it.t0 >= it.t1) {
+        k = next_active(k + stride, it);
+        if (k < total_items) raw = load_block_id<BS>(a, it.b, it.t0, lane);
+      }
+    }
     int ci = 0;
     int32_t y = 0;
     bool badl = false;
-    if (k < total_items) load_ids(it, 0, y, badl);
+    if (k < total_items) block_rows(it, 0, raw, y, badl);
     while (k < total_items && ok) {
       const int nchunks = (it.t1 - it.t0 + kChunk - 1) / kChunk;
-      // look ahead: the next chunk and its block ids
-      Item it2 = it;
-      int64_t k2 = k;
-      int ci2 = ci + 1;
-      if (ci2 >= nchunks) {
-        k2 = next_active(k + stride, it2);
-        ci2 = 0;
-      }
-      int32_t y2 = 0;
-      bool bad2 = false;
-      if (k2 < total_items) load_ids(it2, ci2, y2, bad2);
-
       if (__any_sync(0xffffffffu, badl) && lane == 0) set_status(a.status, PA_ERR_BAD_BLOCK_ID);
       if (ci == 0) {
         // q rows of the item's query heads (8 rows; rows past G are ignored)
@@ -352,6 +404,25 @@ __global__ void __launch_bounds__(tc::kThreads, CPS)
           ++g;
         }
       }
+      // Look ahead while the values stream: the next chunk (of this item, or
+      // the next item's first) and its block ids.  The loads are only issued
+      // here; their results are first used after the value stages.
+      Item it2 = it;
+      int64_t k2 = k;
+      int ci2 = ci + 1;
+      int32_t L2 = 0;
+      const bool same_item = ci2 < nchunks;
+      if (!same_item) {
+        k2 = k + stride;
+        ci2 = 0;
+        if (k2 < total_items) {
+          it2 = item_coords(a, prefix, k2, kV2);
+          L2 = __ldg(a.seq_lens + it2.b);
+        }
+      }
+      int32_t raw2 = 0;
+      const int32_t t2_spec = it2.t0 + ci2 * kChunk;
+      if (k2 < total_items) raw2 = load_block_id<BS>(a, it2.b, t2_spec, lane);
       const int nv = (n + Lay::kVTokens - 1) / Lay::kVTokens;
       for (int v = 0; v < nv && ok; ++v) {
         const int jb0 = v * Lay::kVTokens / BS;
@@ -393,11 +464,18 @@ __global__ void __launch_bounds__(tc::kThreads, CPS)
           if (lane == 0) sm100::mbar_arrive(&c.full[slot]);  // no bytes: the data is there
         }
       }
+      if (!same_item && k2 < total_items) {
+        item_range(a, it2, L2, kV2, rank, cs);
+        if (it2.t0 < it2.t1 && it2.t0 != t2_spec) raw2 = load_block_id<BS>(a, it2.b, it2.t0, lane);
+        if (it2.t0 >= it2.t1) {  // an empty item: find the next one with tokens
+          k2 = next_active(k2 + stride, it2);
+          if (k2 < total_items) raw2 = load_block_id<BS>(a, it2.b, it2.t0, lane);
+        }
+      }
       k = k2;
       ci = ci2;
       it = it2;
-      y = y2;
-      badl = bad2;
+      if (k < total_items) block_rows(it, ci, raw2, y, badl);
     }
     if (!ok) {
       if (lane == 0) fail(c, a.status);
@@ -423,8 +501,8 @@ __global__ void __launch_bounds__(tc::kThreads, CPS)
       // diagnostic: wait for an event that never happens, so the bounded
       // wait runs out and the abort path is exercised
       if (a.selftest_stall) ok = sm100::mbar_wait(&c.never, 0, budget, abort_flag);
-      for (int64_t k = blockIdx.x; k < total_items && ok; k += stride) {
-        const Item it = item_at(a, prefix, k, kV2);
+      for (int64_t k = cid; k < total_items && ok; k += stride) {
+        const Item it = item_at(a, prefix, k, kV2, rank, cs);
         if (it.t0 >= it.t1) continue;
         const int qb = qn & 1;
         ok = sm100::mbar_wait(&c.qfull[qb], (qn >> 1) & 1, budget, abort_flag);
@@ -504,16 +582,94 @@ __global__ void __launch_bounds__(tc::kThreads, CPS)
     const int r = tid;  // tensor-memory lane: token of a tile, or head_dim row
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     const float sl2 = a.scale_log2;
-    uint32_t cc = 0;
-    for (int64_t k = blockIdx.x; k < total_items; k += stride) {
-      const Item it = item_at(a, prefix, k, kV2);
+    // Cluster combine of the cluster's item (the host launches one cluster
+    // per item, so each CTA combines once and no buffer is reused).  The CTA
+    // that merges head_dim elements [r * D / cs, (r + 1) * D / cs) is CTA r:
+    // every CTA pushes its unnormalised P.V sums for those elements, and its
+    // running max (log2 units), running sum and poison flag, into CTA r's
+    // combine buffer with remote stores counted on CTA r's mbarrier; CTA r
+    // then merges them with the same log-sum-exp identity as the V2 reduce
+    // and writes the output.
+    auto combine = [&](const float (&acc)[Lay::kHalves][8], const float (&m_run)[8],
+                       const float (&s_run)[8], bool poison, const Item& it, int64_t row0,
+                       uint64_t keep_l2, uint32_t ic) {
+      const int dn = D / cs;  // head_dim elements each CTA merges
+      // receive side: its own buffer, since a peer may push while this CTA's
+      // last P.V still reads its P^T
+      float* recv = reinterpret_cast<float*>(smem + Lay::kCombOff);  // [cs][8][dn] sums
+      float* rst = recv + 8 * D;                                     // [cs][20] statistics
+      const uint32_t bar_s = sm100::smem_u32(&c.comb_ready);
+      if (tid == 0)
+        sm100::mbar_arrive_expect_tx(&c.comb_ready,
+                                     static_cast<uint32_t>(cs * (G * dn + 20) * 4));
+      // send side: stage the sums in the P^T buffer (idle: this CTA's last
+      // P.V has completed) and push them as 16-byte pieces
+      float* xo = reinterpret_cast<float*>(pt);  // [8][D]
+#pragma unroll
+      for (int j = 0; j < Lay::kHalves; ++j)
+#pragma unroll
+        for (int h = 0; h < 8; ++h)
+          if (h < G) xo[h * D + j * 128 + tid] = acc[j][h];
+      softmax_sync();
+      for (int u = tid; u < G * (D / 4); u += 128) {
+        const int h = u / (D / 4), d = (u % (D / 4)) * 4;
+        const uint32_t owner = static_cast<uint32_t>(d / dn);
+        const float4 v = *reinterpret_cast<const float4*>(xo + h * D + d);
+        sm100::st_async_v4(
+            sm100::mapa_shared(sm100::smem_u32(recv + (rank * 8 + h) * dn + d % dn), owner), v,
+            sm100::mapa_shared(bar_s, owner));
+      }
+      if (tid < cs) {  // statistics: max[8], sum[8], poison, padding
+        const uint32_t dst = sm100::mapa_shared(sm100::smem_u32(rst + rank * 20), tid);
+        const uint32_t bar = sm100::mapa_shared(bar_s, tid);
+        sm100::st_async_v4(dst, make_float4(m_run[0], m_run[1], m_run[2], m_run[3]), bar);
+        sm100::st_async_v4(dst + 16, make_float4(m_run[4], m_run[5], m_run[6], m_run[7]), bar);
+        sm100::st_async_v4(dst + 32, make_float4(s_run[0], s_run[1], s_run[2], s_run[3]), bar);
+        sm100::st_async_v4(dst + 48, make_float4(s_run[4], s_run[5], s_run[6], s_run[7]), bar);
+        sm100::st_async_v4(dst + 64, make_float4(poison ? 1.f : 0.f, 0.f, 0.f, 0.f), bar);
+      }
+      const bool ready = sm100::mbar_wait_cluster(&c.comb_ready, ic & 1, budget, abort_flag);
+      if (!ready) fail(c, a.status);
+      // merge: each thread derives its head's weights from the statistics
+      bool pz = !ready;
+      for (int q = 0; q < cs; ++q) pz |= rst[q * 20 + 16] != 0.f;
+      for (int i = tid; i < G * dn; i += 128) {
+        const int h = i / dn, dl = i % dn, d = rank * dn + dl;
+        float M = -INFINITY;
+        for (int q = 0; q < cs; ++q) M = fmaxf(M, rst[q * 20 + h]);
+        float S = 0.f, O = 0.f;
+        for (int q = 0; q < cs; ++q) {
+          const float mq = rst[q * 20 + h];
+          const float f = mq == -INFINITY ? 0.f : exp2f(mq - M);
+          S = fmaf(rst[q * 20 + 8 + h], f, S);
+          O = fmaf(recv[(q * 8 + h) * dn + dl], f, O);
+        }
+        const float o = pz ? qnan() : O / S;
+        if constexpr (kV2) {
+          sm100::st_f32_policy(a.tmp_out + ((row0 + h) * a.num_partitions + it.part) * D + d, o,
+                               keep_l2);
+          if (rank == 0 && dl == 0) {
+            const int64_t w = (row0 + h) * a.num_partitions + it.part;
+            sm100::st_f32_policy(a.max_logits + w, pz ? qnan() : M * kLn2, keep_l2);
+            sm100::st_f32_policy(a.exp_sums + w, S, keep_l2);
+          }
+        } else {
+          store_out(a.out, (row0 + h) * D + d, a.out_dtype, o);
+        }
+      }
+    };
+    uint32_t cc = 0, ic = 0;  // chunks / cluster combines so far
+    for (int64_t k = cid; k < total_items; k += stride) {
+      const Item it = item_at(a, prefix, k, kV2, rank, cs);
       const int64_t row0 = static_cast<int64_t>(it.b) * Hq + it.kvh * G;
-      if (it.t0 >= it.t1) {
-        if (!it.len_ok && it.part == 0 && it.kvh == 0 && tid == 0)
-          set_status(a.status, PA_ERR_BAD_SEQ_LEN);
-        if (!kV2) {  // V1 row of a sequence with nothing to attend to
-          const float v = it.len_ok ? 0.f : qnan();
-          for (int i = tid; i < G * D; i += 128) store_out(a.out, row0 * D + i, a.out_dtype, v);
+      if (!it.any) {  // nothing to attend to in the whole item
+        if (rank == 0) {
+          if (!it.len_ok && it.part == 0 && it.kvh == 0 && tid == 0)
+            set_status(a.status, PA_ERR_BAD_SEQ_LEN);
+          if (!kV2) {  // V1 row of a sequence with nothing to attend to
+            const float v = it.len_ok ? 0.f : qnan();
+            for (int i = tid; i < G * D; i += 128) store_out(a.out, row0 * D + i, a.out_dtype, v);
+          }
         }
         continue;
       }
@@ -635,6 +791,11 @@ __global__ void __launch_bounds__(tc::kThreads, CPS)
       // them in L2 (the key / value stream is marked evict-first)
       const uint64_t keep_l2 = sm100::l2_evict_last_policy();
       const bool poison = bad || *abort_flag != 0;
+      if (cs > 1) {
+        combine(acc, m_run, s_run, poison, it, row0, keep_l2, ic);
+        ++ic;
+        continue;
+      }
 #pragma unroll
       for (int j = 0; j < Lay::kHalves; ++j) {
         const int d = j * 128 + tid;
@@ -669,13 +830,29 @@ __global__ void __launch_bounds__(tc::kThreads, CPS)
   __syncthreads();
   sm100::tc_fence_after();
   if (warp == 5) sm100::tmem_dealloc(tmem, kTmemCols);
+  // no CTA leaves while a peer may still read its shared memory
+  if (cs > 1) sm100::cluster_sync_all();
+}
+
+// Kernel attributes, set once per device: the dynamic shared memory, and for
+// the one-CTA-per-SM variant clusters of up to 16 CTAs.
+template <typename T, int D, int BS, bool V2, int NST, int CPS>
+cudaError_t configure_tc(int dev) {
+  static bool configured[128] = {};
+  if (configured[dev]) return cudaSuccess;
+  auto kern = pa_tc_kernel<T, D, BS, V2, NST, CPS>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       tc::Layout<D, NST>::kSmemCompact);
+  if (e == cudaSuccess && NST == tc::kDeepStages)
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e == cudaSuccess) configured[dev] = true;
+  return e;
 }
 
 template <typename T, int D, int BS, bool V2, int NST, int CPS>
 cudaError_t launch_tc_variant(const KernelArgs& a, const CUtensorMap& km, const CUtensorMap& vm,
                               const CUtensorMap& qm, int64_t items, unsigned grid, int compact,
-                              cudaStream_t s) {
-  static bool configured[128] = {};
+                              int cs, cudaStream_t s) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
   auto kern = pa_tc_kernel<T, D, BS, V2, NST, CPS>;
@@ -683,15 +860,59 @@ cudaError_t launch_tc_variant(const KernelArgs& a, const CUtensorMap& km, const 
   // the compact work list's prefix table only takes shared memory when used,
   // which leaves room on each SM for the reduce kernel's waiting CTAs
   const int smem = compact ? Lay::kSmemCompact : Lay::kSmem;
-  if (!configured[dev]) {
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmemCompact);
-    if (e != cudaSuccess) return e;
-    configured[dev] = true;
-  }
+  if (cudaError_t e = configure_tc<T, D, BS, V2, NST, CPS>(dev)) return e;
   const long long budget = a.selftest_stall ? tc::kSelftestWaitBudget : tc::kDefaultWaitBudget;
-  kern<<<grid, tc::kThreads, smem, s>>>(a, km, vm, qm, items, compact, budget);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(tc::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = cs > 1 ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, a, km, vm, qm, items, compact, cs, budget);
+}
+
+// Largest cluster size <= want (a power of two) of which at least `need`
+// clusters of the one-CTA-per-SM variant can be resident at once.  The
+// resident-cluster counts are queried once per device and size.
+template <typename T, int D, int BS, bool V2>
+int fit_cluster(int want, int64_t need) {
+  static int resident[128][5];  // [device][log2 size], 0 = not queried yet
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 1;
+  if (configure_tc<T, D, BS, V2, tc::kDeepStages, 1>(dev) != cudaSuccess) return 1;
+  auto kern = pa_tc_kernel<T, D, BS, V2, tc::kDeepStages, 1>;
+  int lg = 0;
+  while ((2 << lg) <= want && lg < 4) ++lg;  // log2 of the largest power of two <= want
+  for (; lg >= 1; --lg) {
+    const int cs = 1 << lg;
+    if (resident[dev][lg] == 0) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(static_cast<unsigned>(cs), 1, 1);
+      cfg.blockDim = dim3(tc::kThreads, 1, 1);
+      cfg.dynamicSmemBytes = static_cast<size_t>(tc::Layout<D, tc::kDeepStages>::kSmemCompact);
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        cudaGetLastError();  // a refused size is not an error of the decode call
+        n = 0;
+      }
+      resident[dev][lg] = n > 0 ? n : -1;
+    }
+    if (resident[dev][lg] >= need) return cs;
+  }
+  return 1;
 }
 
 template <typename T, int D, int BS>
@@ -702,10 +923,23 @@ cudaError_t launch_tc_t(const KernelArgs& a, const CUtensorMap& km, const CUtens
                         (v2 ? a.num_partitions : 1);
   if (items == 0) return cudaSuccess;
   const int compact = (v2 && a.num_seqs > 1 && a.num_seqs <= tc::kMaxCompactSeqs) ? 1 : 0;
-  if (items < num_sms) {  // few items: one deep-ring CTA each
-    const unsigned grid = static_cast<unsigned>(items);
-    return v2 ? launch_tc_variant<T, D, BS, true, 12, 1>(a, km, vm, qm, items, grid, compact, s)
-              : launch_tc_variant<T, D, BS, false, 12, 1>(a, km, vm, qm, items, grid, compact, s);
+  if (items < num_sms) {
+    // Few items: one deep-ring CTA per SM, and when at most half the SMs
+    // would be busy, each item is shared by a cluster of cs CTAs (up to 16)
+    // that split its 128-token tiles and merge their partial results -- as
+    // long as every CTA keeps at least four tiles (512 tokens), below which
+    // the merge costs more than the split saves.
+    const int range = v2 ? std::min(a.partition_size, a.max_seq_len) : a.max_seq_len;
+    const int tiles = (range + tc::kTile - 1) / tc::kTile;
+    int want = 1;
+    while (want < 16 && items * want * 2 <= num_sms && want * 2 * 4 <= tiles) want *= 2;
+    const int cs = want > 1 ? (v2 ? fit_cluster<T, D, BS, true>(want, items)
+                                  : fit_cluster<T, D, BS, false>(want, items))
+                            : 1;
+    const unsigned grid = static_cast<unsigned>(items * cs);
+    return v2 ? launch_tc_variant<T, D, BS, true, tc::kDeepStages, 1>(a, km, vm, qm, items, grid, compact, cs, s)
+              : launch_tc_variant<T, D, BS, false, tc::kDeepStages, 1>(a, km, vm, qm, items, grid, compact, cs,
+                                                          s);
   }
   // Persistent grid: at most two CTAs per SM.  When the items are all the
   // same size (not a compact work list) the grid is sized so every CTA does
@@ -718,8 +952,8 @@ cudaError_t launch_tc_t(const KernelArgs& a, const CUtensorMap& km, const CUtens
     grid64 = (items + rounds - 1) / rounds;
   }
   const unsigned grid = static_cast<unsigned>(grid64);
-  return v2 ? launch_tc_variant<T, D, BS, true, 5, 2>(a, km, vm, qm, items, grid, compact, s)
-            : launch_tc_variant<T, D, BS, false, 5, 2>(a, km, vm, qm, items, grid, compact, s);
+  return v2 ? launch_tc_variant<T, D, BS, true, 5, 2>(a, km, vm, qm, items, grid, compact, 1, s)
+            : launch_tc_variant<T, D, BS, false, 5, 2>(a, km, vm, qm, items, grid, compact, 1, s);
 }
 
 template <typename T>

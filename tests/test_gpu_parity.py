@@ -47,6 +47,9 @@ SMALL = [
      (512, 96)),
     ("f16_gqa", wl.scaled(wl.WORKLOADS["gqa_8k"], seq_len=777, dtype=torch.float16), None,
      (256,)),
+    # long enough that V1 (and V2 at P = 1024) share each item across a cluster
+    ("f16_gqa_split", wl.scaled(wl.WORKLOADS["gqa_8k"], seq_len=3001, dtype=torch.float16),
+     None, (1024,)),
     ("f32_d128", wl.scaled(wl.WORKLOADS["serving_256"], num_seqs=3, max_len=700,
                            dtype=torch.float32), None, (64,)),
 ]
@@ -224,6 +227,26 @@ def test_bad_seq_len_poisons_the_row_and_sets_status():
         assert_close(got[0], ref[0], 2e-3, "untouched row")
         if path == "v2":
             assert pa.read_device_status(ws) == pa.PA_ERR_BAD_SEQ_LEN
+
+
+def test_bad_inputs_on_split_items():
+    """Tensor-core shapes whose items are shared by a cluster of CTAs (V1 and
+    small V2 batches): a bad block id inside one CTA's share poisons the
+    whole row, a bad seq_len poisons its row, the other rows stay exact."""
+    lens = (3000, 2500, 2000)
+    good = problem(dtype=torch.bfloat16, lens=lens, Hq=12, Hkv=2, D=256, BS=16, seed=13)
+    ref = _ref(good)
+    bc = problem(dtype=torch.bfloat16, lens=lens, Hq=12, Hkv=2, D=256, BS=16, seed=13)
+    bc.block_tables[0, 150] = -7                              # token 2400: a late share
+    bg = bc.to("cuda")
+    bg.seq_lens[2] = 3001                                     # > max_seq_len promised
+    for path in ("v1", "v2"):
+        got, ws = run(bg, path=path, partition_size=1024, return_ws=True, check_status=False)
+        assert np.all(np.isnan(got[0])), path
+        assert np.all(np.isnan(got[2])), path
+        assert_close(got[1], ref[1], 2e-3, f"untouched row {path}")
+        if path == "v2":
+            assert pa.read_device_status(ws) in (pa.PA_ERR_BAD_BLOCK_ID, pa.PA_ERR_BAD_SEQ_LEN)
 
 
 # ---------------------------------------------------------------------------
