@@ -213,6 +213,34 @@ PA_API pa_status_t pa_decode_v2_static(const pa_params_t* params, const void* q,
                                        const int32_t* block_tables, const int32_t* seq_lens,
                                        void* out, cudaStream_t stream);
 
+/*
+ * The decode step from host memory.  The per-step inputs -- q, block_tables
+ * and seq_lens -- are read from HOST buffers and `out` is written to a HOST
+ * buffer; k_cache, v_cache and the workspace are device memory that stays
+ * resident between steps.  The call enqueues on `stream` the three
+ * host-to-device copies into `staging`, the pa_decode step (V1 or V2 by the
+ * same threshold) and the device-to-host copy of the result, then WAITS for
+ * the stream: `out_host` is complete when it returns PA_OK.  It is therefore
+ * not for use inside stream capture.
+ *   staging    caller-owned device memory of pa_host_staging_size(params)
+ *              bytes, 256-byte aligned; it holds the copied inputs and the
+ *              result (q | block_tables | seq_lens | out, each on a 256-byte
+ *              boundary) and may hold anything between calls.
+ *   host buffers: page-locked memory (cudaHostAlloc / pinned tensors) makes
+ *              the copies asynchronous DMA; pageable memory also works, with
+ *              the copies staged by the CUDA driver.
+ * Errors: the checks of pa_decode, a null or misaligned staging buffer
+ * (PA_ERR_INVALID_ARG / PA_ERR_MISALIGNED), staging_bytes too small
+ * (PA_ERR_WORKSPACE_TOO_SMALL), all before anything is enqueued; a failed
+ * copy or wait gives PA_ERR_CUDA.
+ */
+PA_API size_t pa_host_staging_size(const pa_params_t* params);
+PA_API pa_status_t pa_decode_host(const pa_params_t* params, const void* q_host,
+                                  const void* k_cache, const void* v_cache,
+                                  const int32_t* block_tables_host, const int32_t* seq_lens_host,
+                                  void* workspace, size_t workspace_bytes, void* staging,
+                                  size_t staging_bytes, void* out_host, cudaStream_t stream);
+
 /* Which path pa_decode takes for these parameters: 1 (V1), 2 (V2) or 0 if
  * the parameters are invalid.  Pure host function. */
 PA_API int pa_decode_path(const pa_params_t* params);

@@ -7,8 +7,9 @@ and raises :class:`PaError` on a non-OK status.  There is no fallback: if
 ``libpa.so`` has not been built, every call raises.
 
 Functions mirror the C entry points: :func:`workspace_size`,
-:func:`decode_v1`, :func:`decode_v2`, :func:`decode`, :func:`decode_path`,
-:func:`status_string`, :func:`workspace_init`, :func:`read_device_status`.
+:func:`decode_v1`, :func:`decode_v2`, :func:`decode`, :func:`decode_host`,
+:func:`decode_path`, :func:`status_string`, :func:`workspace_init`,
+:func:`read_device_status`.
 """
 from __future__ import annotations
 
@@ -38,7 +39,7 @@ DEFAULT_V1_MAX_SEQ_LEN = 8192
 EXPORTS = ("pa_workspace_size", "pa_decode_v1", "pa_decode_v2", "pa_decode_v2_partitions",
            "pa_decode_v2_reduce", "pa_decode", "pa_decode_path", "pa_status_string",
            "pa_workspace_init", "pa_read_device_status", "pa_version", "pa_decode_v2_static",
-           "pa_decode_kernel")
+           "pa_decode_kernel", "pa_host_staging_size", "pa_decode_host")
 PA_STATIC_WORKSPACE_BYTES = 16 << 20
 
 
@@ -109,6 +110,11 @@ def lib() -> ctypes.CDLL:
             L.pa_version.restype = ctypes.c_int
             L.pa_decode_v2_static.argtypes = [PP, P, P, P, P, P, P, P]
             L.pa_decode_v2_static.restype = ctypes.c_int
+            L.pa_host_staging_size.argtypes = [PP]
+            L.pa_host_staging_size.restype = ctypes.c_size_t
+            L.pa_decode_host.argtypes = [PP, P, P, P, P, P, P, ctypes.c_size_t, P, ctypes.c_size_t,
+                                         P, P]
+            L.pa_decode_host.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -273,6 +279,54 @@ def decode_v2_static(q, k_cache, v_cache, block_tables, seq_lens, out, *, max_se
                                    _ptr(block_tables), _ptr(seq_lens), _ptr(out), _stream(stream))
     if st != PA_OK:
         raise PaError(st, "pa_decode_v2_static")
+    return out
+
+
+def host_staging_size(params: Params) -> int:
+    return int(lib().pa_host_staging_size(ctypes.byref(params)))
+
+
+def alloc_host_staging(params: Params, device=None):
+    """A CUDA uint8 tensor of :func:`host_staging_size` bytes for
+    :func:`decode_host` (allocated by torch, reused across calls)."""
+    import torch
+    n = host_staging_size(params)
+    if n == 0:
+        raise PaError(PA_ERR_INVALID_ARG, "pa_host_staging_size")
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def decode_host(q, k_cache, v_cache, block_tables, seq_lens, out, workspace, staging, *,
+                max_seq_len: int = 0, scale: float = 0.0, partition_size: int = 512,
+                v1_max_seq_len: int = DEFAULT_V1_MAX_SEQ_LEN, portable: bool = False,
+                params: Params | None = None, stream=None):
+    """``pa_decode_host``: the decode step with q, block_tables, seq_lens and
+    ``out`` in HOST memory (CPU tensors; pinned ones make the copies
+    asynchronous), the caches and ``workspace`` (None for V1) and
+    ``staging`` (see :func:`alloc_host_staging`) on the device.  Returns when
+    ``out`` holds the result.  ``params`` (from :func:`make_params`) may be
+    passed to reuse one description across steps."""
+    if params is None:
+        import torch
+        for name, t in (("q", q), ("block_tables", block_tables), ("seq_lens", seq_lens),
+                        ("out", out)):
+            if t.is_cuda or not t.is_contiguous():
+                raise PaError(PA_ERR_INVALID_ARG, f"{name} must be a contiguous host tensor")
+        for name, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+            if not t.is_cuda or not t.is_contiguous():
+                raise PaError(PA_ERR_INVALID_ARG, f"{name} must be a contiguous CUDA tensor")
+        if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+            raise PaError(PA_ERR_INVALID_ARG, "block_tables and seq_lens must be int32")
+        if tuple(out.shape) != tuple(q.shape):
+            raise PaError(PA_ERR_INVALID_ARG, "out must have q's shape")
+        params = _params_for(q, k_cache, block_tables, out, max_seq_len, scale, partition_size,
+                             v1_max_seq_len, portable)
+    nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib().pa_decode_host(ctypes.byref(params), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                              _ptr(block_tables), _ptr(seq_lens), _ptr(workspace), nbytes,
+                              _ptr(staging), staging.numel(), _ptr(out), _stream(stream))
+    if st != PA_OK:
+        raise PaError(st, "pa_decode_host")
     return out
 
 

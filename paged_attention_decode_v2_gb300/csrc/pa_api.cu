@@ -21,6 +21,8 @@ size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 bool aligned(const void* p, uintptr_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
 
+}  // namespace
+
 // Checks shared by every decode entry point; `v2` adds the partition rules.
 pa_status_t check_params(const pa_params_t* p, bool v2) {
   if (!p) return PA_ERR_INVALID_ARG;
@@ -43,6 +45,8 @@ pa_status_t check_params(const pa_params_t* p, bool v2) {
   }
   return PA_OK;
 }
+
+namespace {
 
 int32_t threshold(const pa_params_t* p) {
   return p->v1_max_seq_len > 0 ? p->v1_max_seq_len : kDefaultV1MaxSeqLen;

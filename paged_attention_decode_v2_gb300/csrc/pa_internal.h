@@ -43,6 +43,8 @@ cudaError_t launch_generic_f32(const KernelArgs& a, bool v2, cudaStream_t s);
 cudaError_t launch_generic_bf16(const KernelArgs& a, bool v2, cudaStream_t s);
 cudaError_t launch_generic_f16(const KernelArgs& a, bool v2, cudaStream_t s);
 cudaError_t launch_reduce(const KernelArgs& a, cudaStream_t s, bool pdl);
+// Parameter checks of every decode entry point (`v2`: the partition rules too).
+pa_status_t check_params(const pa_params_t* p, bool v2);
 
 // Tensor-core path (pa_tc_host.cu): whether it serves these parameters on
 // the current device, and its launch (pass 1 for V2, the whole pass for V1).

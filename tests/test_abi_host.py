@@ -168,3 +168,20 @@ def test_decode_kernel_query(L):
     assert pa.decode_kernel(params(kv_dtype=pa.PA_F32)) == 1
     assert pa.decode_kernel(params(num_heads=36, num_kv_heads=4)) == 1   # group 9 > 8
     assert pa.decode_kernel(params()) in (1, 2)
+
+
+def test_host_staging_size_and_checks(L):
+    """pa_host_staging_size: q | block_tables | seq_lens | out, each rounded to
+    256 bytes; pa_decode_host refuses a missing, misaligned or short staging
+    buffer before it enqueues anything."""
+    r = lambda x: (x + 255) // 256 * 256
+    p = params(num_seqs=2, max_blocks_per_seq=6250)
+    want = r(2 * 24 * 256 * 2) + r(2 * 6250 * 4) + r(2 * 4) + r(2 * 24 * 256 * 4)
+    assert pa.host_staging_size(p) == want
+    assert pa.host_staging_size(params(num_heads=25)) == 0          # invalid parameters
+    fake = ctypes.c_void_p(0x10000)                                   # never dereferenced
+    call = lambda staging, nbytes: L.pa_decode_host(ctypes.byref(p), fake, fake, fake, fake, fake,
+                                                    fake, 1 << 30, staging, nbytes, fake, None)
+    assert call(None, want) == pa.PA_ERR_INVALID_ARG
+    assert call(ctypes.c_void_p(0x10008), want) == pa.PA_ERR_MISALIGNED
+    assert call(ctypes.c_void_p(0x10000), want - 1) == pa.PA_ERR_WORKSPACE_TOO_SMALL

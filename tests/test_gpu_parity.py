@@ -279,3 +279,24 @@ def test_full_size_workload(name):
             got = run(bg, path=path, partition_size=P).reshape(rows_all, w.head_dim)
             assert_close(got[rows], ref, tol, f"{name} {path} P={P}")
             assert np.all(np.isfinite(got)), "every row finite"
+
+
+def test_decode_from_host_buffers_matches_device_call():
+    """pa_decode_host (host q / block table / lengths / out, pinned) gives the
+    same bits as pa_decode on device copies of the same inputs, on both
+    paths."""
+    for L, v1max in ((3000, pa.DEFAULT_V1_MAX_SEQ_LEN), (3000, 1024)):
+        bc = wl.make(wl.scaled(wl.WORKLOADS["mixed_32"], num_seqs=3, max_len=L), poison=True)
+        bg = bc.to("cuda")
+        params = pa.make_params(bc.q, bc.k_cache, bc.block_tables, max_seq_len=bc.max_seq_len,
+                                scale=bc.scale, out_dtype=torch.float32, v1_max_seq_len=v1max)
+        ws = pa.alloc_workspace(params) if pa.decode_path(params) == 2 else None
+        ref = run(bg, path="decode", v1_max_seq_len=v1max)
+        staging = pa.alloc_host_staging(params)
+        out_h = torch.empty(tuple(bc.q.shape), dtype=torch.float32).pin_memory()
+        pa.decode_host(bc.q.pin_memory(), bg.k_cache, bg.v_cache, bc.block_tables.pin_memory(),
+                       bc.seq_lens.pin_memory(), out_h, ws, staging, max_seq_len=bc.max_seq_len,
+                       scale=bc.scale, v1_max_seq_len=v1max)
+        assert np.array_equal(out_h.double().numpy(), ref), f"path {pa.decode_path(params)}"
+        if ws is not None:
+            assert pa.read_device_status(ws) == pa.PA_OK
