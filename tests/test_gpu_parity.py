@@ -300,3 +300,38 @@ def test_decode_from_host_buffers_matches_device_call():
         assert np.array_equal(out_h.double().numpy(), ref), f"path {pa.decode_path(params)}"
         if ws is not None:
             assert pa.read_device_status(ws) == pa.PA_OK
+
+
+def test_cuda_graph_capture_and_replay():
+    """pa_decode captured once in a CUDA graph (V2 with its programmatic-
+    dependent reduce, and V1 with clustered CTAs) and replayed with new q and
+    shorter sequence lengths copied into the captured buffers: every replay
+    matches the oracle on that replay's inputs."""
+    cases = [(wl.scaled(wl.WORKLOADS["long_100k"], seq_len=20000), 512),
+             (wl.WORKLOADS["gqa_8k"], 512)]
+    for w, P in cases:
+        bc = wl.make(w, poison=True)
+        bg = bc.to("cuda")
+        params = pa.make_params(bc.q, bc.k_cache, bc.block_tables, max_seq_len=bc.max_seq_len,
+                                scale=bc.scale, partition_size=P, out_dtype=torch.float32)
+        ws = pa.alloc_workspace(params) if pa.decode_path(params) == 2 else None
+        out = torch.empty(tuple(bc.q.shape), device="cuda")
+        kw = dict(max_seq_len=bc.max_seq_len, scale=bc.scale, partition_size=P)
+        pa.decode(bg.q, bg.k_cache, bg.v_cache, bg.block_tables, bg.seq_lens, out, ws, **kw)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            pa.decode(bg.q, bg.k_cache, bg.v_cache, bg.block_tables, bg.seq_lens, out, ws, **kw)
+        g = torch.Generator().manual_seed(77)
+        for cut in (0, 777, 4099):
+            q_new = torch.randn(tuple(bc.q.shape), generator=g).to(bc.q.dtype)
+            lens = (bc.seq_lens - cut).clamp(min=1)
+            bg.q.copy_(q_new)
+            bg.seq_lens.copy_(lens)
+            graph.replay()
+            torch.cuda.synchronize()
+            ref = oracle.decode(q_new, bc.k_cache, bc.v_cache, bc.block_tables, lens, bc.scale)
+            assert_close(out.double().cpu().numpy(), ref, 2e-3,
+                         f"graph replay path {pa.decode_path(params)} cut {cut}")
+        if ws is not None:
+            assert pa.read_device_status(ws) == pa.PA_OK
