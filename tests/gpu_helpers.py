@@ -10,21 +10,48 @@ import paged_attention_decode_v2_gb300 as pa
 TOL = {torch.float32: 1e-5, torch.bfloat16: 2e-3, torch.float16: 2e-3}
 
 
+GUARD_BYTES = 4096          # canary region on each side of out and the workspace
+GUARD_F = -4096.0           # canary of out's guards (exact in f32, bf16 and f16)
+GUARD_B = 0xA5              # canary byte of the workspace's guards
+
+
+def _guarded(n_elems, dtype, fill, device):
+    """A tensor of n_elems elements with GUARD_BYTES of canaries on each side
+    (the interior stays 256-byte aligned): returns (whole, interior)."""
+    esz = torch.tensor([], dtype=dtype).element_size()
+    g = GUARD_BYTES // esz
+    whole = torch.empty(n_elems + 2 * g, dtype=dtype, device=device)
+    whole.fill_(fill)
+    return whole, whole[g:g + n_elems]
+
+
+def _guards_intact(whole, n_elems, fill):
+    g = GUARD_BYTES // whole.element_size()
+    lo, hi = whole[:g], whole[g + n_elems:]
+    return bool((lo == fill).all().item()) and bool((hi == fill).all().item())
+
+
 def run(batch, path="decode", partition_size=512, portable=False, out_dtype=torch.float32,
         v1_max_seq_len=pa.DEFAULT_V1_MAX_SEQ_LEN, workspace=None, return_ws=False,
         check_status=True):
     """Run one decode step of ``batch`` (already on the GPU); returns out as a
     float64 numpy array (and the workspace tensor when asked).  When a
     workspace was used, its device status word must read OK afterwards
-    (unless ``check_status`` is False)."""
+    (unless ``check_status`` is False).  ``out`` and a workspace made here
+    sit between canary regions that must be untouched after the call (no
+    write outside the buffers the call was given)."""
     b = batch
-    out = torch.full(tuple(b.q.shape), float("nan"), dtype=out_dtype, device=b.q.device)
+    n_out = int(np.prod(tuple(b.q.shape)))
+    out_whole, out_flat = _guarded(n_out, out_dtype, GUARD_F, b.q.device)
+    out_flat.fill_(float("nan"))
+    out = out_flat.view(tuple(b.q.shape))
     params = pa.make_params(b.q, b.k_cache, b.block_tables, max_seq_len=b.max_seq_len,
                             scale=b.scale, partition_size=partition_size, out_dtype=out_dtype,
                             v1_max_seq_len=v1_max_seq_len, portable=portable)
+    ws_whole = None
     if workspace is None and path in ("v2", "decode"):
         n = pa.workspace_size(params)
-        workspace = torch.empty(n, dtype=torch.uint8, device=b.q.device)
+        ws_whole, workspace = _guarded(n, torch.uint8, GUARD_B, b.q.device)
         workspace.view(torch.float32)[64:].fill_(float("nan"))   # poison all but the status
         pa.workspace_init(workspace)
     kw = dict(max_seq_len=b.max_seq_len, scale=b.scale, portable=portable)
@@ -37,6 +64,9 @@ def run(batch, path="decode", partition_size=512, portable=False, out_dtype=torc
         pa.decode(b.q, b.k_cache, b.v_cache, b.block_tables, b.seq_lens, out, workspace,
                   partition_size=partition_size, v1_max_seq_len=v1_max_seq_len, **kw)
     torch.cuda.synchronize()
+    assert _guards_intact(out_whole, n_out, GUARD_F), "write outside out"
+    if ws_whole is not None:
+        assert _guards_intact(ws_whole, workspace.numel(), GUARD_B), "write outside the workspace"
     if check_status and workspace is not None and path in ("v2", "decode"):
         st = pa.read_device_status(workspace, clear=False)
         assert st == pa.PA_OK, f"device status {st}: {pa.status_string(st)}"
