@@ -87,6 +87,18 @@ typedef enum pa_dtype { PA_F32 = 0, PA_BF16 = 1, PA_F16 = 2 } pa_dtype_t;
                               workspace status word reads
                               PA_ERR_DEVICE_TIMEOUT.  Ignored by the
                               CUDA-core kernels, which have no such waits. */
+#define PA_FLAG_SPLIT_X 4 /* the caches are in the layout commit 4eb83a7e
+                              "qwen3_6_scripts", paragraph "Hardware testing
+                              confirmed", gives for its V1 kernel:
+                                k_cache [num_blocks, num_kv_heads,
+                                         head_dim / x, block_size, x]
+                                v_cache [num_blocks, num_kv_heads,
+                                         head_dim, block_size]
+                              with x = 16 / element bytes (8 for bf16 / f16,
+                              4 for f32).  Read directly, with no conversion
+                              copy, by the CUDA-core kernels (the tensor-core
+                              kernels need the [.., block_size, head_dim]
+                              layout); every call accepts it. */
 
 typedef struct pa_params {
   int32_t num_seqs;           /* B >= 0                                      */

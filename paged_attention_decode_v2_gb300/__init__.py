@@ -33,6 +33,7 @@ PA_ERR_BAD_SEQ_LEN = 8
 PA_F32, PA_BF16, PA_F16 = 0, 1, 2
 PA_FLAG_PORTABLE = 1
 PA_FLAG_SELFTEST_STALL = 2
+PA_FLAG_SPLIT_X = 4
 DEFAULT_V1_MAX_SEQ_LEN = 8192
 
 # Every symbol include/pa.h declares.
@@ -131,20 +132,35 @@ def _dtype_code(dtype) -> int:
     return codes[dtype]
 
 
+def cache_dims(k_cache, split_x: bool = False):
+    """(num_blocks, num_kv_heads, block_size, head_dim) of a key cache in the
+    standard [blocks, kv_heads, block_size, head_dim] layout, or (split_x) in
+    the split-x layout [blocks, kv_heads, head_dim / x, block_size, x]."""
+    if split_x:
+        if k_cache.dim() != 5:
+            raise PaError(PA_ERR_INVALID_ARG, "split-x k_cache must be 5-D")
+        nb, hkv, dx, bs, x = k_cache.shape
+        return nb, hkv, bs, dx * x
+    if k_cache.dim() != 4:
+        raise PaError(PA_ERR_INVALID_ARG, "k_cache must be 4-D")
+    return tuple(k_cache.shape)
+
+
 def make_params(q, k_cache, block_tables, *, max_seq_len: int, scale: float,
                 partition_size: int = 512, out_dtype=None,
                 v1_max_seq_len: int = DEFAULT_V1_MAX_SEQ_LEN, portable: bool = False,
-                flags: int = 0) -> Params:
+                flags: int = 0, split_x: bool = False) -> Params:
     """Fill a :class:`Params` from tensor shapes (no device access)."""
     num_seqs, num_heads, head_dim = q.shape
-    num_blocks, num_kv_heads, block_size, d2 = k_cache.shape
+    num_blocks, num_kv_heads, block_size, d2 = cache_dims(k_cache, split_x)
     if d2 != head_dim:
         raise PaError(PA_ERR_INVALID_ARG, "q and k_cache head_dim differ")
     return Params(num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
                   block_tables.shape[1], int(max_seq_len), int(partition_size),
                   int(v1_max_seq_len), _dtype_code(k_cache.dtype),
                   _dtype_code(out_dtype if out_dtype is not None else q.dtype), float(scale),
-                  (PA_FLAG_PORTABLE if portable else 0) | int(flags))
+                  (PA_FLAG_PORTABLE if portable else 0) | (PA_FLAG_SPLIT_X if split_x else 0) |
+                  int(flags))
 
 
 def workspace_size(params: Params) -> int:
@@ -170,7 +186,7 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
 
 
-def _check_inputs(q, k_cache, v_cache, block_tables, seq_lens, out):
+def _check_inputs(q, k_cache, v_cache, block_tables, seq_lens, out, split_x=False):
     import torch
     for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache),
                     ("block_tables", block_tables), ("seq_lens", seq_lens), ("out", out)):
@@ -180,25 +196,29 @@ def _check_inputs(q, k_cache, v_cache, block_tables, seq_lens, out):
             raise PaError(PA_ERR_INVALID_ARG, f"{name} must be contiguous")
     if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
         raise PaError(PA_ERR_INVALID_ARG, "block_tables and seq_lens must be int32")
-    if v_cache.shape != k_cache.shape or v_cache.dtype != k_cache.dtype or q.dtype != k_cache.dtype:
+    nb, hkv, bs, d = cache_dims(k_cache, split_x)
+    v_shape = (nb, hkv, d, bs) if split_x else (nb, hkv, bs, d)
+    if tuple(v_cache.shape) != v_shape or v_cache.dtype != k_cache.dtype or q.dtype != k_cache.dtype:
         raise PaError(PA_ERR_INVALID_ARG, "q, k_cache and v_cache must agree in dtype/shape")
     if tuple(out.shape) != tuple(q.shape):
         raise PaError(PA_ERR_INVALID_ARG, "out must have q's shape")
 
 
 def _params_for(q, k_cache, block_tables, out, max_seq_len, scale, partition_size,
-                v1_max_seq_len, portable, flags=0):
+                v1_max_seq_len, portable, flags=0, split_x=False):
     return make_params(q, k_cache, block_tables, max_seq_len=max_seq_len, scale=scale,
                        partition_size=partition_size, out_dtype=out.dtype,
-                       v1_max_seq_len=v1_max_seq_len, portable=portable, flags=flags)
+                       v1_max_seq_len=v1_max_seq_len, portable=portable, flags=flags,
+                       split_x=split_x)
 
 
 def decode_v1(q, k_cache, v_cache, block_tables, seq_lens, out, *, max_seq_len: int,
-              scale: float, portable: bool = False, stream=None):
-    """``pa_decode_v1``: single pass per (sequence, KV head), into ``out``."""
-    _check_inputs(q, k_cache, v_cache, block_tables, seq_lens, out)
+              scale: float, portable: bool = False, split_x: bool = False, stream=None):
+    """``pa_decode_v1``: single pass per (sequence, KV head), into ``out``.
+    ``split_x``: the caches are in the split-x layout (``PA_FLAG_SPLIT_X``)."""
+    _check_inputs(q, k_cache, v_cache, block_tables, seq_lens, out, split_x)
     p = _params_for(q, k_cache, block_tables, out, max_seq_len, scale, 512,
-                    DEFAULT_V1_MAX_SEQ_LEN, portable)
+                    DEFAULT_V1_MAX_SEQ_LEN, portable, split_x=split_x)
     st = lib().pa_decode_v1(ctypes.byref(p), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                             _ptr(block_tables), _ptr(seq_lens), _ptr(out), _stream(stream))
     if st != PA_OK:
@@ -208,15 +228,15 @@ def decode_v1(q, k_cache, v_cache, block_tables, seq_lens, out, *, max_seq_len: 
 
 def decode_v2(q, k_cache, v_cache, block_tables, seq_lens, out, workspace, *, max_seq_len: int,
               scale: float, partition_size: int = 512, portable: bool = False, stream=None,
-              flags: int = 0):
+              flags: int = 0, split_x: bool = False):
     """``pa_decode_v2``: split-KV pass 1 + log-sum-exp reduce, into ``out``.
 
     ``workspace`` is a CUDA uint8 tensor of at least :func:`workspace_size`
     bytes, allocated once and reused.
     """
-    _check_inputs(q, k_cache, v_cache, block_tables, seq_lens, out)
+    _check_inputs(q, k_cache, v_cache, block_tables, seq_lens, out, split_x)
     p = _params_for(q, k_cache, block_tables, out, max_seq_len, scale, partition_size,
-                    DEFAULT_V1_MAX_SEQ_LEN, portable, flags)
+                    DEFAULT_V1_MAX_SEQ_LEN, portable, flags, split_x)
     st = lib().pa_decode_v2(ctypes.byref(p), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                             _ptr(block_tables), _ptr(seq_lens), _ptr(workspace),
                             workspace.numel() * workspace.element_size(), _ptr(out),
@@ -252,11 +272,12 @@ def decode_v2_reduce(params: Params, seq_lens, workspace, out, stream=None):
 
 def decode(q, k_cache, v_cache, block_tables, seq_lens, out, workspace=None, *,
            max_seq_len: int, scale: float, partition_size: int = 512,
-           v1_max_seq_len: int = DEFAULT_V1_MAX_SEQ_LEN, portable: bool = False, stream=None):
+           v1_max_seq_len: int = DEFAULT_V1_MAX_SEQ_LEN, portable: bool = False,
+           split_x: bool = False, stream=None):
     """``pa_decode``: V2 when ``max_seq_len > v1_max_seq_len``, else V1."""
-    _check_inputs(q, k_cache, v_cache, block_tables, seq_lens, out)
+    _check_inputs(q, k_cache, v_cache, block_tables, seq_lens, out, split_x)
     p = _params_for(q, k_cache, block_tables, out, max_seq_len, scale, partition_size,
-                    v1_max_seq_len, portable)
+                    v1_max_seq_len, portable, split_x=split_x)
     nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     st = lib().pa_decode(ctypes.byref(p), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                          _ptr(block_tables), _ptr(seq_lens), _ptr(workspace), nbytes, _ptr(out),

@@ -33,7 +33,8 @@ pa_status_t check_params(const pa_params_t* p, bool v2) {
   if (static_cast<int64_t>(p->max_seq_len) >
       static_cast<int64_t>(p->max_blocks_per_seq) * p->block_size)
     return PA_ERR_INVALID_ARG;
-  if (p->flags & ~(PA_FLAG_PORTABLE | PA_FLAG_SELFTEST_STALL)) return PA_ERR_INVALID_ARG;
+  if (p->flags & ~(PA_FLAG_PORTABLE | PA_FLAG_SELFTEST_STALL | PA_FLAG_SPLIT_X))
+    return PA_ERR_INVALID_ARG;
   if (p->kv_dtype != PA_F32 && p->kv_dtype != PA_BF16 && p->kv_dtype != PA_F16)
     return PA_ERR_UNSUPPORTED;
   if (p->out_dtype != PA_F32 && p->out_dtype != p->kv_dtype) return PA_ERR_UNSUPPORTED;
@@ -90,6 +91,7 @@ KernelArgs make_args(const pa_params_t* p, const void* q, const void* k, const v
   a.out_dtype = p->out_dtype;
   a.scale_log2 = p->scale * kLog2eHost;
   a.selftest_stall = (p->flags & PA_FLAG_SELFTEST_STALL) ? 1 : 0;
+  a.split_x = (p->flags & PA_FLAG_SPLIT_X) ? 1 : 0;
   return a;
 }
 

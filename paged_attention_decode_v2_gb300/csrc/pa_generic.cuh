@@ -21,6 +21,10 @@
 //
 // These kernels are the portable path: they run for every dtype, head_dim
 // and block size the ABI accepts, and they are the only path for float32.
+// They also read the caches in the layout the same page gives for its V1
+// kernel ("Hardware testing confirmed": keys [blocks, kv_heads, head_dim / x,
+// block_size, x], values [blocks, kv_heads, head_dim, block_size]) when the
+// call asks for it, x being the elements of one 16-byte group.
 #pragma once
 
 #include "pa_device.cuh"
@@ -36,6 +40,8 @@ struct GenericCfg {
   static constexpr int EPL = D / 32;          // QK: head_dim elements per lane
   static constexpr int U = 32 / HP;           // QK: tokens per warp step
   static constexpr int VEC = 16 / sizeof(T);  // PV: elements per 16-byte load
+  static constexpr int X = 16 / sizeof(T);    // split-x layout: elements per key group
+  static constexpr int KG = EPL < X ? EPL : X;  // QK: elements per contiguous key load
   static constexpr int WSLICE = D / NW;       // PV: head_dim slice per warp
   static constexpr int LPT = WSLICE / VEC;    // PV: lanes per token row
   static constexpr int TPS = 32 / LPT;        // PV: tokens per warp step
@@ -151,9 +157,23 @@ __global__ void __launch_bounds__(256) pa_generic_kernel(const KernelArgs a) {
           const int t = c0 + tt;
           const int32_t id = tt < n ? sm.blk[t / BS - blk0] : -1;
           if (id >= 0) {
-            const T* row = kc + (static_cast<int64_t>(id) * a.num_kv_heads + kvh) * head_stride +
-                           static_cast<int64_t>(t % BS) * D + lane * C::EPL;
-            load_row<T, C::EPL>(row, kf[u]);
+            const T* slice = kc + (static_cast<int64_t>(id) * a.num_kv_heads + kvh) * head_stride;
+            if (!a.split_x) {
+              load_row<T, C::EPL>(slice + static_cast<int64_t>(t % BS) * D + lane * C::EPL, kf[u]);
+            } else {
+              // element (slot s, d) at ((d / X) * BS + s) * X + d % X: this
+              // lane's EPL elements are whole or part of 16-byte groups
+#pragma unroll
+              for (int g = 0; g < C::EPL / C::KG; ++g) {
+                const int d = lane * C::EPL + g * C::KG;
+                float f[C::KG];
+                load_row<T, C::KG>(slice + (static_cast<int64_t>(d / C::X) * BS + t % BS) * C::X +
+                                       d % C::X,
+                                   f);
+#pragma unroll
+                for (int e = 0; e < C::KG; ++e) kf[u][g * C::KG + e] = f[e];
+              }
+            }
           } else {
 #pragma unroll
             for (int e = 0; e < C::EPL; ++e) kf[u][e] = 0.f;
@@ -220,9 +240,14 @@ __global__ void __launch_bounds__(256) pa_generic_kernel(const KernelArgs a) {
           const int32_t id = sm.blk[t / BS - blk0];
           if (id < 0) continue;  // masked: never read its value row
           float vf[C::VEC];
-          load_row<T, C::VEC>(vc + (static_cast<int64_t>(id) * a.num_kv_heads + kvh) * head_stride +
-                                  static_cast<int64_t>(t % BS) * D + d0,
-                              vf);
+          const T* vslice = vc + (static_cast<int64_t>(id) * a.num_kv_heads + kvh) * head_stride;
+          if (!a.split_x) {
+            load_row<T, C::VEC>(vslice + static_cast<int64_t>(t % BS) * D + d0, vf);
+          } else {  // values [head_dim][block_size]: element (s, d) at d * BS + s
+#pragma unroll
+            for (int e = 0; e < C::VEC; ++e)
+              vf[e] = to_float(vslice[static_cast<int64_t>(d0 + e) * BS + t % BS]);
+          }
           const float4 pa4 = *reinterpret_cast<const float4*>(&sm.p[tt][0]);
           const float4 pb4 = *reinterpret_cast<const float4*>(&sm.p[tt][4]);
           const float pp[8] = {pa4.x, pa4.y, pa4.z, pa4.w, pb4.x, pb4.y, pb4.z, pb4.w};

@@ -36,6 +36,7 @@ struct KernelArgs {
   int32_t out_dtype;       // pa_dtype_t
   float scale_log2;        // scale * log2(e): logits are kept in base-2 units
   int32_t selftest_stall;  // PA_FLAG_SELFTEST_STALL was given
+  int32_t split_x;         // PA_FLAG_SPLIT_X: the pages' V1 cache layout
 };
 
 // Launchers return cudaSuccess or the launch error.

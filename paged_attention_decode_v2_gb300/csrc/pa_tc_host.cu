@@ -63,7 +63,7 @@ const DeviceInfo& device_info() {
 }  // namespace
 
 bool tc_applicable(const pa_params_t* p) {
-  if (p->flags & PA_FLAG_PORTABLE) return false;
+  if (p->flags & (PA_FLAG_PORTABLE | PA_FLAG_SPLIT_X)) return false;
   if (p->kv_dtype != PA_BF16 && p->kv_dtype != PA_F16) return false;
   if (p->num_heads / p->num_kv_heads > 8) return false;
   const int D = p->head_dim, BS = p->block_size;

@@ -130,7 +130,12 @@ def test_host_checks_reject_bad_arguments(L):
     assert _call_v2(L, params(max_seq_len=100001, max_blocks_per_seq=6250)) == pa.PA_ERR_INVALID_ARG
     assert _call_v2(L, params(num_blocks=0)) == pa.PA_ERR_INVALID_ARG
     assert _call_v2(L, params(flags=8)) == pa.PA_ERR_INVALID_ARG
-    assert _call_v2(L, params(flags=4)) == pa.PA_ERR_INVALID_ARG
+    assert _call_v2(L, params(flags=16)) == pa.PA_ERR_INVALID_ARG
+    # the split-x cache layout is a valid flag: the call gets past the
+    # parameter checks and fails only on the undersized workspace
+    assert _call_v2(L, params(flags=pa.PA_FLAG_SPLIT_X), ws_bytes=1000) == \
+        pa.PA_ERR_WORKSPACE_TOO_SMALL
+    assert pa.decode_kernel(params(flags=pa.PA_FLAG_SPLIT_X)) == 1   # CUDA-core kernels only
     assert L.pa_decode_v2(None, None, None, None, None, None, None, 0, None, None) == \
         pa.PA_ERR_INVALID_ARG
     V = ctypes.c_void_p

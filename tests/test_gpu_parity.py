@@ -335,3 +335,48 @@ def test_cuda_graph_capture_and_replay():
                          f"graph replay path {pa.decode_path(params)} cut {cut}")
         if ws is not None:
             assert pa.read_device_status(ws) == pa.PA_OK
+
+
+def _split_x(bc):
+    """The caches of `bc` rewritten (on the host, as test input) into the
+    split-x layout: keys [blocks, kv_heads, head_dim / x, block_size, x],
+    values [blocks, kv_heads, head_dim, block_size], x = 16 / element bytes."""
+    nb, hkv, bs, d = bc.k_cache.shape
+    x = 16 // bc.k_cache.element_size()
+    k5 = bc.k_cache.view(nb, hkv, bs, d // x, x).permute(0, 1, 3, 2, 4).contiguous()
+    v4 = bc.v_cache.permute(0, 1, 3, 2).contiguous()
+    return k5, v4
+
+
+@pytest.mark.parametrize("dtype,D,BS", [(torch.bfloat16, 256, 16), (torch.float16, 128, 32),
+                                        (torch.float32, 64, 16), (torch.float32, 256, 32),
+                                        (torch.bfloat16, 64, 8)])
+def test_split_x_layout(dtype, D, BS):
+    """PA_FLAG_SPLIT_X: the caches in the pages' V1 layout, read directly: the
+    same bits as the standard layout on the same (CUDA-core) kernels, and the
+    oracle's result within the tolerance, on V1, V2 and pa_decode."""
+    lens = (1, BS - 1, 300, 777, 0, 1500)
+    bc = problem(dtype=dtype, lens=lens, Hq=12, Hkv=3, D=D, BS=BS, seed=21)
+    ref = _ref(bc)
+    bg = bc.to("cuda")
+    k5, v4 = (t.cuda() for t in _split_x(bc))
+    kw = dict(max_seq_len=bc.max_seq_len, scale=bc.scale)
+    for path in ("v1", "v2", "decode"):
+        want = run(bg, path=path, partition_size=256, portable=True, v1_max_seq_len=1024)
+        got = torch.full(tuple(bc.q.shape), float("nan"), device="cuda")
+        params = pa.make_params(bc.q, k5, bc.block_tables, partition_size=256,
+                                out_dtype=torch.float32, split_x=True, **kw)
+        ws = pa.alloc_workspace(params)
+        if path == "v1":
+            pa.decode_v1(bg.q, k5, v4, bg.block_tables, bg.seq_lens, got, split_x=True, **kw)
+        elif path == "v2":
+            pa.decode_v2(bg.q, k5, v4, bg.block_tables, bg.seq_lens, got, ws, partition_size=256,
+                         split_x=True, **kw)
+        else:
+            pa.decode(bg.q, k5, v4, bg.block_tables, bg.seq_lens, got, ws, partition_size=256,
+                      v1_max_seq_len=1024, split_x=True, **kw)
+        torch.cuda.synchronize()
+        g = got.double().cpu().numpy()
+        assert np.array_equal(g, want), f"split-x {path} differs from the standard layout"
+        assert_close(g, ref, TOL[dtype], f"split-x {path}")
+        assert pa.read_device_status(ws) == pa.PA_OK
