@@ -490,7 +490,11 @@ __global__ void __launch_bounds__(tc::kThreads, CPS)
     }
   } else if (warp == 5) {
     // ========================= MMA issuer =========================================
-    if (lane == 0) {
+    // The whole warp runs the loop (waits, descriptors) in convergent code and
+    // one elected lane issues each MMA and commit; every branch below depends
+    // on warp-uniform values only (a wait's result is agreed with __all_sync).
+    {
+      constexpr unsigned kAll = 0xffffffffu;
       constexpr uint32_t id_qk = sm100::idesc_f16(kBf16, false, false, 128, 16);
       constexpr uint32_t id_pv = sm100::idesc_f16(kBf16, true, false, 128, 16);
       const uint32_t q_base = sm100::smem_u32(qs);
@@ -500,12 +504,12 @@ __global__ void __launch_bounds__(tc::kThreads, CPS)
       bool ok = true;
       // diagnostic: wait for an event that never happens, so the bounded
       // wait runs out and the abort path is exercised
-      if (a.selftest_stall) ok = sm100::mbar_wait(&c.never, 0, budget, abort_flag);
+      if (a.selftest_stall) ok = __all_sync(kAll, sm100::mbar_wait(&c.never, 0, budget, abort_flag));
       for (int64_t k = cid; k < total_items && ok; k += stride) {
         const Item it = item_at(a, prefix, k, kV2, rank, cs);
         if (it.t0 >= it.t1) continue;
         const int qb = qn & 1;
-        ok = sm100::mbar_wait(&c.qfull[qb], (qn >> 1) & 1, budget, abort_flag);
+        ok = __all_sync(kAll, sm100::mbar_wait(&c.qfull[qb], (qn >> 1) & 1, budget, abort_flag));
         if (!ok) break;
         ++qn;
         const uint32_t qbuf = q_base + qb * Lay::kSlices * 1024;
@@ -517,7 +521,7 @@ __global__ void __launch_bounds__(tc::kThreads, CPS)
           for (int tt = 0; tt < nt && ok; ++tt) {
             for (int sl = 0; sl < Lay::kSlices; ++sl) {
               const int slot = g % NST;
-              ok = sm100::mbar_wait(&c.full[slot], (g / NST) & 1, budget, abort_flag);
+              ok = __all_sync(kAll, sm100::mbar_wait(&c.full[slot], (g / NST) & 1, budget, abort_flag));
               if (!ok) break;
               sm100::tc_fence_after();
               const uint32_t st = ring_base + slot * kStageBytes;
@@ -526,23 +530,23 @@ __global__ void __launch_bounds__(tc::kThreads, CPS)
                 const uint64_t ad = sm100::smem_desc(st + kk * 32, 16, 1024, sm100::kSw128);
                 const uint64_t bd =
                     sm100::smem_desc(qbuf + sl * 1024 + kk * 32, 16, 1024, sm100::kSw128);
-                sm100::mma_f16(tmem + tt * 16, ad, bd, id_qk, (sl | kk) != 0);
+                sm100::mma_f16_elect(tmem + tt * 16, ad, bd, id_qk, (sl | kk) != 0);
               }
-              sm100::mma_commit(&c.empty[slot]);
+              sm100::mma_commit_elect(&c.empty[slot]);
               ++g;
             }
           }
           if (!ok) break;
-          if (ci == nchunks - 1) sm100::mma_commit(&c.qempty[qb]);
-          sm100::mma_commit(&c.s_full);
-          ok = sm100::mbar_wait(&c.p_ready, cc & 1, budget, abort_flag);
+          if (ci == nchunks - 1) sm100::mma_commit_elect(&c.qempty[qb]);
+          sm100::mma_commit_elect(&c.s_full);
+          ok = __all_sync(kAll, sm100::mbar_wait(&c.p_ready, cc & 1, budget, abort_flag));
           if (!ok) break;
           sm100::tc_fence_after();
           const int nv = (n + Lay::kVTokens - 1) / Lay::kVTokens;
           bool first = true;
           for (int v = 0; v < nv; ++v) {
             const int slot = g % NST;
-            ok = sm100::mbar_wait(&c.full[slot], (g / NST) & 1, budget, abort_flag);
+            ok = __all_sync(kAll, sm100::mbar_wait(&c.full[slot], (g / NST) & 1, budget, abort_flag));
             if (!ok) break;
             sm100::tc_fence_after();
             const uint32_t st = ring_base + slot * kStageBytes;
@@ -556,21 +560,21 @@ __global__ void __launch_bounds__(tc::kThreads, CPS)
                 const uint64_t ad =
                     sm100::smem_desc(st + jb * BS * D * 2 + 2 * j * BS * 128 + s0 * 128, BS * 128,
                                      1024, sm100::kSw128);
-                sm100::mma_f16(tmem + kOCol + 16 * j, ad, bd, id_pv, !first);
+                sm100::mma_f16_elect(tmem + kOCol + 16 * j, ad, bd, id_pv, !first);
               }
               first = false;
             }
-            sm100::mma_commit(&c.empty[slot]);
+            sm100::mma_commit_elect(&c.empty[slot]);
             ++g;
           }
           if (!ok) break;
-          sm100::mma_commit(&c.o_full);
+          sm100::mma_commit_elect(&c.o_full);
         }
       }
       if (!ok) {
-        fail(c, a.status);
+        if (lane == 0) fail(c, a.status);
         // no MMA may still be running when tensor memory is released
-        sm100::mma_commit(&c.drain);
+        sm100::mma_commit_elect(&c.drain);
         sm100::mbar_wait(&c.drain, 0, budget, nullptr);
       }
     }
