@@ -1,4 +1,5 @@
-"""Float64 CPU oracle for paged single-token decode attention.
+"""Float64 CPU oracle for paged single-token decode attention and paged
+prefix prefill.
 
 TEST INFRASTRUCTURE ONLY: the test suite, ``__graft_entry__.smoke()`` and the
 CPU-baseline leg of ``bench.py`` are the only callers.  The product library
@@ -17,7 +18,14 @@ Sources (commit pages of the project "project_6"):
     (decode <= 8192)": V1 is checked against plain ("manual") attention,
     which is :func:`decode`;
   * commit 4eb83a7e "qwen3_6_scripts", paragraph "Hardware testing
-    confirmed": the [blocks, kv_heads, block_size, head_dim] cache layout.
+    confirmed": the [blocks, kv_heads, block_size, head_dim] cache layout;
+  * commit 1a4e1005 "paged_attn.py", opening paragraph, and commit 4eb83a7e
+    "qwen3_6_scripts", paragraphs on the prefix attention's pre-allocated
+    buffers, "Complete rewrite of qwen3_6_scripts/paged_attn.py" (item 1)
+    and "Prefill (flash_attn_func)": prefill as online softmax over key
+    tiles, a context phase from the paged cache then a causal phase over the
+    chunk's own tokens -- :func:`prefill` is the plain definition,
+    :func:`prefill_tiled` the tiled algorithm.
 """
 from __future__ import annotations
 
@@ -96,6 +104,34 @@ def _prep(q, k_cache, v_cache, block_tables, seq_lens, scale):
     return shape, keep
 
 
+def _prep_prefill(q, k_new, v_new, k_cache, v_cache, block_tables, query_start, ctx_lens,
+                  scale):
+    for name, t in (("q", q), ("k_new", k_new), ("v_new", v_new), ("k_cache", k_cache),
+                    ("v_cache", v_cache)):
+        if t.device.type != "cpu":
+            raise ValueError(f"oracle: {name} must be a CPU tensor")
+        if t.dtype != q.dtype:
+            raise ValueError("oracle: q, k_new, v_new and the caches must share one dtype")
+    if q.dtype not in _DTYPE_CODE:
+        raise ValueError("oracle: dtype must be f32, bf16 or f16")
+    if k_cache.dim() != 4 or v_cache.shape != k_cache.shape or q.dim() != 3:
+        raise ValueError("oracle: q [T,Hq,D], caches [blocks, kv_heads, block_size, D]")
+    nb, hkv, bs, d = k_cache.shape
+    T, hq, dq = q.shape
+    if dq != d or k_new.shape != (T, hkv, d) or v_new.shape != (T, hkv, d):
+        raise ValueError("oracle: k_new / v_new must be [T, Hkv, D]")
+    bt = block_tables.cpu().to(torch.int32).contiguous()
+    qs = query_start.cpu().to(torch.int32).contiguous()
+    cl = ctx_lens.cpu().to(torch.int32).contiguous()
+    B = cl.shape[0]
+    if bt.dim() != 2 or bt.shape[0] != B or qs.shape != (B + 1,):
+        raise ValueError("oracle: block_tables [B, max_blocks], query_start [B+1], ctx_lens [B]")
+    shape = _Shape(_DTYPE_CODE[q.dtype], B, hq, hkv, d, bs, nb, bt.shape[1], float(scale))
+    keep = [q.contiguous(), k_new.contiguous(), v_new.contiguous(), k_cache.contiguous(),
+            v_cache.contiguous(), bt, qs, cl]
+    return shape, T, keep
+
+
 def _check(rc: int) -> None:
     if rc == -2:
         raise ValueError("oracle: block table entry outside the pool")
@@ -116,6 +152,12 @@ class Oracle:
             ctypes.POINTER(_Shape), P, P, P, P, P, ctypes.c_int32, ctypes.c_int32,
             P, P, P, P]
         lib.pa_oracle_decode_partitioned.restype = ctypes.c_int
+        lib.pa_oracle_prefill.argtypes = [ctypes.POINTER(_Shape), ctypes.c_int64, P, P, P, P,
+                                          P, P, P, P, P, ctypes.c_int64, P]
+        lib.pa_oracle_prefill.restype = ctypes.c_int
+        lib.pa_oracle_prefill_tiled.argtypes = [ctypes.POINTER(_Shape), ctypes.c_int64, P, P,
+                                                P, P, P, P, P, P, ctypes.c_int32, P]
+        lib.pa_oracle_prefill_tiled.restype = ctypes.c_int
         lib.pa_oracle_max_threads.restype = ctypes.c_int
         lib.pa_oracle_set_threads.argtypes = [ctypes.c_int]
         self.lib = lib
@@ -178,6 +220,51 @@ class Oracle:
         return out, ml, es, to
 
 
+    def prefill(self, q, k_new, v_new, k_cache, v_cache, block_tables, query_start, ctx_lens,
+                scale, rows=None):
+        """Paged prefix prefill by the plain definition: query row (t, h) of
+        sequence b (query_start[b] <= t < query_start[b+1], i = t -
+        query_start[b]) attends to the sequence's ctx_lens[b] cached tokens
+        and to its new tokens 0..i (k_new / v_new rows query_start[b]..t).
+
+        Returns float64 ``[T, Hq, D]``; with ``rows`` (flat ``t*Hq + h``
+        indices) returns ``[len(rows), D]``.
+        """
+        shape, T, keep = _prep_prefill(q, k_new, v_new, k_cache, v_cache, block_tables,
+                                       query_start, ctx_lens, scale)
+        qc, kn, vn, kc, vc, bt, qs, cl = keep
+        d = shape.head_dim
+        if rows is None:
+            out = np.empty((T, shape.num_heads, d), dtype=np.float64)
+            rows_arr, nrows, rows_ptr = None, 0, None
+        else:
+            rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+            nrows = rows_arr.size
+            rows_ptr = rows_arr.ctypes.data
+            out = np.empty((nrows, d), dtype=np.float64)
+        rc = self.lib.pa_oracle_prefill(ctypes.byref(shape), T, qc.data_ptr(), kn.data_ptr(),
+                                        vn.data_ptr(), kc.data_ptr(), vc.data_ptr(),
+                                        bt.data_ptr(), qs.data_ptr(), cl.data_ptr(), rows_ptr,
+                                        nrows, out.ctypes.data)
+        _check(rc)
+        return out
+
+    def prefill_tiled(self, q, k_new, v_new, k_cache, v_cache, block_tables, query_start,
+                      ctx_lens, scale, tile):
+        """The pages' tiled online-softmax prefill (context tiles, then chunk
+        tiles), in double; ``[T, Hq, D]``."""
+        shape, T, keep = _prep_prefill(q, k_new, v_new, k_cache, v_cache, block_tables,
+                                       query_start, ctx_lens, scale)
+        qc, kn, vn, kc, vc, bt, qs, cl = keep
+        out = np.empty((T, shape.num_heads, shape.head_dim), dtype=np.float64)
+        rc = self.lib.pa_oracle_prefill_tiled(ctypes.byref(shape), T, qc.data_ptr(),
+                                              kn.data_ptr(), vn.data_ptr(), kc.data_ptr(),
+                                              vc.data_ptr(), bt.data_ptr(), qs.data_ptr(),
+                                              cl.data_ptr(), int(tile), out.ctypes.data)
+        _check(rc)
+        return out
+
+
 _default = None
 
 
@@ -209,3 +296,17 @@ def decode_partitioned(q, k_cache, v_cache, block_tables, seq_lens, scale, parti
     """See :meth:`Oracle.decode_partitioned`."""
     return default().decode_partitioned(q, k_cache, v_cache, block_tables, seq_lens, scale,
                                         partition_size, max_partitions)
+
+
+def prefill(q, k_new, v_new, k_cache, v_cache, block_tables, query_start, ctx_lens, scale,
+            rows=None) -> np.ndarray:
+    """See :meth:`Oracle.prefill`."""
+    return default().prefill(q, k_new, v_new, k_cache, v_cache, block_tables, query_start,
+                             ctx_lens, scale, rows)
+
+
+def prefill_tiled(q, k_new, v_new, k_cache, v_cache, block_tables, query_start, ctx_lens,
+                  scale, tile) -> np.ndarray:
+    """See :meth:`Oracle.prefill_tiled`."""
+    return default().prefill_tiled(q, k_new, v_new, k_cache, v_cache, block_tables,
+                                   query_start, ctx_lens, scale, tile)

@@ -1,6 +1,8 @@
 /*
  * pa_oracle.c -- plain, slow, float64 CPU oracle for single-token decode
- * attention over a paged KV cache.
+ * attention over a paged KV cache, and for paged prefix prefill (a chunk of
+ * new tokens attending to a cached context and causally to itself; its own
+ * sources are listed above pa_oracle_prefill).
  *
  * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
  * benchmark's CPU-baseline leg may call this code.  It shares nothing with
@@ -295,6 +297,235 @@ int pa_oracle_decode_partitioned(const orc_shape* s, const void* q, const void* 
       }
     }
     free(m); free(sp); free(op); free(l);
+  }
+  return err;
+}
+
+/* ======================================================================
+ * Paged prefix prefill (a chunk of new tokens after a cached context).
+ *
+ * Sources (same project):
+ *   [PREFIX]  commit 1a4e1005 "paged_attn.py", opening paragraph: prefill
+ *             is Flash-Attention-style online softmax over key tiles;
+ *   [PHASES]  commit 4eb83a7e "qwen3_6_scripts", paragraph on the
+ *             pre-allocated buffers of the prefix attention: a tile loop
+ *             over the cached context, then one over the current chunk's
+ *             tokens, each tile updating a block max (m_blk), the running
+ *             max (m_new) and a correction factor (corr);
+ *   [GATHER]  same page, paragraph "Complete rewrite of
+ *             qwen3_6_scripts/paged_attn.py", item 1: the context keys and
+ *             values come from the paged cache through the block table;
+ *   [CAUSAL]  same page, paragraph "Prefill (flash_attn_func)": the chunk
+ *             attends causally (causal=True).
+ *
+ * Layout (readings where the pages are silent, listed in the design notes):
+ * sequence b owns rows query_start[b] .. query_start[b+1]-1 of q [T, Hq, D],
+ * k_new and v_new [T, Hkv, D] (its n_b new tokens, in order), and its first
+ * ctx_lens[b] = C_b tokens sit in the paged cache.  New token i (0-based in
+ * the chunk) attends to the C_b context tokens and to new tokens 0..i.
+ * ====================================================================== */
+
+/* Sequence that owns token row t (query_start is non-decreasing). */
+static int orc_seq_of_row(const int32_t* query_start, int num_seqs, int64_t t) {
+  int lo = 0, hi = num_seqs; /* largest b with query_start[b] <= t */
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) / 2;
+    if (query_start[mid] <= t) lo = mid;
+    else hi = mid;
+  }
+  return lo;
+}
+
+static int orc_prefill_check(const orc_shape* s, int64_t T, const int32_t* query_start,
+                             const int32_t* ctx_lens) {
+  int rc = orc_check(s);
+  if (rc) return rc;
+  if (T < 0 || query_start[0] != 0 || query_start[s->num_seqs] != T) return ORC_BAD_ARG;
+  for (int b = 0; b < s->num_seqs; ++b) {
+    if (query_start[b + 1] < query_start[b]) return ORC_BAD_ARG;
+    if (ctx_lens[b] < 0 || ctx_lens[b] > (int64_t)s->max_blocks_per_seq * s->block_size)
+      return ORC_BAD_ARG;
+  }
+  return ORC_OK;
+}
+
+/* Visible key j of new token i of sequence b: context token j < C from the
+ * paged cache [GATHER], else new token j - C from k_new / v_new (row
+ * query_start[b] + j - C).  Sets *base to the element offset of the key's
+ * row in the array it returns through *which (0: cache, 1: new); returns
+ * ORC_BAD_BLOCK for a table entry outside the pool. */
+static int orc_prefill_key(const orc_shape* s, const int32_t* block_tables, int b, int kvh,
+                           int32_t C, int32_t qs, int64_t j, int* which, int64_t* base) {
+  if (j < C) {
+    const int32_t blk = orc_block(s, block_tables, b, j);
+    if (blk < 0) return ORC_BAD_BLOCK;
+    *which = 0;
+    *base = orc_row(s, blk, kvh, (int)(j % s->block_size));
+  } else {
+    *which = 1;
+    *base = (((int64_t)qs + (j - C)) * s->num_kv_heads + kvh) * (int64_t)s->head_dim;
+  }
+  return ORC_OK;
+}
+
+/* logit of query row (t, h) against key row `base` of `keys`:
+ *   l = scale * sum_d q[t,h,d] * K[d]                                       */
+static double orc_prefill_logit(const orc_shape* s, const void* q, int64_t t, int h,
+                                const void* keys, int64_t base) {
+  const int64_t qb = (t * s->num_heads + h) * (int64_t)s->head_dim;
+  double dot = 0.0;
+  for (int d = 0; d < s->head_dim; ++d)
+    dot += orc_load(q, s->dtype, qb + d) * orc_load(keys, s->dtype, base + d);
+  return s->scale * dot;
+}
+
+/*
+ * Direct prefill oracle: for every query row (t, h), plain softmax attention
+ * over its visible keys,
+ *   M = max_j l_j,  w_j = exp(l_j - M),  out[d] = sum_j w_j V_j[d] / sum_j w_j.
+ * out is float64 [T, Hq, D] when rows == NULL; otherwise only the listed
+ * rows (index t*Hq + h) are computed, row r of the request going to
+ * out[r*D .. r*D + D).
+ */
+int pa_oracle_prefill(const orc_shape* s, int64_t T, const void* q, const void* k_new,
+                      const void* v_new, const void* k_cache, const void* v_cache,
+                      const int32_t* block_tables, const int32_t* query_start,
+                      const int32_t* ctx_lens, const int64_t* rows, int64_t nrows, double* out) {
+  int rc = orc_prefill_check(s, T, query_start, ctx_lens);
+  if (rc) return rc;
+  const int64_t all = T * s->num_heads;
+  const int64_t n = rows ? nrows : all;
+  for (int64_t r = 0; rows && r < n; ++r)
+    if (rows[r] < 0 || rows[r] >= all) return ORC_BAD_ARG;
+  const int G = s->num_heads / s->num_kv_heads;
+  const int D = s->head_dim;
+  int err = ORC_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t r = 0; r < n; ++r) {
+    const int64_t row = rows ? rows[r] : r;
+    const int64_t t = row / s->num_heads;
+    const int h = (int)(row % s->num_heads);
+    const int kvh = h / G; /* [GQA] */
+    const int b = orc_seq_of_row(query_start, s->num_seqs, t);
+    const int32_t C = ctx_lens[b], qs = query_start[b];
+    const int64_t nvis = (int64_t)C + (t - qs) + 1; /* [CAUSAL]: new tokens 0..i */
+    double* o = out + r * D;
+    for (int d = 0; d < D; ++d) o[d] = 0.0;
+    double* l = (double*)malloc(sizeof(double) * (size_t)nvis);
+    if (!l) {
+#pragma omp atomic write
+      err = ORC_NO_MEM;
+      continue;
+    }
+    int e = ORC_OK, which = 0;
+    int64_t base = 0;
+    double M = -INFINITY;
+    for (int64_t j = 0; j < nvis && !e; ++j) {
+      e = orc_prefill_key(s, block_tables, b, kvh, C, qs, j, &which, &base);
+      if (e) break;
+      l[j] = orc_prefill_logit(s, q, t, h, which ? k_new : k_cache, base);
+      if (l[j] > M) M = l[j];
+    }
+    if (!e) {
+      double den = 0.0;
+      for (int64_t j = 0; j < nvis; ++j) {
+        const double w = exp(l[j] - M);
+        orc_prefill_key(s, block_tables, b, kvh, C, qs, j, &which, &base);
+        const void* vals = which ? v_new : v_cache;
+        den += w;
+        for (int d = 0; d < D; ++d) o[d] += w * orc_load(vals, s->dtype, base + d);
+      }
+      for (int d = 0; d < D; ++d) o[d] /= den;
+    } else {
+#pragma omp atomic write
+      err = e;
+    }
+    free(l);
+  }
+  return err;
+}
+
+/*
+ * The pages' tiled prefill [PREFIX] [PHASES], in double: for every query
+ * row, the visible keys are taken in tiles of `tile` keys -- first the
+ * context [0, C) from the paged cache, then the chunk's new tokens up to
+ * the row's own -- and each tile updates the running state
+ *   m_blk = max over the tile's logits
+ *   m_new = max(m, m_blk)
+ *   corr  = exp(m - m_new)            (0 while nothing has been seen)
+ *   acc   = acc * corr + sum_j exp(l_j - m_new) V_j
+ *   l_sum = l_sum * corr + sum_j exp(l_j - m_new)
+ *   m     = m_new
+ * and out = acc / l_sum.  Reaches the direct oracle's value up to
+ * rounding; out is float64 [T, Hq, D].
+ */
+int pa_oracle_prefill_tiled(const orc_shape* s, int64_t T, const void* q, const void* k_new,
+                            const void* v_new, const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables, const int32_t* query_start,
+                            const int32_t* ctx_lens, int32_t tile, double* out) {
+  int rc = orc_prefill_check(s, T, query_start, ctx_lens);
+  if (rc) return rc;
+  if (tile <= 0) return ORC_BAD_ARG;
+  const int G = s->num_heads / s->num_kv_heads;
+  const int D = s->head_dim;
+  const int64_t all = T * s->num_heads;
+  int err = ORC_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t row = 0; row < all; ++row) {
+    const int64_t t = row / s->num_heads;
+    const int h = (int)(row % s->num_heads);
+    const int kvh = h / G;
+    const int b = orc_seq_of_row(query_start, s->num_seqs, t);
+    const int32_t C = ctx_lens[b], qs = query_start[b];
+    const int64_t i = t - qs; /* the row's place in its chunk */
+    double* acc = out + row * D;
+    for (int d = 0; d < D; ++d) acc[d] = 0.0;
+    double* l = (double*)malloc(sizeof(double) * (size_t)tile);
+    if (!l) {
+#pragma omp atomic write
+      err = ORC_NO_MEM;
+      continue;
+    }
+    double m = -INFINITY, lsum = 0.0;
+    int e = ORC_OK;
+    /* phase 0: context tiles [j0, j1) of [0, C); phase 1: chunk tiles of
+     * new tokens [j0, j1) of [0, i + 1) */
+    for (int phase = 0; phase < 2 && !e; ++phase) {
+      const int64_t end = phase == 0 ? C : i + 1;
+      for (int64_t j0 = 0; j0 < end && !e; j0 += tile) {
+        const int64_t j1 = (j0 + tile < end) ? j0 + tile : end;
+        int which = 0;
+        int64_t base = 0;
+        double m_blk = -INFINITY;
+        for (int64_t j = j0; j < j1; ++j) {
+          e = orc_prefill_key(s, block_tables, b, kvh, C, qs, phase == 0 ? j : C + j, &which,
+                              &base);
+          if (e) break;
+          l[j - j0] = orc_prefill_logit(s, q, t, h, which ? k_new : k_cache, base);
+          if (l[j - j0] > m_blk) m_blk = l[j - j0];
+        }
+        if (e) break;
+        const double m_new = m > m_blk ? m : m_blk;
+        const double corr = m == -INFINITY ? 0.0 : exp(m - m_new);
+        for (int d = 0; d < D; ++d) acc[d] *= corr;
+        lsum *= corr;
+        for (int64_t j = j0; j < j1; ++j) {
+          const double p = exp(l[j - j0] - m_new);
+          orc_prefill_key(s, block_tables, b, kvh, C, qs, phase == 0 ? j : C + j, &which, &base);
+          const void* vals = which ? v_new : v_cache;
+          lsum += p;
+          for (int d = 0; d < D; ++d) acc[d] += p * orc_load(vals, s->dtype, base + d);
+        }
+        m = m_new;
+      }
+    }
+    if (e) {
+#pragma omp atomic write
+      err = e;
+    } else {
+      for (int d = 0; d < D; ++d) acc[d] /= lsum;
+    }
+    free(l);
   }
   return err;
 }

@@ -196,3 +196,135 @@ def make(w: Workload, device="cpu", *, seed: Optional[int] = None, poison: bool 
                 k[last, :, L % BS:, :] = nan
                 v[last, :, L % BS:, :] = nan
     return Batch(w, q, k, v, table.to(dev), lens.to(dev), max_len)
+
+
+# ---------------------------------------------------------------------------
+# Paged prefix prefill: a chunk of new tokens per sequence after a cached
+# context (commit 1a4e1005 "paged_attn.py", opening paragraph; commit
+# 4eb83a7e "qwen3_6_scripts", paragraph "Complete rewrite of
+# qwen3_6_scripts/paged_attn.py", item 1).  Chunks of up to 8192 tokens
+# follow the serving configuration on the same page (max-num-batched-tokens
+# 8192 -> 16384 / 32768).
+# ---------------------------------------------------------------------------
+
+@dataclasses.dataclass(frozen=True)
+class PrefillWorkload:
+    name: str
+    dtype: torch.dtype
+    num_seqs: int
+    num_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    seed: int
+    ctx_lens: Callable[[torch.Generator], torch.Tensor]   # cached tokens per sequence
+    new_lens: Callable[[torch.Generator], torch.Tensor]   # chunk tokens per sequence
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.head_dim)
+
+
+@dataclasses.dataclass
+class PrefillBatch:
+    """One prefill step's inputs.  All tensors live on one device."""
+    workload: PrefillWorkload
+    q: torch.Tensor              # [T, Hq, D]
+    k: torch.Tensor              # [T, Hkv, D]  the chunk's keys
+    v: torch.Tensor              # [T, Hkv, D]  the chunk's values
+    k_cache: torch.Tensor        # [NB, Hkv, BS, D]  the cached context
+    v_cache: torch.Tensor
+    block_tables: torch.Tensor   # int32 [B, MB]
+    query_start: torch.Tensor    # int32 [B + 1]
+    ctx_lens: torch.Tensor       # int32 [B]
+    max_query_len: int
+    max_ctx_len: int
+
+    @property
+    def scale(self) -> float:
+        return self.workload.scale
+
+    def to(self, device) -> "PrefillBatch":
+        return dataclasses.replace(
+            self, q=self.q.to(device), k=self.k.to(device), v=self.v.to(device),
+            k_cache=self.k_cache.to(device), v_cache=self.v_cache.to(device),
+            block_tables=self.block_tables.to(device), query_start=self.query_start.to(device),
+            ctx_lens=self.ctx_lens.to(device))
+
+
+def _lens(values):
+    vals = tuple(int(x) for x in values)
+    return lambda g: torch.tensor(vals, dtype=torch.int32)
+
+
+PREFILL_WORKLOADS = {
+    # one 8192-token chunk after 24576 cached tokens, the decode shapes' heads
+    "prefill_32k": PrefillWorkload(
+        "prefill_32k", torch.bfloat16, 1, 24, 4, 256, 16, 2001, _lens([24576]), _lens([8192])),
+    # a mixed batch: four chunks of different sizes over different contexts
+    "prefill_mixed": PrefillWorkload(
+        "prefill_mixed", torch.bfloat16, 4, 24, 4, 256, 16, 2002,
+        _lens([0, 5000, 12000, 30000]), _lens([2048, 1000, 3000, 500])),
+}
+
+
+def prefill_problem(dtype=torch.bfloat16, ctx=(100,), new=(37,), Hq=6, Hkv=2, D=128, BS=16,
+                    seed=0) -> PrefillWorkload:
+    """A small prefill workload with the given per-sequence lengths."""
+    return PrefillWorkload("prefill_pin", dtype, len(ctx), Hq, Hkv, D, BS, seed, _lens(ctx),
+                           _lens(new))
+
+
+def make_prefill(w: PrefillWorkload, device="cpu", *, poison: bool = False) -> PrefillBatch:
+    """Draw one prefill batch of ``w``.
+
+    The cache holds each sequence's context in blocks taken from a seeded
+    permutation of the pool; the chunk's q, k and v are separate tensors.
+    ``poison=True`` writes NaN into every pool block no context owns and into
+    the slots past each context's last token, and -1 into block-table entries
+    past the last context block.
+    """
+    g_cpu = torch.Generator().manual_seed(w.seed)
+    ctx = w.ctx_lens(g_cpu).to(torch.int32)
+    new = w.new_lens(g_cpu).to(torch.int32)
+    B, BS = w.num_seqs, w.block_size
+    blocks_needed = [(int(c) + BS - 1) // BS for c in ctx.tolist()]
+    total = sum(blocks_needed)
+    nb = max(1, math.ceil(1.1 * total))
+    mb = max(1, max(blocks_needed) if B else 1)
+    perm = torch.randperm(nb, generator=g_cpu).to(torch.int32)
+    table = torch.full((B, mb), -1 if poison else 0, dtype=torch.int32)
+    used = torch.zeros(nb, dtype=torch.bool)
+    pos = 0
+    for b, n in enumerate(blocks_needed):
+        table[b, :n] = perm[pos:pos + n]
+        used[perm[pos:pos + n].long()] = True
+        pos += n
+    qs = torch.zeros(B + 1, dtype=torch.int32)
+    qs[1:] = torch.cumsum(new, 0).to(torch.int32)
+    T = int(qs[-1])
+
+    dev = torch.device(device)
+    g = torch.Generator(device=dev).manual_seed(w.seed + 7)
+    shape = (nb, w.num_kv_heads, BS, w.head_dim)
+    k_cache = torch.randn(shape, generator=g, device=dev, dtype=torch.float32).to(w.dtype)
+    v_cache = torch.randn(shape, generator=g, device=dev, dtype=torch.float32).to(w.dtype)
+    q = torch.randn((T, w.num_heads, w.head_dim), generator=g, device=dev,
+                    dtype=torch.float32).to(w.dtype)
+    k = torch.randn((T, w.num_kv_heads, w.head_dim), generator=g, device=dev,
+                    dtype=torch.float32).to(w.dtype)
+    v = torch.randn((T, w.num_kv_heads, w.head_dim), generator=g, device=dev,
+                    dtype=torch.float32).to(w.dtype)
+    if poison:
+        nan = torch.tensor(float("nan"), dtype=w.dtype, device=dev)
+        unused = (~used).nonzero().flatten().to(dev)
+        k_cache[unused] = nan
+        v_cache[unused] = nan
+        for b, n in enumerate(blocks_needed):
+            C = int(ctx[b])
+            if n and C % BS:
+                last = int(table[b, n - 1])
+                k_cache[last, :, C % BS:, :] = nan
+                v_cache[last, :, C % BS:, :] = nan
+    return PrefillBatch(w, q, k, v, k_cache, v_cache, table.to(dev), qs.to(dev), ctx.to(dev),
+                        int(new.max()) if B else 0, int(ctx.max()) if B else 0)

@@ -312,7 +312,152 @@ def pin_golden_partition_counts(orc):
         assert last == c["last_partition_tokens"], f"last partition has {last} tokens"
 
 
+# --------------------------------------------------------------------------
+# paged prefix prefill (commit 1a4e1005 "paged_attn.py", opening paragraph;
+# commit 4eb83a7e "qwen3_6_scripts", paragraphs on the prefix attention's
+# pre-allocated buffers, "Complete rewrite ..." item 1, "Prefill
+# (flash_attn_func)": context from the paged cache, the chunk causal)
+# --------------------------------------------------------------------------
+def _prefill(orc, pb, **kw):
+    return orc.prefill(pb.q, pb.k, pb.v, pb.k_cache, pb.v_cache, pb.block_tables,
+                       pb.query_start, pb.ctx_lens, pb.scale, **kw)
+
+
+def _prefill_dense(pb):
+    """Brute force with torch: gather each sequence's context from the cache
+    by indexing, append the chunk's keys / values, and call
+    scaled_dot_product_attention in float64 with an explicit boolean mask
+    (context visible, chunk lower-triangular)."""
+    w = pb.workload
+    G = w.num_heads // w.num_kv_heads
+    T = pb.q.shape[0]
+    out = torch.zeros(T, w.num_heads, w.head_dim, dtype=torch.float64)
+    for b in range(w.num_seqs):
+        C = int(pb.ctx_lens[b])
+        s0, s1 = int(pb.query_start[b]), int(pb.query_start[b + 1])
+        n = s1 - s0
+        if n == 0:
+            continue
+        t = torch.arange(C)
+        blk = pb.block_tables[b, t // w.block_size].long()
+        off = t % w.block_size
+        for h in range(w.num_heads):
+            kvh = h // G
+            K = torch.cat([pb.k_cache[blk, kvh, off].double(), pb.k[s0:s1, kvh].double()])
+            V = torch.cat([pb.v_cache[blk, kvh, off].double(), pb.v[s0:s1, kvh].double()])
+            Q = pb.q[s0:s1, h].double()
+            mask = torch.ones(n, C + n, dtype=torch.bool)
+            mask[:, C:] = torch.tril(torch.ones(n, n, dtype=torch.bool))
+            o = F.scaled_dot_product_attention(Q[None, None], K[None, None], V[None, None],
+                                               attn_mask=mask[None, None], scale=pb.scale)
+            out[s0:s1, h] = o[0, 0]
+    return out.numpy()
+
+
+def pin_prefill_brute_force(orc):
+    """Against torch SDPA with an explicit mask, for batches mixing an empty
+    context, ragged contexts and chunks, GQA and each element type."""
+    for dtype, ctx, new, Hq, Hkv, D, BS in (
+            (torch.float32, (23, 0, 40), (9, 13, 1), 6, 2, 16, 4),
+            (torch.bfloat16, (50, 7), (20, 33), 4, 4, 32, 16),
+            (torch.float16, (0,), (29,), 3, 1, 8, 8)):
+        pb = wl.make_prefill(wl.prefill_problem(dtype=dtype, ctx=ctx, new=new, Hq=Hq, Hkv=Hkv,
+                                                D=D, BS=BS, seed=41), poison=True)
+        _close(_prefill(orc, pb), _prefill_dense(pb), 1e-12, f"prefill brute force {dtype}")
+
+
+def pin_prefill_one_token_is_decode(orc):
+    """A chunk of one token after C cached ones is a single-token decode over
+    C + 1 tokens: write the token's key / value into slot C of a decode
+    cache and compare with the decode oracle (itself pinned above)."""
+    lens = (41, 1, 16)
+    d = problem(dtype=torch.float32, lens=lens, Hq=6, Hkv=3, D=16, BS=4, seed=17, poison=False)
+    B = len(lens)
+    pos = torch.tensor([L - 1 for L in lens])
+    blk = d.block_tables[torch.arange(B), pos // 4].long()
+    off = pos % 4
+    k_new = d.k_cache[blk, :, off].clone()          # [B, Hkv, D]: the last token's rows
+    v_new = d.v_cache[blk, :, off].clone()
+    kc, vc = d.k_cache.clone(), d.v_cache.clone()
+    kc[blk, :, off] = float("nan")                   # the prefill must not read slot C
+    vc[blk, :, off] = float("nan")
+    pw = wl.prefill_problem(dtype=torch.float32, ctx=[L - 1 for L in lens], new=[1] * B,
+                            Hq=6, Hkv=3, D=16, BS=4)
+    pb = wl.PrefillBatch(pw, d.q.clone(), k_new, v_new, kc, vc, d.block_tables,
+                         torch.arange(B + 1, dtype=torch.int32),
+                         torch.tensor([L - 1 for L in lens], dtype=torch.int32), 1, max(lens) - 1)
+    _close(_prefill(orc, pb), _run(orc, d), 1e-12, "one-token prefill vs decode")
+
+
+def pin_prefill_no_context_is_causal(orc):
+    """With no cached context the chunk is plain causal self-attention:
+    torch SDPA with is_causal=True (GQA by repeating each KV head over its
+    query heads)."""
+    pb = wl.make_prefill(wl.prefill_problem(dtype=torch.float32, ctx=(0, 0), new=(31, 12),
+                                            Hq=6, Hkv=2, D=16, BS=4, seed=5))
+    got = _prefill(orc, pb)
+    G = 3
+    for b in range(2):
+        s0, s1 = int(pb.query_start[b]), int(pb.query_start[b + 1])
+        Q = pb.q[s0:s1].double().transpose(0, 1)                        # [Hq, n, D]
+        K = pb.k[s0:s1].double().transpose(0, 1).repeat_interleave(G, 0)
+        V = pb.v[s0:s1].double().transpose(0, 1).repeat_interleave(G, 0)
+        ref = F.scaled_dot_product_attention(Q, K, V, is_causal=True, scale=pb.scale)
+        _close(got[s0:s1], ref.transpose(0, 1).numpy(), 1e-12, f"causal sequence {b}")
+
+
+def pin_prefill_prefix_means(orc):
+    """Closed form: with q = 0 every visible logit is 0, so row i is the
+    plain mean of the context values and of the chunk values 0..i."""
+    pb = wl.make_prefill(wl.prefill_problem(dtype=torch.float32, ctx=(10, 0), new=(6, 4),
+                                            Hq=2, Hkv=1, D=4, BS=4, seed=8))
+    pb.q.zero_()
+    got = _prefill(orc, pb)
+    for b in range(2):
+        C = int(pb.ctx_lens[b])
+        s0, s1 = int(pb.query_start[b]), int(pb.query_start[b + 1])
+        t = torch.arange(C)
+        ctx_v = pb.v_cache[pb.block_tables[b, t // 4].long(), 0, t % 4].double()
+        for i in range(s1 - s0):
+            vis = torch.cat([ctx_v, pb.v[s0:s0 + i + 1, 0].double()])
+            for h in range(2):
+                _close(got[s0 + i, h], vis.mean(0).numpy(), 1e-13, f"prefix mean b={b} i={i}")
+
+
+def pin_prefill_causality(orc):
+    """Changing the key and value of chunk token j changes the rows of tokens
+    i >= j of that sequence only."""
+    pb = wl.make_prefill(wl.prefill_problem(dtype=torch.float32, ctx=(9, 5), new=(8, 6),
+                                            Hq=2, Hkv=1, D=8, BS=4, seed=12))
+    base = _prefill(orc, pb)
+    j = int(pb.query_start[0]) + 4
+    pb.k[j] += 3.0
+    pb.v[j] -= 2.0
+    moved = np.abs(_prefill(orc, pb) - base).max(axis=(1, 2)) > 0
+    expect = np.zeros(pb.q.shape[0], dtype=bool)
+    expect[j:int(pb.query_start[1])] = True
+    assert np.array_equal(moved, expect), f"rows changed: {np.nonzero(moved)[0].tolist()}"
+
+
+def pin_prefill_tiled_is_direct(orc):
+    """The pages' tiled online softmax (context tiles, then chunk tiles,
+    with m_blk / m_new / corr) reaches the plain definition for any tile."""
+    pb = wl.make_prefill(wl.prefill_problem(dtype=torch.bfloat16, ctx=(45, 0, 16), new=(20, 9, 3),
+                                            Hq=4, Hkv=2, D=16, BS=8, seed=23), poison=True)
+    direct = _prefill(orc, pb)
+    for tile in (1, 7, 16, 128):
+        tiled = orc.prefill_tiled(pb.q, pb.k, pb.v, pb.k_cache, pb.v_cache, pb.block_tables,
+                                  pb.query_start, pb.ctx_lens, pb.scale, tile)
+        _close(tiled, direct, 1e-13, f"tiled prefill, tile {tile}")
+
+
 ALL_PINS = [
+    pin_prefill_brute_force,
+    pin_prefill_one_token_is_decode,
+    pin_prefill_no_context_is_causal,
+    pin_prefill_prefix_means,
+    pin_prefill_causality,
+    pin_prefill_tiled_is_direct,
     pin_brute_force,
     pin_partition_identity,
     pin_single_key,

@@ -38,6 +38,22 @@ MUTANTS = [
     ("phase2_first_max_only", "if (m[p] > gmax) gmax = m[p];", "gmax = m[0];"),
     ("rescale_sign", "const double wgt = exp(m[p] - gmax) * sp[p] / total;",
      "const double wgt = exp(gmax - m[p]) * sp[p] / total;"),
+    # paged prefix prefill
+    ("prefill_causal_exclusive", "const int64_t nvis = (int64_t)C + (t - qs) + 1;",
+     "const int64_t nvis = (int64_t)C + (t - qs);"),
+    ("prefill_context_dropped", "const int64_t nvis = (int64_t)C + (t - qs) + 1;",
+     "const int64_t nvis = (t - qs) + 1;"),
+    ("prefill_new_row_ignores_sequence_start",
+     "*base = (((int64_t)qs + (j - C)) * s->num_kv_heads + kvh) * (int64_t)s->head_dim;",
+     "*base = ((j - C) * s->num_kv_heads + kvh) * (int64_t)s->head_dim;"),
+    ("prefill_context_slot_off_by_one",
+     "*base = orc_row(s, blk, kvh, (int)(j % s->block_size));",
+     "*base = orc_row(s, blk, kvh, (int)((j + 1) % s->block_size));"),
+    ("prefill_tiled_corr_sign", "const double corr = m == -INFINITY ? 0.0 : exp(m - m_new);",
+     "const double corr = m == -INFINITY ? 0.0 : exp(m_new - m);"),
+    ("prefill_tiled_sum_not_corrected", "    lsum *= corr;\n", ""),
+    ("prefill_tiled_skips_context", "const int64_t end = phase == 0 ? C : i + 1;",
+     "const int64_t end = phase == 0 ? 0 : i + 1;"),
 ]
 
 
