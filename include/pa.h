@@ -278,6 +278,59 @@ PA_API pa_status_t pa_workspace_init(void* workspace, size_t workspace_bytes, cu
 PA_API pa_status_t pa_read_device_status(const void* workspace, int32_t* status, int clear,
                                   cudaStream_t stream);
 
+/*
+ * Paged prefix prefill (chunked prefill): sequence b attends a chunk of n_b
+ * new tokens to its C_b cached tokens and, causally, to the chunk itself.
+ * Source: commit 1a4e1005 "paged_attn.py", opening paragraph (prefill is
+ * online softmax over key tiles); commit 4eb83a7e "qwen3_6_scripts",
+ * paragraphs on the prefix attention's pre-allocated m_blk / m_new / corr
+ * buffers (a tile loop over the cached context, then one over the chunk),
+ * "Complete rewrite of qwen3_6_scripts/paged_attn.py" item 1 (the context
+ * comes from the paged cache) and "Prefill (flash_attn_func)" (causal).
+ *
+ *   q    [kv_dtype] [T, num_heads, head_dim]    the chunk's queries
+ *   k, v [kv_dtype] [T, num_kv_heads, head_dim] the chunk's keys / values
+ *   k_cache, v_cache, block_tables: as for decode; only each sequence's
+ *        first ctx_lens[b] tokens are read
+ *   query_start [int32] [num_seqs + 1]: sequence b owns rows
+ *        query_start[b] .. query_start[b+1] - 1 of q / k / v / out
+ *   ctx_lens    [int32] [num_seqs]: C_b cached tokens
+ *   out  [out_dtype] [T, num_heads, head_dim]
+ * Row i of sequence b (0-based in its chunk), query head h, reads KV head
+ * h / (num_heads / num_kv_heads) and gives
+ *   softmax(scale * q . k_j) over j = the C_b context tokens and the chunk's
+ *   tokens 0..i, applied to the matching values.
+ * Tensor-core kernel only: bf16 or f16, head_dim 128 (block_size 16, 32, 64)
+ * or 256 (block_size 16, 32); anything else is PA_ERR_UNSUPPORTED.
+ * Device-side checks: a sequence whose chunk does not satisfy
+ * 0 <= n_b <= max_query_len and query_start[b+1] <= total_tokens is skipped
+ * (its rows are not written); a context length outside
+ * 0..min(max_ctx_len, max_blocks_per_seq * block_size), or a context block
+ * id outside the pool, makes the affected rows NaN.  Asynchronous on
+ * `stream`; no workspace.
+ */
+typedef struct pa_prefill_params {
+  int32_t num_seqs;           /* B >= 0                                      */
+  int32_t num_heads;          /* Hq >= 1                                     */
+  int32_t num_kv_heads;       /* Hkv >= 1, divides Hq                        */
+  int32_t head_dim;           /* D: 128 or 256                               */
+  int32_t block_size;         /* tokens per cache block                      */
+  int32_t num_blocks;         /* blocks in each cache pool                   */
+  int32_t max_blocks_per_seq; /* row length of block_tables                  */
+  int32_t total_tokens;       /* T: rows of q / k / v / out                  */
+  int32_t max_query_len;      /* host-known bound of every n_b               */
+  int32_t max_ctx_len;        /* host-known bound of every C_b               */
+  pa_dtype_t kv_dtype;        /* PA_BF16 or PA_F16: q, k, v and the caches   */
+  pa_dtype_t out_dtype;       /* PA_F32 or kv_dtype                          */
+  float scale;                /* logit scale, usually 1/sqrt(head_dim)       */
+  int32_t flags;              /* 0                                           */
+} pa_prefill_params_t;
+
+PA_API pa_status_t pa_prefill(const pa_prefill_params_t* params, const void* q, const void* k,
+                              const void* v, const void* k_cache, const void* v_cache,
+                              const int32_t* block_tables, const int32_t* query_start,
+                              const int32_t* ctx_lens, void* out, cudaStream_t stream);
+
 /* ABI version: major * 10000 + minor * 100 + patch. */
 PA_API int pa_version(void);
 

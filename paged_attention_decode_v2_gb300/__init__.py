@@ -40,7 +40,7 @@ DEFAULT_V1_MAX_SEQ_LEN = 8192
 EXPORTS = ("pa_workspace_size", "pa_decode_v1", "pa_decode_v2", "pa_decode_v2_partitions",
            "pa_decode_v2_reduce", "pa_decode", "pa_decode_path", "pa_status_string",
            "pa_workspace_init", "pa_read_device_status", "pa_version", "pa_decode_v2_static",
-           "pa_decode_kernel", "pa_host_staging_size", "pa_decode_host")
+           "pa_decode_kernel", "pa_host_staging_size", "pa_decode_host", "pa_prefill")
 PA_STATIC_WORKSPACE_BYTES = 16 << 20
 
 
@@ -63,6 +63,26 @@ class Params(ctypes.Structure):
         ("max_seq_len", ctypes.c_int32),
         ("partition_size", ctypes.c_int32),
         ("v1_max_seq_len", ctypes.c_int32),
+        ("kv_dtype", ctypes.c_int32),
+        ("out_dtype", ctypes.c_int32),
+        ("scale", ctypes.c_float),
+        ("flags", ctypes.c_int32),
+    ]
+
+
+class PrefillParams(ctypes.Structure):
+    """Mirror of ``pa_prefill_params_t``."""
+    _fields_ = [
+        ("num_seqs", ctypes.c_int32),
+        ("num_heads", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("block_size", ctypes.c_int32),
+        ("num_blocks", ctypes.c_int32),
+        ("max_blocks_per_seq", ctypes.c_int32),
+        ("total_tokens", ctypes.c_int32),
+        ("max_query_len", ctypes.c_int32),
+        ("max_ctx_len", ctypes.c_int32),
         ("kv_dtype", ctypes.c_int32),
         ("out_dtype", ctypes.c_int32),
         ("scale", ctypes.c_float),
@@ -116,6 +136,8 @@ def lib() -> ctypes.CDLL:
             L.pa_decode_host.argtypes = [PP, P, P, P, P, P, P, ctypes.c_size_t, P, ctypes.c_size_t,
                                          P, P]
             L.pa_decode_host.restype = ctypes.c_int
+            L.pa_prefill.argtypes = [ctypes.POINTER(PrefillParams), P, P, P, P, P, P, P, P, P, P]
+            L.pa_prefill.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -381,3 +403,54 @@ def read_device_status(workspace, clear: bool = True, stream=None) -> int:
 
 def version() -> int:
     return int(lib().pa_version())
+
+
+def make_prefill_params(q, k_cache, block_tables, *, max_query_len: int, max_ctx_len: int,
+                        scale: float, out_dtype=None, flags: int = 0) -> PrefillParams:
+    """Fill a :class:`PrefillParams` from tensor shapes (no device access)."""
+    total_tokens, num_heads, head_dim = q.shape
+    num_blocks, num_kv_heads, block_size, d2 = cache_dims(k_cache)
+    if d2 != head_dim:
+        raise PaError(PA_ERR_INVALID_ARG, "q and k_cache head_dim differ")
+    return PrefillParams(block_tables.shape[0], num_heads, num_kv_heads, head_dim, block_size,
+                         num_blocks, block_tables.shape[1], total_tokens, int(max_query_len),
+                         int(max_ctx_len), _dtype_code(k_cache.dtype),
+                         _dtype_code(out_dtype if out_dtype is not None else q.dtype),
+                         float(scale), int(flags))
+
+
+def prefill(q, k, v, k_cache, v_cache, block_tables, query_start, ctx_lens, out, *,
+            max_query_len: int, max_ctx_len: int, scale: float, flags: int = 0, stream=None):
+    """``pa_prefill``: paged prefix prefill of a chunk of new tokens per
+    sequence.  ``q`` [T, Hq, D], ``k`` / ``v`` [T, Hkv, D], the caches
+    [blocks, Hkv, BS, D], ``block_tables`` [B, max_blocks], ``query_start``
+    [B + 1], ``ctx_lens`` [B], ``out`` [T, Hq, D] (CUDA tensors)."""
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v), ("k_cache", k_cache), ("v_cache", v_cache),
+                    ("block_tables", block_tables), ("query_start", query_start),
+                    ("ctx_lens", ctx_lens), ("out", out)):
+        if not t.is_cuda:
+            raise PaError(PA_ERR_INVALID_ARG, f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise PaError(PA_ERR_INVALID_ARG, f"{name} must be contiguous")
+    for t in (block_tables, query_start, ctx_lens):
+        if t.dtype != torch.int32:
+            raise PaError(PA_ERR_INVALID_ARG, "block_tables, query_start and ctx_lens must be int32")
+    T, hq, d = q.shape
+    nb, hkv, bs, d2 = cache_dims(k_cache)
+    if (tuple(k.shape) != (T, hkv, d) or tuple(v.shape) != (T, hkv, d) or d2 != d or
+            tuple(v_cache.shape) != tuple(k_cache.shape) or tuple(out.shape) != tuple(q.shape)):
+        raise PaError(PA_ERR_INVALID_ARG, "prefill tensor shapes disagree")
+    if not (q.dtype == k.dtype == v.dtype == k_cache.dtype == v_cache.dtype):
+        raise PaError(PA_ERR_INVALID_ARG, "q, k, v and the caches must share one dtype")
+    B = block_tables.shape[0]
+    if tuple(query_start.shape) != (B + 1,) or tuple(ctx_lens.shape) != (B,):
+        raise PaError(PA_ERR_INVALID_ARG, "query_start must be [B + 1] and ctx_lens [B]")
+    params = make_prefill_params(q, k_cache, block_tables, max_query_len=max_query_len,
+                                 max_ctx_len=max_ctx_len, scale=scale, out_dtype=out.dtype,
+                                 flags=flags)
+    st = lib().pa_prefill(ctypes.byref(params), _ptr(q), _ptr(k), _ptr(v), _ptr(k_cache),
+                          _ptr(v_cache), _ptr(block_tables), _ptr(query_start), _ptr(ctx_lens),
+                          _ptr(out), _stream(stream))
+    if st != PA_OK:
+        raise PaError(st, "pa_prefill")

@@ -85,6 +85,40 @@ __device__ __forceinline__ void store_out(void* out, int64_t i, int32_t dtype, f
     static_cast<__half*>(out)[i] = __float2half_rn(v);
 }
 
+// Store 16 consecutive output elements starting at element i (a multiple of
+// 16; the output 16-byte aligned) in the requested output type.
+__device__ __forceinline__ void store_row16(void* out, int64_t i, int32_t dtype,
+                                            const float (&v)[16]) {
+  if (dtype == PA_F32) {
+    float4* p = reinterpret_cast<float4*>(static_cast<float*>(out) + i);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) p[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+  } else {
+    uint32_t w[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (dtype == PA_BF16) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
+        w[k] = *reinterpret_cast<uint32_t*>(&h);
+      } else {
+        __half2 h = __floats2half2_rn(v[2 * k], v[2 * k + 1]);
+        w[k] = *reinterpret_cast<uint32_t*>(&h);
+      }
+    }
+    uint4* p = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + i);
+    p[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    p[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+}
+
+// 16-bit element bits and round-to-nearest conversion, per element type.
+__device__ __forceinline__ uint16_t bits16(__nv_bfloat16 x) { return __bfloat16_as_ushort(x); }
+__device__ __forceinline__ uint16_t bits16(__half x) { return __half_as_ushort(x); }
+__device__ __forceinline__ __nv_bfloat16 round16(float x, __nv_bfloat16*) {
+  return __float2bfloat16_rn(x);
+}
+__device__ __forceinline__ __half round16(float x, __half*) { return __float2half_rn(x); }
+
 // Record a device-side error in the status word (if the call has one).
 __device__ __forceinline__ void set_status(int32_t* status, int32_t code) {
   if (status) atomicExch(status, code);

@@ -1,0 +1,595 @@
+// pa_prefill.cuh -- paged prefix prefill on the tensor cores (tcgen05).
+//
+// A chunk of n_b new tokens of sequence b attends to the sequence's C_b
+// cached tokens (read from the paged cache through the block table) and,
+// causally, to the chunk itself: commit 1a4e1005 "paged_attn.py", opening
+// paragraph (Flash-Attention-style online softmax over key tiles), and
+// commit 4eb83a7e "qwen3_6_scripts", paragraphs on the prefix attention's
+// pre-allocated m_blk / m_new / corr buffers (a tile loop over the context,
+// then one over the chunk), "Complete rewrite of qwen3_6_scripts/
+// paged_attn.py" item 1 (the context comes from the cache) and "Prefill
+// (flash_attn_func)" (causal=True).
+//
+// Work unit: (sequence, query head, 128-query tile of the chunk).  Units are
+// walked last query tile first (the tiles that see the most keys start
+// first) by a persistent grid of one CTA per SM.  Per unit the key tiles
+// (128 keys each) are the context tiles, then the chunk's tiles up to the
+// diagonal one; each tile runs
+//   QK^T  S[q, k] = sum_d Q[q, d] K[k, d]     M = 128 queries, N = 128 keys,
+//         into one of two tensor-memory buffers (the next tile's QK^T runs
+//         while the softmax warps work on this one);
+//   softmax (one thread per query row): tile max over the visible keys, the
+//         running reference max m moves (and the running sum and the output
+//         are rescaled by corr = 2^(m_old - m_new)) only when the tile max
+//         exceeds it by more than 2^8, so p = 2^(s - m) <= 256; p is rounded
+//         to 16 bits for the MMA and the running sum adds the rounded
+//         values, so the result is an exact weighted mean of the values with
+//         weights perturbed by at most one rounding each;
+//   P.V   O[q, d] += sum_k P[q, k] V[k, d]    M = 128, N = head_dim, K = keys,
+//         accumulated in tensor memory (V is the MN-major operand).
+// Roles (192 threads): warp 4 streams q, keys and values with TMA into a
+// ring of 16 KB stages; warp 5 issues the MMAs; warps 0-3 run the softmax
+// and the epilogue.  Every wait is bounded; a wait that gives up makes the
+// CTA's outputs NaN.
+#pragma once
+
+#include <algorithm>
+#include <type_traits>
+
+#include <cuda.h>
+
+#include "pa_device.cuh"
+#include "pa_sm100.cuh"
+
+namespace pa {
+
+namespace pf {
+
+constexpr int kThreads = 192;
+constexpr int kTile = 128;          // queries per unit and keys per key tile
+constexpr int kStage = 16384;       // one ring stage
+constexpr int kMaxStages = 12;      // barrier slots in the control block
+constexpr int kTmemCols = 512;      // S0 | S1 | O
+constexpr int kS1Col = 128;         // second logits buffer
+constexpr int kOCol = 256;          // output accumulator (head_dim columns)
+constexpr float kRescaleLog2 = 8.f; // move the reference max past 2^8 growth only
+constexpr long long kWaitBudget = 4000000000LL;    // cycles (about 2 s)
+constexpr long long kSelftestBudget = 20000000LL;  // cycles (about 10 ms)
+constexpr int kSmemLimit = 227 * 1024;
+
+// Shared memory: q (head_dim / 64 slices of [128 rows][128 B]), P (two
+// 64-key halves of [128 rows][128 B]), the ring, the control block.  Every
+// operand tile starts on a 1024-byte boundary (128-byte swizzle atoms).
+template <int D>
+struct Layout {
+  static constexpr int kSlices = D / 64;
+  static constexpr int kVTokens = kStage / (D * 2);  // keys per value stage
+  static constexpr int kPOff = kSlices * kStage;
+  static constexpr int kRingOff = kPOff + 2 * kStage;
+  static constexpr int kStages =
+      std::min(kMaxStages, (kSmemLimit - kRingOff - 2048) / kStage);
+  static constexpr int kCtrlOff = kRingOff + kStages * kStage;
+  static constexpr int kSmem = kCtrlOff + 1024 + 1024;  // + room to align to 1024
+  static_assert(kSmem <= kSmemLimit, "shared memory");
+  static_assert(kStages >= 4, "ring depth");
+};
+
+struct Ctrl {
+  uint64_t full[kMaxStages];   // stage landed
+  uint64_t empty[kMaxStages];  // stage consumed by its MMAs
+  uint64_t qfull;              // q tile landed
+  uint64_t qempty;             // q tile no longer read
+  uint64_t s_full[2];          // a tile's logits ready (per buffer)
+  uint64_t p_ready;            // P written (128 softmax threads arrive)
+  uint64_t o_done;             // a tile's P.V completed
+  uint64_t tail;               // producer-private: a tail value stage landed
+  uint64_t drain;              // abort path: all issued MMAs finished
+  uint64_t never;              // self-test: nothing ever arrives here
+  uint32_t tmem;
+  int abort;
+};
+static_assert(sizeof(Ctrl) <= 1024, "control block");
+
+// One work unit, decoded the same way by every role.
+struct Unit {
+  int b, h, qt;
+  int32_t s0;      // first row of the sequence's chunk
+  int32_t n;       // chunk tokens
+  int32_t C;       // context tokens (0 when invalid)
+  bool run;        // the unit exists and its sequence's rows are trusted
+  bool poison;     // the context length is invalid: rows become NaN
+  int nctx;        // context key tiles
+  int ntiles;      // context tiles + chunk tiles up to the diagonal
+};
+
+__device__ __forceinline__ Unit unit_at(const PrefillArgs& a, int64_t k) {
+  const int64_t per = static_cast<int64_t>(a.num_seqs) * a.num_heads;
+  Unit u;
+  u.qt = a.qtiles - 1 - static_cast<int>(k / per);
+  const int64_t rem = k % per;
+  u.b = static_cast<int>(rem / a.num_heads);
+  u.h = static_cast<int>(rem % a.num_heads);
+  u.s0 = __ldg(a.query_start + u.b);
+  const int32_t s1 = __ldg(a.query_start + u.b + 1);
+  u.n = s1 - u.s0;
+  const int32_t C = __ldg(a.ctx_lens + u.b);
+  const bool seq_ok = u.s0 >= 0 && u.n >= 0 && u.n <= a.max_query_len && s1 <= a.total_tokens;
+  u.run = seq_ok && u.qt * kTile < u.n;
+  const bool ctx_ok = C >= 0 && C <= a.max_ctx_len &&
+                      static_cast<int64_t>(C) <= static_cast<int64_t>(a.max_blocks_per_seq) *
+                                                     a.block_size;
+  u.poison = !ctx_ok;
+  u.C = ctx_ok ? C : 0;
+  u.nctx = (u.C + kTile - 1) / kTile;
+  u.ntiles = u.nctx + u.qt + 1;
+  return u;
+}
+
+// Keys of key tile j of unit u (context tile or chunk tile).
+__device__ __forceinline__ int tile_keys(const Unit& u, int j) {
+  return j < u.nctx ? min(kTile, u.C - j * kTile) : min(kTile, u.n - (j - u.nctx) * kTile);
+}
+
+__device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+}  // namespace pf
+
+// kcmap / vcmap: the caches as rows of head_dim (box 64 x BS, and a whole
+// block slice-major); qmap / knmap / vnmap: q, k, v as (64, heads, T,
+// head_dim / 64) with boxes (64, 1, 128, 1) for a q or key slice of 128
+// rows and (64, 1, 16, head_dim / 64) for 16 value rows slice-major.
+template <typename T, int D, int BS>
+__global__ void __launch_bounds__(pf::kThreads, 1)
+    pa_prefill_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
+                      const __grid_constant__ CUtensorMap knmap,
+                      const __grid_constant__ CUtensorMap vnmap,
+                      const __grid_constant__ CUtensorMap kcmap,
+                      const __grid_constant__ CUtensorMap vcmap, long long budget) {
+  using namespace pf;
+  using Lay = Layout<D>;
+  constexpr int NST = Lay::kStages;
+  constexpr int kSl = Lay::kSlices;
+  constexpr int kVT = Lay::kVTokens;
+  static_assert(D == 128 || D == 256, "head_dim");
+  static_assert(BS % 16 == 0 && kTile % BS == 0 && kVT % BS == 0, "block size");
+  constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (sm100::smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* qs = smem;
+  uint8_t* ps = smem + Lay::kPOff;
+  uint8_t* ring = smem + Lay::kRingOff;
+  Ctrl& c = *reinterpret_cast<Ctrl*>(smem + Lay::kCtrlOff);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t units = static_cast<int64_t>(a.qtiles) * a.num_seqs * a.num_heads;
+
+  if (tid == 0) {
+    for (int s = 0; s < NST; ++s) {
+      sm100::mbar_init(&c.full[s], 1);
+      sm100::mbar_init(&c.empty[s], 1);
+    }
+    sm100::mbar_init(&c.qfull, 1);
+    sm100::mbar_init(&c.qempty, 1);
+    sm100::mbar_init(&c.s_full[0], 1);
+    sm100::mbar_init(&c.s_full[1], 1);
+    sm100::mbar_init(&c.p_ready, 128);
+    sm100::mbar_init(&c.o_done, 1);
+    sm100::mbar_init(&c.tail, 1);
+    sm100::mbar_init(&c.drain, 1);
+    sm100::mbar_init(&c.never, 1);
+    c.abort = 0;
+  }
+  if (warp == 5) {
+    sm100::tmem_alloc(&c.tmem, kTmemCols);
+    sm100::tmem_relinquish();
+  }
+  if (warp == 4 && lane == 0) {
+    sm100::tma_prefetch_desc(&qmap);
+    sm100::tma_prefetch_desc(&knmap);
+    sm100::tma_prefetch_desc(&vnmap);
+    sm100::tma_prefetch_desc(&kcmap);
+    sm100::tma_prefetch_desc(&vcmap);
+  }
+  sm100::fence_proxy_async_smem();
+  sm100::tc_fence_before();
+  __syncthreads();
+  sm100::tc_fence_after();
+  const uint32_t tmem = c.tmem;
+  volatile int* abort_flag = &c.abort;
+
+  if (warp == 4) {
+    // ========================= producer ===========================================
+    // Per unit: q, then keys of tile 0, then (keys of tile j, values of tile
+    // j - 1) for j >= 1, then the last tile's values -- the order the MMA
+    // warp consumes the ring in.
+    uint64_t keep;  // q, the chunk's keys / values and the context: read by several units
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(keep));
+    uint32_t g = 0, un = 0, tn = 0;
+    int tail_pending = -1;
+    bool ok = true;
+
+    // TMA row of each lane's block in context tile j (lanes past the tile:
+    // 0, unused); a block id outside the pool becomes a negative row, which
+    // TMA fills with zeros instead of reading memory.
+    auto ctx_rows = [&](const Unit& u, int j) -> int32_t {
+      const int nblk = (tile_keys(u, j) + BS - 1) / BS;
+      if (lane >= nblk) return 0;
+      const int32_t id = __ldg(a.block_tables + static_cast<int64_t>(u.b) * a.max_blocks_per_seq +
+                               j * (kTile / BS) + lane);
+      const int kvh = u.h / a.group;
+      return (id < 0 || id >= a.num_blocks) ? -BS : (id * a.num_kv_heads + kvh) * BS;
+    };
+
+    auto issue_k = [&](const Unit& u, int j, int32_t y) -> bool {
+      const int kvh = u.h / a.group;
+      const int nk = tile_keys(u, j);
+      const bool ctx = j < u.nctx;
+      const int nblk = (nk + BS - 1) / BS;
+      for (int sl = 0; sl < kSl; ++sl) {
+        const int slot = g % NST;
+        if (!__all_sync(0xffffffffu, sm100::mbar_wait(&c.empty[slot], ((g / NST) & 1) ^ 1, budget,
+                                                        abort_flag)))
+          return false;
+        uint8_t* st = ring + slot * kStage;
+        if (ctx) {
+          if (lane == 0) sm100::mbar_arrive_expect_tx(&c.full[slot], nblk * BS * 128);
+          __syncwarp();
+          if (lane < nblk)
+            sm100::tma_load_2d(st + lane * BS * 128, &kcmap, &c.full[slot], sl * 64, y, keep);
+        } else {
+          if (lane == 0) {
+            sm100::mbar_arrive_expect_tx(&c.full[slot], kStage);
+            sm100::tma_load_4d(st, &knmap, &c.full[slot], 0, kvh,
+                               u.s0 + (j - u.nctx) * kTile, sl, keep);
+          }
+        }
+        __syncwarp();
+        ++g;
+      }
+      return true;
+    };
+
+    // Values of tile j.  The stage that holds the tile's last key, when that
+    // key ends inside a 16-key MMA step, lands on the producer's own barrier
+    // first and the rows past it are cleared (P is zero there, but 0 * NaN
+    // would be NaN) before the stage is handed to the MMA warp.
+    auto issue_v = [&](const Unit& u, int j, int32_t y) -> bool {
+      const int kvh = u.h / a.group;
+      const int nk = tile_keys(u, j);
+      const bool ctx = j < u.nctx;
+      const int vbs = ctx ? BS : 16;  // rows per copy (cache block / 16 chunk rows)
+      const int nv = (nk + kVT - 1) / kVT;
+      for (int v = 0; v < nv; ++v) {
+        const int slot = g % NST;
+        if (!__all_sync(0xffffffffu, sm100::mbar_wait(&c.empty[slot], ((g / NST) & 1) ^ 1, budget,
+                                                        abort_flag)))
+          return false;
+        const int toks = min(kVT, nk - v * kVT);
+        const int ncp = (toks + vbs - 1) / vbs;  // copies in this stage
+        const bool tail = v == nv - 1 && (nk % 16) != 0;
+        uint64_t* land = tail ? &c.tail : &c.full[slot];
+        uint8_t* st = ring + slot * kStage;
+        if (lane == 0) sm100::mbar_arrive_expect_tx(land, ncp * vbs * D * 2);
+        __syncwarp();
+        if (ctx) {
+          const int jb0 = v * kVT / BS;
+          const int32_t yj = __shfl_sync(0xffffffffu, y, (jb0 + lane) & 31);
+          if (lane < ncp)
+            sm100::tma_load_3d(st + lane * BS * D * 2, &vcmap, land, 0, yj, 0, keep);
+        } else if (lane < ncp) {
+          sm100::tma_load_4d(st + lane * 16 * D * 2, &vnmap, land, 0, kvh,
+                             u.s0 + (j - u.nctx) * kTile + v * kVT + lane * 16, 0, keep);
+        }
+        __syncwarp();
+        ++g;
+        if (tail) {
+          tail_pending = slot;
+          if (!__all_sync(0xffffffffu, sm100::mbar_wait(&c.tail, tn & 1, budget, abort_flag)))
+            return false;
+          ++tn;
+          tail_pending = -1;
+          const int r0 = toks;                  // first row past the tile's last key
+          const int r1 = (r0 + 15) / 16 * 16;   // end of its 16-key step
+          const int pieces = (r1 - r0) * kSl * 8;
+          for (int i = lane; i < pieces; i += 32) {
+            const int line = i / 8, piece = i % 8;
+            const int r = r0 + line / kSl, sl = line % kSl;
+            *reinterpret_cast<uint4*>(st + (r / vbs) * vbs * D * 2 + sl * vbs * 128 +
+                                      (r % vbs) * 128 + piece * 16) = make_uint4(0u, 0u, 0u, 0u);
+          }
+          sm100::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) sm100::mbar_arrive(&c.full[slot]);
+        }
+      }
+      return true;
+    };
+
+    for (int64_t k = blockIdx.x; k < units && ok; k += gridDim.x) {
+      const Unit u = unit_at(a, k);
+      if (!u.run) continue;
+      // q tile (rows past the chunk belong to other sequences or lie past T,
+      // where TMA fills zeros; their rows are never stored)
+      ok = __all_sync(0xffffffffu, sm100::mbar_wait(&c.qempty, (un & 1) ^ 1, budget, abort_flag));
+      if (!ok) break;
+      if (lane == 0) sm100::mbar_arrive_expect_tx(&c.qfull, kSl * kStage);
+      __syncwarp();
+      if (lane < kSl)
+        sm100::tma_load_4d(qs + lane * kStage, &qmap, &c.qfull, 0, u.h, u.s0 + u.qt * kTile, lane,
+                           keep);
+      ++un;
+      int32_t yprev = 0;
+      for (int j = 0; j < u.ntiles && ok; ++j) {
+        const int32_t y = j < u.nctx ? ctx_rows(u, j) : 0;
+        ok = issue_k(u, j, y);
+        if (ok && j > 0) ok = issue_v(u, j - 1, yprev);
+        yprev = y;
+      }
+      if (ok) ok = issue_v(u, u.ntiles - 1, yprev);
+    }
+    if (!ok) {
+      if (lane == 0) c.abort = 1;
+      // copies already issued must land before the CTA may exit
+      for (uint32_t gg = g > NST ? g - NST : 0; gg < g; ++gg)
+        if (static_cast<int>(gg % NST) != tail_pending)
+          sm100::mbar_wait(&c.full[gg % NST], (gg / NST) & 1, budget, nullptr);
+      if (tail_pending >= 0) sm100::mbar_wait(&c.tail, tn & 1, budget, nullptr);
+      if (un > 0) sm100::mbar_wait(&c.qfull, (un - 1) & 1, budget, nullptr);
+    }
+  } else if (warp == 5) {
+    // ========================= MMA issuer =========================================
+    // The whole warp runs the loop in convergent code; one elected lane
+    // issues each MMA and commit.  Per unit: QK^T(0), then (QK^T(j),
+    // P.V(j - 1)) for j >= 1, then P.V(last), so the next tile's logits are
+    // computed while the softmax warps work on this tile's.
+    constexpr unsigned kAll = 0xffffffffu;
+    constexpr uint32_t id_qk = sm100::idesc_f16(kBf16, false, false, 128, kTile);
+    constexpr uint32_t id_pv = sm100::idesc_f16(kBf16, false, true, 128, D);
+    const uint32_t q_base = sm100::smem_u32(qs);
+    const uint32_t p_base = sm100::smem_u32(ps);
+    const uint32_t ring_base = sm100::smem_u32(ring);
+    uint32_t g = 0, un = 0, gt = 0, pn = 0;
+    bool ok = true;
+    if (a.selftest_stall) ok = __all_sync(kAll, sm100::mbar_wait(&c.never, 0, budget, abort_flag));
+
+    auto qk = [&]() -> bool {
+      const uint32_t sbuf = tmem + ((gt & 1) ? kS1Col : 0);
+      for (int sl = 0; sl < kSl; ++sl) {
+        const int slot = g % NST;
+        if (!__all_sync(kAll, sm100::mbar_wait(&c.full[slot], (g / NST) & 1, budget, abort_flag)))
+          return false;
+        sm100::tc_fence_after();
+        const uint32_t st = ring_base + slot * kStage;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t ad = sm100::smem_desc(q_base + sl * kStage + kk * 32, 16, 1024, sm100::kSw128);
+          const uint64_t bd = sm100::smem_desc(st + kk * 32, 16, 1024, sm100::kSw128);
+          sm100::mma_f16_elect(sbuf, ad, bd, id_qk, (sl | kk) != 0);
+        }
+        sm100::mma_commit_elect(&c.empty[slot]);
+        ++g;
+      }
+      return true;
+    };
+    auto pv = [&](const Unit& u, int j) -> bool {
+      if (!__all_sync(kAll, sm100::mbar_wait(&c.p_ready, pn & 1, budget, abort_flag))) return false;
+      ++pn;
+      sm100::tc_fence_after();
+      const int nk = tile_keys(u, j);
+      const int vbs = j < u.nctx ? BS : 16;
+      const int nv = (nk + kVT - 1) / kVT;
+      for (int v = 0; v < nv; ++v) {
+        const int slot = g % NST;
+        if (!__all_sync(kAll, sm100::mbar_wait(&c.full[slot], (g / NST) & 1, budget, abort_flag)))
+          return false;
+        sm100::tc_fence_after();
+        const uint32_t st = ring_base + slot * kStage;
+        const int toks = min(kVT, nk - v * kVT);
+        for (int r = 0; r < toks; r += 16) {
+          const int key = v * kVT + r;
+          const uint64_t ad = sm100::smem_desc(p_base + (key / 64) * kStage + ((key % 64) / 16) * 32,
+                                               16, 1024, sm100::kSw128);
+          const uint64_t bd = sm100::smem_desc(st + (r / vbs) * vbs * D * 2 + (r % vbs) * 128,
+                                               vbs * 128, 1024, sm100::kSw128);
+          sm100::mma_f16_elect(tmem + kOCol, ad, bd, id_pv, (j | v | r) != 0);
+        }
+        sm100::mma_commit_elect(&c.empty[slot]);
+        ++g;
+      }
+      sm100::mma_commit_elect(&c.o_done);
+      return true;
+    };
+
+    for (int64_t k = blockIdx.x; k < units && ok; k += gridDim.x) {
+      const Unit u = unit_at(a, k);
+      if (!u.run) continue;
+      ok = __all_sync(kAll, sm100::mbar_wait(&c.qfull, un & 1, budget, abort_flag));
+      if (!ok) break;
+      ++un;
+      sm100::tc_fence_after();
+      for (int j = 0; j < u.ntiles && ok; ++j) {
+        ok = qk();
+        if (!ok) break;
+        if (j == u.ntiles - 1) sm100::mma_commit_elect(&c.qempty);
+        sm100::mma_commit_elect(&c.s_full[gt & 1]);
+        ++gt;
+        if (j > 0) ok = pv(u, j - 1);
+      }
+      if (ok) ok = pv(u, u.ntiles - 1);
+    }
+    if (!ok) {
+      if (lane == 0) c.abort = 1;
+      // no MMA may still be running when tensor memory is released
+      sm100::mma_commit_elect(&c.drain);
+      sm100::mbar_wait(&c.drain, 0, budget, nullptr);
+    }
+    __syncwarp();
+  } else {
+    // ========================= softmax + epilogue (warps 0-3) =====================
+    // Thread r owns query row r of the unit (tensor-memory lane r).  Every
+    // softmax thread runs the same iterations whatever happens; a failed
+    // wait only marks the abort, which ends later waits.
+    const int r = tid;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const float sl2 = a.scale_log2;
+    uint32_t gt = 0;  // key tiles so far (logits buffer, s_full / o_done phases)
+    for (int64_t k = blockIdx.x; k < units; k += gridDim.x) {
+      const Unit u = unit_at(a, k);
+      if (!u.run) continue;
+      const int i = u.qt * kTile + r;  // this row's place in the chunk
+      const bool row_ok = i < u.n;
+      float m_ref = -INFINITY, lsum = 0.f;
+      bool bad = u.poison;
+      for (int j = 0; j < u.ntiles; ++j, ++gt) {
+        const int nk = tile_keys(u, j);
+        const bool ctx = j < u.nctx;
+        // visible keys of the tile form a prefix: all context keys, chunk keys
+        // up to the row's own
+        const int vis = ctx ? nk : max(0, min(nk, i - (j - u.nctx) * kTile + 1));
+        if (ctx) {  // context block ids: one outside the pool poisons the unit
+          const int nblk = (nk + BS - 1) / BS;
+          bool bl = false;
+          if (lane < nblk) {
+            const int32_t id = __ldg(a.block_tables +
+                                     static_cast<int64_t>(u.b) * a.max_blocks_per_seq +
+                                     j * (kTile / BS) + lane);
+            bl = id < 0 || id >= a.num_blocks;
+          }
+          bad |= __any_sync(0xffffffffu, bl);
+        }
+        if (!sm100::mbar_wait(&c.s_full[gt & 1], (gt >> 1) & 1, budget, abort_flag)) c.abort = 1;
+        sm100::tc_fence_after();
+        __syncwarp();
+        const uint32_t sbuf = tmem + lane_base + ((gt & 1) ? kS1Col : 0);
+        float mx = -INFINITY;
+#pragma unroll 1
+        for (int c0 = 0; c0 < kTile; c0 += 16) {
+          float sv[16];
+          sm100::tmem_ld16(sbuf + c0, sv);
+          sm100::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            if (c0 + e < vis) mx = fmaxf(mx, sv[e]);
+        }
+        const float mt = mx * sl2;
+        // P.V of the previous tile must be done: it reads P, and O is rescaled
+        if (j > 0) {
+          if (!sm100::mbar_wait(&c.o_done, (gt - 1) & 1, budget, abort_flag)) c.abort = 1;
+          sm100::tc_fence_after();
+          __syncwarp();
+        }
+        const float m_new = fmaxf(m_ref, mt);
+        const bool move = m_new > m_ref + kRescaleLog2;
+        float corr = 1.f;
+        if (move) {
+          corr = m_ref == -INFINITY ? 0.f : exp2f(m_ref - m_new);
+          lsum *= corr;
+          m_ref = m_new;
+        }
+        if (j > 0 && __any_sync(0xffffffffu, move)) {
+          // the warp's rows that moved their reference max rescale their O row
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 16) {
+            float ov[16];
+            sm100::tmem_ld16(tmem + lane_base + kOCol + c0, ov);
+            sm100::tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) ov[e] *= corr;
+            sm100::tmem_st16(tmem + lane_base + kOCol + c0, ov);
+          }
+          sm100::tmem_wait_st();
+        }
+        // p = 2^(s * scale * log2(e) - m_ref) for the visible keys, rounded to
+        // 16 bits into P (row r, 128-byte swizzled rows of two 64-key halves)
+#pragma unroll 1
+        for (int c0 = 0; c0 < kTile; c0 += 16) {
+          float sv[16];
+          sm100::tmem_ld16(sbuf + c0, sv);
+          sm100::tmem_wait_ld();
+          uint32_t w[8];
+#pragma unroll
+          for (int e = 0; e < 16; e += 2) {
+            const float p0 = c0 + e < vis ? exp2f(sv[e] * sl2 - m_ref) : 0.f;
+            const float p1 = c0 + e + 1 < vis ? exp2f(sv[e + 1] * sl2 - m_ref) : 0.f;
+            const T h0 = round16(p0, static_cast<T*>(nullptr));
+            const T h1 = round16(p1, static_cast<T*>(nullptr));
+            lsum += to_float(h0) + to_float(h1);
+            w[e / 2] = static_cast<uint32_t>(bits16(h0)) | (static_cast<uint32_t>(bits16(h1)) << 16);
+          }
+#pragma unroll
+          for (int half8 = 0; half8 < 2; ++half8) {
+            const int key = c0 + half8 * 8;  // 8 keys = one 16-byte piece
+            const int piece = ((key % 64) / 8) ^ (r & 7);
+            *reinterpret_cast<uint4*>(ps + (key / 64) * kStage + r * 128 + piece * 16) =
+                make_uint4(w[half8 * 4 + 0], w[half8 * 4 + 1], w[half8 * 4 + 2], w[half8 * 4 + 3]);
+          }
+        }
+        sm100::fence_proxy_async_smem();
+        sm100::tc_fence_before();
+        sm100::mbar_arrive(&c.p_ready);
+      }
+      // ---- epilogue of the unit: O / lsum into out ---------------------------------
+      if (!sm100::mbar_wait(&c.o_done, (gt - 1) & 1, budget, abort_flag)) c.abort = 1;
+      sm100::tc_fence_after();
+      __syncwarp();
+      const bool poison = bad || *abort_flag != 0;
+      const float inv = 1.f / lsum;
+      const int64_t orow = (static_cast<int64_t>(u.s0) + i) * a.num_heads + u.h;
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 16) {
+        float ov[16];
+        sm100::tmem_ld16(tmem + lane_base + kOCol + c0, ov);
+        sm100::tmem_wait_ld();
+        if (row_ok) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) ov[e] = poison ? qnan() : ov[e] * inv;
+          store_row16(a.out, orow * D + c0, a.out_dtype, ov);
+        }
+      }
+      sm100::tc_fence_before();
+    }
+  }
+
+  // ---- teardown -------------------------------------------------------------------
+  sm100::tc_fence_before();
+  __syncthreads();
+  sm100::tc_fence_after();
+  if (warp == 5) sm100::tmem_dealloc(tmem, kTmemCols);
+}
+
+// Persistent launch: one CTA per SM (the kernel takes ~226 KB of shared
+// memory and all 512 tensor-memory columns), at most one per unit.
+template <typename T, int D, int BS>
+cudaError_t launch_prefill_t(const PrefillArgs& a, const CUtensorMap (&m)[5], int num_sms,
+                             cudaStream_t s) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+  auto kern = pa_prefill_kernel<T, D, BS>;
+  static bool configured[128] = {};
+  if (!configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         pf::Layout<D>::kSmem);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  const int64_t units = static_cast<int64_t>(a.qtiles) * a.num_seqs * a.num_heads;
+  if (units == 0) return cudaSuccess;
+  const unsigned grid = static_cast<unsigned>(std::min<int64_t>(units, num_sms));
+  const long long budget = a.selftest_stall ? pf::kSelftestBudget : pf::kWaitBudget;
+  kern<<<grid, pf::kThreads, pf::Layout<D>::kSmem, s>>>(a, m[0], m[1], m[2], m[3], m[4], budget);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_prefill_dtype(const PrefillArgs& a, const CUtensorMap (&m)[5], int num_sms,
+                                 cudaStream_t s) {
+  if (a.head_dim == 256 && a.block_size == 16) return launch_prefill_t<T, 256, 16>(a, m, num_sms, s);
+  if (a.head_dim == 256 && a.block_size == 32) return launch_prefill_t<T, 256, 32>(a, m, num_sms, s);
+  if (a.head_dim == 128 && a.block_size == 16) return launch_prefill_t<T, 128, 16>(a, m, num_sms, s);
+  if (a.head_dim == 128 && a.block_size == 32) return launch_prefill_t<T, 128, 32>(a, m, num_sms, s);
+  if (a.head_dim == 128 && a.block_size == 64) return launch_prefill_t<T, 128, 64>(a, m, num_sms, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace pa

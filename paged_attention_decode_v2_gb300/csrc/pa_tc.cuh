@@ -193,12 +193,6 @@ __device__ __forceinline__ void fail(Ctrl& c, int32_t* status) {
   set_status(status, PA_ERR_DEVICE_TIMEOUT);
 }
 
-__device__ __forceinline__ uint16_t bits16(__nv_bfloat16 x) { return __bfloat16_as_ushort(x); }
-__device__ __forceinline__ uint16_t bits16(__half x) { return __half_as_ushort(x); }
-__device__ __forceinline__ __nv_bfloat16 round16(float x, __nv_bfloat16*) {
-  return __float2bfloat16_rn(x);
-}
-__device__ __forceinline__ __half round16(float x, __half*) { return __float2half_rn(x); }
 
 }  // namespace tc
 

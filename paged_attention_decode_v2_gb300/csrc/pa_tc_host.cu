@@ -62,6 +62,32 @@ const DeviceInfo& device_info() {
 
 }  // namespace
 
+cudaError_t encode_tiled(CUtensorMap* map, pa_dtype_t dtype, uint32_t rank, const void* base,
+                         const uint64_t* dims, const uint64_t* strides, const uint32_t* box) {
+  auto enc = encoder();
+  if (!enc) return cudaErrorNotSupported;
+  const CUtensorMapDataType dt =
+      dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  cuuint64_t d[5], st[4];
+  cuuint32_t bx[5], es[5];
+  for (uint32_t i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+    if (i + 1 < rank) st[i] = strides[i];
+  }
+  return enc(map, dt, rank, const_cast<void*>(base), d, st, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+             ? cudaSuccess
+             : cudaErrorInvalidValue;
+}
+
+int sm100_num_sms() {
+  const DeviceInfo& d = device_info();
+  return d.state == 1 ? d.num_sms : 0;
+}
+
 bool tc_applicable(const pa_params_t* p) {
   if (p->flags & (PA_FLAG_PORTABLE | PA_FLAG_SPLIT_X)) return false;
   if (p->kv_dtype != PA_BF16 && p->kv_dtype != PA_F16) return false;

@@ -43,3 +43,24 @@ def test_wait_that_runs_out_reports_timeout_and_context_survives():
     assert pa.read_device_status(ws) == pa.PA_OK
     ref = oracle.decode(bc.q, bc.k_cache, bc.v_cache, bc.block_tables, bc.seq_lens, bc.scale)
     assert float(np.max(np.abs(out.double().cpu().numpy() - ref))) <= 2e-3
+
+
+def test_prefill_wait_that_runs_out_gives_nan_and_context_survives():
+    """The prefill kernel's bounded waits: with PA_FLAG_SELFTEST_STALL its
+    MMA warp waits for an event that never happens, gives up after ~10 ms,
+    drains and returns; the outputs are NaN and the next call is correct."""
+    pb = wl.make_prefill(wl.prefill_problem(dtype=torch.bfloat16, ctx=(300,), new=(200,), Hq=4,
+                                            Hkv=2, D=128, BS=16, seed=1))
+    g = pb.to("cuda")
+    out = torch.zeros(tuple(g.q.shape), dtype=torch.float32, device="cuda")
+    kw = dict(max_query_len=pb.max_query_len, max_ctx_len=pb.max_ctx_len, scale=pb.scale)
+    pa.prefill(g.q, g.k, g.v, g.k_cache, g.v_cache, g.block_tables, g.query_start, g.ctx_lens,
+               out, flags=pa.PA_FLAG_SELFTEST_STALL, **kw)
+    torch.cuda.synchronize()
+    assert torch.isnan(out).all().item()
+    pa.prefill(g.q, g.k, g.v, g.k_cache, g.v_cache, g.block_tables, g.query_start, g.ctx_lens,
+               out, **kw)
+    torch.cuda.synchronize()
+    ref = oracle.prefill(pb.q, pb.k, pb.v, pb.k_cache, pb.v_cache, pb.block_tables,
+                         pb.query_start, pb.ctx_lens, pb.scale)
+    assert float(np.max(np.abs(out.double().cpu().numpy() - ref))) <= 4e-3
