@@ -348,6 +348,194 @@ def run_ours(args, rank, world, device):
 
 
 # ---------------------------------------------------------------------------
+# prefill workloads (pa_prefill): TFLOP/s of the causal attention work
+# ---------------------------------------------------------------------------
+PREFILL_METRIC = "paged prefix-prefill attention TFLOP/s (causal FLOPs, tensor-core roofline)"
+PREFILL_UNIT = "TFLOP/s"
+
+
+def prefill_flops(pb) -> int:
+    """Algorithmic FLOPs of one prefill step: 4 * D per (query head, query,
+    visible key) -- 2 D for q . k and 2 D for p * v -- where query i of
+    sequence b sees its C_b context tokens and chunk tokens 0..i."""
+    w = pb.workload
+    total = 0
+    for b in range(w.num_seqs):
+        n = int(pb.query_start[b + 1]) - int(pb.query_start[b])
+        C = int(pb.ctx_lens[b])
+        total += n * C + n * (n + 1) // 2
+    return 4 * w.head_dim * w.num_heads * total
+
+
+def measured_tensor_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback"
+
+
+def run_prefill(args, rank, world, device):
+    w = wl.PREFILL_WORKLOADS[args.workload]
+    pb = wl.make_prefill(w, device=device)
+    out = torch.empty(tuple(pb.q.shape), dtype=torch.float32, device=device)
+    flush_buf = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=device)
+    flush_sink = torch.empty((), dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream(device)
+    kw = dict(max_query_len=pb.max_query_len, max_ctx_len=pb.max_ctx_len, scale=pb.scale)
+
+    def flush():
+        torch.amax(flush_buf, dim=0, out=flush_sink)
+        torch.cuda._sleep(200_000)
+
+    def step(q, k, v, qs, cl, bt, o):
+        pa.prefill(q, k, v, pb.k_cache, pb.v_cache, bt, qs, cl, o, **kw)
+
+    flops = prefill_flops(pb)
+    sampler = ClockSampler(gpu_id_for_smi(device))
+    if rank == 0:
+        sampler.start()
+    for _ in range(args.warmup):
+        flush()
+        step(pb.q, pb.k, pb.v, pb.query_start, pb.ctx_lens, pb.block_tables, out)
+    torch.cuda.synchronize(device)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(device)
+    t_start = time.time()
+    for i in range(args.steps):
+        flush()
+        ev[i][0].record(stream)
+        step(pb.q, pb.k, pb.v, pb.query_start, pb.ctx_lens, pb.block_tables, out)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(device)
+    if world > 1:
+        torch.distributed.barrier()
+    t_end = time.time()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+
+    # end to end: the chunk's q / k / v, block table and lengths copied in
+    # from pinned host memory, the call, the output copied back and waited for
+    host = {n: getattr(pb, n).cpu().pin_memory()
+            for n in ("q", "k", "v", "query_start", "ctx_lens", "block_tables")}
+    dev = {n: torch.empty_like(getattr(pb, n)) for n in host}
+    out_h = torch.empty(tuple(out.shape), dtype=out.dtype).pin_memory()
+    e2e_s = []
+    for i in range(args.warmup + args.steps):
+        flush()
+        torch.cuda.synchronize(device)
+        t0 = time.perf_counter()
+        for n in host:
+            dev[n].copy_(host[n], non_blocking=True)
+        step(dev["q"], dev["k"], dev["v"], dev["query_start"], dev["ctx_lens"],
+             dev["block_tables"], out)
+        out_h.copy_(out, non_blocking=True)
+        torch.cuda.synchronize(device)
+        if i >= args.warmup:
+            e2e_s.append(time.perf_counter() - t0)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+    if rank == 0:
+        sampler.stop()
+    assert torch.isfinite(out).all().item(), "non-finite output"
+
+    t_step, t_e2e = max_over_ranks([statistics.mean(step_ms), statistics.mean(e2e_s) * 1e3],
+                                   world, device)
+    tflops = world * flops / (t_step * 1e-3) / 1e12
+    peak, peak_kind = measured_tensor_peak()
+    result = {
+        "metric": PREFILL_METRIC,
+        "value": round(tflops, 2),
+        "unit": PREFILL_UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(t_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) q / k / v and cached context, random block table)",
+        "config": {
+            "workload": f"{w.name}: {w.num_seqs} seq(s), chunk(s) of "
+                        f"{[int(pb.query_start[b + 1] - pb.query_start[b]) for b in range(w.num_seqs)]}"
+                        f" tokens after {[int(x) for x in pb.ctx_lens]} cached, {w.num_heads} q / "
+                        f"{w.num_kv_heads} kv heads, head_dim {w.head_dim}, "
+                        f"{str(w.dtype).replace('torch.', '')}, block {w.block_size}",
+            "accumulate": "f32",
+            "l2": "a 256 MiB read sweep evicts L2 before every timed step",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "roofline": {
+            "bound": "tensor",
+            "kernel": "pa_prefill_kernel",
+            "achieved": round(flops / (t_step * 1e-3) / 1e12, 2),
+            "peak": peak,
+            "peak_source": f"{peak_kind} bf16_tflops (cuBLAS burst)",
+            "unit": "TFLOP/s",
+            "frac": round(flops / (t_step * 1e-3) / 1e12 / peak, 4),
+            "traffic": None,
+            "algorithmic_flops_per_launch": flops,
+            "launch_ms": round(t_step, 4),
+        },
+        "e2e": {"value": round(world * flops / (t_e2e * 1e-3) / 1e12, 2), "unit": PREFILL_UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+    }
+    if rank == 0:
+        result["clocks"] = sampler.summary(t_start, t_end)
+        if world == 1 and not args.no_cpu_baseline:
+            result["cpu_baseline"] = cpu_baseline_prefill(pb, args.cpu_rows, args.cpu_seconds)
+    return result
+
+
+def _prefill_row_work(pb, rows):
+    """Visible keys summed over the given flat (token * Hq + head) rows."""
+    w = pb.workload
+    qs = [int(x) for x in pb.query_start]
+    work = 0
+    for r in rows:
+        t = r // w.num_heads
+        b = max(i for i in range(w.num_seqs) if qs[i] <= t)
+        work += int(pb.ctx_lens[b]) + (t - qs[b]) + 1
+    return work
+
+
+def cpu_baseline_prefill(pb, nrows, seconds, threads=None):
+    """The prefill oracle timed on the host cores on a spread sample of rows,
+    repeated for ``seconds``, scaled to the step's full (row x visible key)
+    work."""
+    import oracle
+    pc = pb.to("cpu")
+    w = pc.workload
+    T = pc.q.shape[0]
+    total_rows = T * w.num_heads
+    rows = [int(i * (total_rows - 1) / max(1, nrows - 1)) for i in range(nrows)]
+    total = sum(int(pc.ctx_lens[b]) * (int(pc.query_start[b + 1]) - int(pc.query_start[b]))
+                for b in range(w.num_seqs))
+    total += sum(n * (n + 1) // 2 for n in
+                 (int(pc.query_start[b + 1]) - int(pc.query_start[b]) for b in range(w.num_seqs)))
+    total *= w.num_heads
+    work = _prefill_row_work(pc, rows)
+    spent, reps = 0.0, 0
+    while reps == 0 or spent < seconds:
+        t0 = time.perf_counter()
+        oracle.prefill(pc.q, pc.k, pc.v, pc.k_cache, pc.v_cache, pc.block_tables,
+                       pc.query_start, pc.ctx_lens, pc.scale, rows=rows)
+        spent += time.perf_counter() - t0
+        reps += 1
+    step_s = spent / reps * total / work
+    flops = prefill_flops(pc)
+    return {"value": round(flops / step_s / 1e12, 6), "unit": PREFILL_UNIT,
+            "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"{len(rows)} of {total_rows} query-head rows spread over the chunk, "
+                      f"{reps} repetitions ({spent:.1f} s), scaled by visible-key work to the "
+                      f"full step ({step_s * 1e3:.0f} ms)"}
+
+
+# ---------------------------------------------------------------------------
 # the oracle on the host cores (cpu_baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
 def _oracle_rows(batch_cpu, rows):
@@ -387,6 +575,26 @@ def run_reference(args, rank, world):
         return None
     import dataclasses
     import oracle
+    if args.workload in wl.PREFILL_WORKLOADS:
+        pb = wl.make_prefill(wl.PREFILL_WORKLOADS[args.workload])
+        base = cpu_baseline_prefill(pb, 8, 0.0)
+        times = []
+        for i in range(args.warmup + args.steps):
+            b = cpu_baseline_prefill(pb, 8, 0.0)
+            if i >= args.warmup:
+                times.append(b["value"])
+        v = round(statistics.mean(times), 6)
+        return {
+            "impl": "reference",
+            "metric": PREFILL_METRIC, "value": v, "unit": PREFILL_UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload},
+            "cpu_baseline": {"value": v, "unit": PREFILL_UNIT, "cores": base["cores"],
+                             "kind": "oracle", "sample": base["sample"]},
+            "e2e": {"value": v, "unit": PREFILL_UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+        }
     w = wl.WORKLOADS[args.workload]
     P = args.partition_size or w.partition_sizes[0]
     bc = wl.make(w, device="cpu")
@@ -423,7 +631,8 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default="long_100k", choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--workload", default="long_100k",
+                    choices=sorted(wl.WORKLOADS) + sorted(wl.PREFILL_WORKLOADS))
     ap.add_argument("--partition-size", type=int, default=0)
     ap.add_argument("--path", choices=("decode", "v1", "v2"), default="decode",
                     help="pa_decode (threshold dispatch), or force V1 / V2")
@@ -466,7 +675,10 @@ def main():
         torch.distributed.barrier()
         if rank != 0:
             build.build()
-    res = run_ours(args, rank, world, device)
+    if args.workload in wl.PREFILL_WORKLOADS:
+        res = run_prefill(args, rank, world, device)
+    else:
+        res = run_ours(args, rank, world, device)
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:

@@ -57,15 +57,18 @@ constexpr long long kWaitBudget = 4000000000LL;    // cycles (about 2 s)
 constexpr long long kSelftestBudget = 20000000LL;  // cycles (about 10 ms)
 constexpr int kSmemLimit = 227 * 1024;
 
-// Shared memory: q (head_dim / 64 slices of [128 rows][128 B]), P (two
-// 64-key halves of [128 rows][128 B]), the ring, the control block.  Every
-// operand tile starts on a 1024-byte boundary (128-byte swizzle atoms).
+// Shared memory: q (head_dim / 64 slices of [128 rows][128 B]), two P
+// buffers (each two 64-key halves of [128 rows][128 B]; tile t uses buffer
+// t % 2, so the softmax of the next tile never waits for this tile's P.V),
+// the ring, the control block.  Every operand tile starts on a 1024-byte
+// boundary (128-byte swizzle atoms).
 template <int D>
 struct Layout {
   static constexpr int kSlices = D / 64;
   static constexpr int kVTokens = kStage / (D * 2);  // keys per value stage
   static constexpr int kPOff = kSlices * kStage;
-  static constexpr int kRingOff = kPOff + 2 * kStage;
+  static constexpr int kPBytes = 2 * kStage;  // one P buffer
+  static constexpr int kRingOff = kPOff + 2 * kPBytes;
   static constexpr int kStages =
       std::min(kMaxStages, (kSmemLimit - kRingOff - 2048) / kStage);
   static constexpr int kCtrlOff = kRingOff + kStages * kStage;
@@ -81,7 +84,7 @@ struct Ctrl {
   uint64_t qempty;             // q tile no longer read
   uint64_t s_full[2];          // a tile's logits ready (per buffer)
   uint64_t p_ready;            // P written (128 softmax threads arrive)
-  uint64_t o_done;             // a tile's P.V completed
+  uint64_t o_done[2];          // P.V of a tile completed (per P buffer)
   uint64_t tail;               // producer-private: a tail value stage landed
   uint64_t drain;              // abort path: all issued MMAs finished
   uint64_t never;              // self-test: nothing ever arrives here
@@ -130,7 +133,26 @@ __device__ __forceinline__ int tile_keys(const Unit& u, int j) {
   return j < u.nctx ? min(kTile, u.C - j * kTile) : min(kTile, u.n - (j - u.nctx) * kTile);
 }
 
-__device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// 2^x by the hardware's approximate exponential (ex2.approx, relative error
+// well below the 16-bit rounding p goes through next; inputs here are <= 8)
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Round two p values to the 16-bit element type, packed low / high for P,
+// and add the rounded values to the running sum.
+__device__ __forceinline__ uint32_t pack2_16(float p0, float p1, float& sum, __nv_bfloat16*) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+  sum += __low2float(h) + __high2float(h);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t pack2_16(float p0, float p1, float& sum, __half*) {
+  const __half2 h = __floats2half2_rn(p0, p1);
+  sum += __low2float(h) + __high2float(h);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
 
 }  // namespace pf
 
@@ -174,7 +196,8 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     sm100::mbar_init(&c.s_full[0], 1);
     sm100::mbar_init(&c.s_full[1], 1);
     sm100::mbar_init(&c.p_ready, 128);
-    sm100::mbar_init(&c.o_done, 1);
+    sm100::mbar_init(&c.o_done[0], 1);
+    sm100::mbar_init(&c.o_done[1], 1);
     sm100::mbar_init(&c.tail, 1);
     sm100::mbar_init(&c.drain, 1);
     sm100::mbar_init(&c.never, 1);
@@ -374,6 +397,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     };
     auto pv = [&](const Unit& u, int j) -> bool {
       if (!__all_sync(kAll, sm100::mbar_wait(&c.p_ready, pn & 1, budget, abort_flag))) return false;
+      const uint32_t pb = pn & 1;  // P buffer of this tile
       ++pn;
       sm100::tc_fence_after();
       const int nk = tile_keys(u, j);
@@ -388,8 +412,9 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         const int toks = min(kVT, nk - v * kVT);
         for (int r = 0; r < toks; r += 16) {
           const int key = v * kVT + r;
-          const uint64_t ad = sm100::smem_desc(p_base + (key / 64) * kStage + ((key % 64) / 16) * 32,
-                                               16, 1024, sm100::kSw128);
+          const uint64_t ad =
+              sm100::smem_desc(p_base + pb * Lay::kPBytes + (key / 64) * kStage + ((key % 64) / 16) * 32,
+                               16, 1024, sm100::kSw128);
           const uint64_t bd = sm100::smem_desc(st + (r / vbs) * vbs * D * 2 + (r % vbs) * 128,
                                                vbs * 128, 1024, sm100::kSw128);
           sm100::mma_f16_elect(tmem + kOCol, ad, bd, id_pv, (j | v | r) != 0);
@@ -397,7 +422,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         sm100::mma_commit_elect(&c.empty[slot]);
         ++g;
       }
-      sm100::mma_commit_elect(&c.o_done);
+      sm100::mma_commit_elect(&c.o_done[pb]);
       return true;
     };
 
@@ -473,12 +498,6 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             if (c0 + e < vis) mx = fmaxf(mx, sv[e]);
         }
         const float mt = mx * sl2;
-        // P.V of the previous tile must be done: it reads P, and O is rescaled
-        if (j > 0) {
-          if (!sm100::mbar_wait(&c.o_done, (gt - 1) & 1, budget, abort_flag)) c.abort = 1;
-          sm100::tc_fence_after();
-          __syncwarp();
-        }
         const float m_new = fmaxf(m_ref, mt);
         const bool move = m_new > m_ref + kRescaleLog2;
         float corr = 1.f;
@@ -487,7 +506,13 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
           lsum *= corr;
           m_ref = m_new;
         }
-        if (j > 0 && __any_sync(0xffffffffu, move)) {
+        const bool rescale = j > 0 && __any_sync(0xffffffffu, move);
+        if (rescale) {
+          // O must be complete up to the previous tile before it is rescaled
+          if (!sm100::mbar_wait(&c.o_done[(gt - 1) & 1], ((gt - 1) >> 1) & 1, budget, abort_flag))
+            c.abort = 1;
+          sm100::tc_fence_after();
+          __syncwarp();
           // the warp's rows that moved their reference max rescale their O row
 #pragma unroll 1
           for (int c0 = 0; c0 < D; c0 += 16) {
@@ -499,30 +524,35 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             sm100::tmem_st16(tmem + lane_base + kOCol + c0, ov);
           }
           sm100::tmem_wait_st();
+        } else if (gt >= 2) {
+          // this tile's P buffer was last read by the P.V two tiles back
+          if (!sm100::mbar_wait(&c.o_done[gt & 1], ((gt - 2) >> 1) & 1, budget, abort_flag))
+            c.abort = 1;
+          __syncwarp();
         }
         // p = 2^(s * scale * log2(e) - m_ref) for the visible keys, rounded to
         // 16 bits into P (row r, 128-byte swizzled rows of two 64-key halves)
+        uint8_t* pbuf = ps + (gt & 1) * Lay::kPBytes;
+        const float neg_m = -m_ref;
 #pragma unroll 1
-        for (int c0 = 0; c0 < kTile; c0 += 16) {
-          float sv[16];
-          sm100::tmem_ld16(sbuf + c0, sv);
+        for (int c0 = 0; c0 < kTile; c0 += 32) {
+          float sv[32];
+          sm100::tmem_ld16(sbuf + c0, *reinterpret_cast<float(*)[16]>(&sv[0]));
+          sm100::tmem_ld16(sbuf + c0 + 16, *reinterpret_cast<float(*)[16]>(&sv[16]));
           sm100::tmem_wait_ld();
-          uint32_t w[8];
+          uint32_t w[16];
 #pragma unroll
-          for (int e = 0; e < 16; e += 2) {
-            const float p0 = c0 + e < vis ? exp2f(sv[e] * sl2 - m_ref) : 0.f;
-            const float p1 = c0 + e + 1 < vis ? exp2f(sv[e + 1] * sl2 - m_ref) : 0.f;
-            const T h0 = round16(p0, static_cast<T*>(nullptr));
-            const T h1 = round16(p1, static_cast<T*>(nullptr));
-            lsum += to_float(h0) + to_float(h1);
-            w[e / 2] = static_cast<uint32_t>(bits16(h0)) | (static_cast<uint32_t>(bits16(h1)) << 16);
+          for (int e = 0; e < 32; e += 2) {
+            const float p0 = c0 + e < vis ? ex2_approx(fmaf(sv[e], sl2, neg_m)) : 0.f;
+            const float p1 = c0 + e + 1 < vis ? ex2_approx(fmaf(sv[e + 1], sl2, neg_m)) : 0.f;
+            w[e / 2] = pack2_16(p0, p1, lsum, static_cast<T*>(nullptr));
           }
 #pragma unroll
-          for (int half8 = 0; half8 < 2; ++half8) {
-            const int key = c0 + half8 * 8;  // 8 keys = one 16-byte piece
+          for (int q8 = 0; q8 < 4; ++q8) {
+            const int key = c0 + q8 * 8;  // 8 keys = one 16-byte piece
             const int piece = ((key % 64) / 8) ^ (r & 7);
-            *reinterpret_cast<uint4*>(ps + (key / 64) * kStage + r * 128 + piece * 16) =
-                make_uint4(w[half8 * 4 + 0], w[half8 * 4 + 1], w[half8 * 4 + 2], w[half8 * 4 + 3]);
+            *reinterpret_cast<uint4*>(pbuf + (key / 64) * kStage + r * 128 + piece * 16) =
+                make_uint4(w[q8 * 4 + 0], w[q8 * 4 + 1], w[q8 * 4 + 2], w[q8 * 4 + 3]);
           }
         }
         sm100::fence_proxy_async_smem();
@@ -530,7 +560,8 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         sm100::mbar_arrive(&c.p_ready);
       }
       // ---- epilogue of the unit: O / lsum into out ---------------------------------
-      if (!sm100::mbar_wait(&c.o_done, (gt - 1) & 1, budget, abort_flag)) c.abort = 1;
+      if (!sm100::mbar_wait(&c.o_done[(gt - 1) & 1], ((gt - 1) >> 1) & 1, budget, abort_flag))
+        c.abort = 1;
       sm100::tc_fence_after();
       __syncwarp();
       const bool poison = bad || *abort_flag != 0;
