@@ -27,9 +27,10 @@
 //         weights perturbed by at most one rounding each;
 //   P.V   O[q, d] += sum_k P[q, k] V[k, d]    M = 128, N = head_dim, K = keys,
 //         accumulated in tensor memory (V is the MN-major operand).
-// Roles (192 threads): warp 4 streams q, keys and values with TMA into a
-// ring of 16 KB stages; warp 5 issues the MMAs; warps 0-3 run the softmax
-// and the epilogue.  Every wait is bounded; a wait that gives up makes the
+// Roles (224 threads): warps 4 and 6 stream q, keys and values with TMA into
+// a ring of 16 KB stages (alternate stages each: a context key stage takes
+// one copy per cache block, so two warps issue them twice as fast); warp 5
+// issues the MMAs; warps 0-3 run the softmax and the epilogue.  Every wait is bounded; a wait that gives up makes the
 // CTA's outputs NaN.
 #pragma once
 
@@ -45,7 +46,7 @@ namespace pa {
 
 namespace pf {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
 constexpr int kTile = 128;          // queries per unit and keys per key tile
 constexpr int kStage = 16384;       // one ring stage
 constexpr int kMaxStages = 12;      // barrier slots in the control block
@@ -85,7 +86,7 @@ struct Ctrl {
   uint64_t s_full[2];          // a tile's logits ready (per buffer)
   uint64_t p_ready;            // P written (128 softmax threads arrive)
   uint64_t o_done[2];          // P.V of a tile completed (per P buffer)
-  uint64_t tail;               // producer-private: a tail value stage landed
+  uint64_t tail[2];            // producer-private: a tail value stage landed
   uint64_t drain;              // abort path: all issued MMAs finished
   uint64_t never;              // self-test: nothing ever arrives here
   uint32_t tmem;
@@ -198,7 +199,8 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     sm100::mbar_init(&c.p_ready, 128);
     sm100::mbar_init(&c.o_done[0], 1);
     sm100::mbar_init(&c.o_done[1], 1);
-    sm100::mbar_init(&c.tail, 1);
+    sm100::mbar_init(&c.tail[0], 1);
+    sm100::mbar_init(&c.tail[1], 1);
     sm100::mbar_init(&c.drain, 1);
     sm100::mbar_init(&c.never, 1);
     c.abort = 0;
@@ -221,11 +223,15 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
   const uint32_t tmem = c.tmem;
   volatile int* abort_flag = &c.abort;
 
-  if (warp == 4) {
-    // ========================= producer ===========================================
+  if (warp == 4 || warp == 6) {
+    // ========================= producers ==========================================
     // Per unit: q, then keys of tile 0, then (keys of tile j, values of tile
     // j - 1) for j >= 1, then the last tile's values -- the order the MMA
-    // warp consumes the ring in.
+    // warp consumes the ring in.  Both producer warps walk this sequence;
+    // producer `pid` fills the stages g with g % 2 == pid (and loads q if
+    // pid == 0).
+    const uint32_t pid = warp == 6 ? 1u : 0u;
+    uint64_t* my_tail = &c.tail[pid];
     uint64_t keep;  // q, the chunk's keys / values and the context: read by several units
     asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(keep));
     uint32_t g = 0, un = 0, tn = 0;
@@ -249,7 +255,8 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       const int nk = tile_keys(u, j);
       const bool ctx = j < u.nctx;
       const int nblk = (nk + BS - 1) / BS;
-      for (int sl = 0; sl < kSl; ++sl) {
+      for (int sl = 0; sl < kSl; ++sl, ++g) {
+        if ((g & 1u) != pid) continue;
         const int slot = g % NST;
         if (!__all_sync(0xffffffffu, sm100::mbar_wait(&c.empty[slot], ((g / NST) & 1) ^ 1, budget,
                                                         abort_flag)))
@@ -268,7 +275,6 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
           }
         }
         __syncwarp();
-        ++g;
       }
       return true;
     };
@@ -283,7 +289,8 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       const bool ctx = j < u.nctx;
       const int vbs = ctx ? BS : 16;  // rows per copy (cache block / 16 chunk rows)
       const int nv = (nk + kVT - 1) / kVT;
-      for (int v = 0; v < nv; ++v) {
+      for (int v = 0; v < nv; ++v, ++g) {
+        if ((g & 1u) != pid) continue;
         const int slot = g % NST;
         if (!__all_sync(0xffffffffu, sm100::mbar_wait(&c.empty[slot], ((g / NST) & 1) ^ 1, budget,
                                                         abort_flag)))
@@ -291,7 +298,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         const int toks = min(kVT, nk - v * kVT);
         const int ncp = (toks + vbs - 1) / vbs;  // copies in this stage
         const bool tail = v == nv - 1 && (nk % 16) != 0;
-        uint64_t* land = tail ? &c.tail : &c.full[slot];
+        uint64_t* land = tail ? my_tail : &c.full[slot];
         uint8_t* st = ring + slot * kStage;
         if (lane == 0) sm100::mbar_arrive_expect_tx(land, ncp * vbs * D * 2);
         __syncwarp();
@@ -305,10 +312,9 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
                              u.s0 + (j - u.nctx) * kTile + v * kVT + lane * 16, 0, keep);
         }
         __syncwarp();
-        ++g;
         if (tail) {
           tail_pending = slot;
-          if (!__all_sync(0xffffffffu, sm100::mbar_wait(&c.tail, tn & 1, budget, abort_flag)))
+          if (!__all_sync(0xffffffffu, sm100::mbar_wait(my_tail, tn & 1, budget, abort_flag)))
             return false;
           ++tn;
           tail_pending = -1;
@@ -334,14 +340,16 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       if (!u.run) continue;
       // q tile (rows past the chunk belong to other sequences or lie past T,
       // where TMA fills zeros; their rows are never stored)
-      ok = __all_sync(0xffffffffu, sm100::mbar_wait(&c.qempty, (un & 1) ^ 1, budget, abort_flag));
-      if (!ok) break;
-      if (lane == 0) sm100::mbar_arrive_expect_tx(&c.qfull, kSl * kStage);
-      __syncwarp();
-      if (lane < kSl)
-        sm100::tma_load_4d(qs + lane * kStage, &qmap, &c.qfull, 0, u.h, u.s0 + u.qt * kTile, lane,
-                           keep);
-      ++un;
+      if (pid == 0) {
+        ok = __all_sync(0xffffffffu, sm100::mbar_wait(&c.qempty, (un & 1) ^ 1, budget, abort_flag));
+        if (!ok) break;
+        if (lane == 0) sm100::mbar_arrive_expect_tx(&c.qfull, kSl * kStage);
+        __syncwarp();
+        if (lane < kSl)
+          sm100::tma_load_4d(qs + lane * kStage, &qmap, &c.qfull, 0, u.h, u.s0 + u.qt * kTile, lane,
+                             keep);
+        ++un;
+      }
       int32_t yprev = 0;
       for (int j = 0; j < u.ntiles && ok; ++j) {
         const int32_t y = j < u.nctx ? ctx_rows(u, j) : 0;
@@ -355,9 +363,9 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       if (lane == 0) c.abort = 1;
       // copies already issued must land before the CTA may exit
       for (uint32_t gg = g > NST ? g - NST : 0; gg < g; ++gg)
-        if (static_cast<int>(gg % NST) != tail_pending)
+        if ((gg & 1u) == pid && static_cast<int>(gg % NST) != tail_pending)
           sm100::mbar_wait(&c.full[gg % NST], (gg / NST) & 1, budget, nullptr);
-      if (tail_pending >= 0) sm100::mbar_wait(&c.tail, tn & 1, budget, nullptr);
+      if (tail_pending >= 0) sm100::mbar_wait(my_tail, tn & 1, budget, nullptr);
       if (un > 0) sm100::mbar_wait(&c.qfull, (un - 1) & 1, budget, nullptr);
     }
   } else if (warp == 5) {
@@ -450,7 +458,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       sm100::mbar_wait(&c.drain, 0, budget, nullptr);
     }
     __syncwarp();
-  } else {
+  } else if (warp < 4) {
     // ========================= softmax + epilogue (warps 0-3) =====================
     // Thread r owns query row r of the unit (tensor-memory lane r).  Every
     // softmax thread runs the same iterations whatever happens; a failed
