@@ -48,22 +48,37 @@ FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
 
 # DRAM bytes (read + write) per launch of the dominant kernel, from one ncu
-# capture, keyed by a hash of the kernel sources it was taken on.  A source
-# change makes the figure stale, and the bench then reports null.
+# capture, keyed by a hash of the sources that kernel is built from.  A change
+# to any of them makes the figure stale, and the bench then reports null.
+KERNEL_SOURCES = {
+    "pa_tc_kernel": ("pa_tc.cuh", "pa_tc_host.cu", "pa_tc_bf16.cu", "pa_sm100.cuh",
+                     "pa_device.cuh", "pa_internal.h"),
+    "pa_generic_kernel": ("pa_generic.cuh", "pa_generic_bf16.cu", "pa_generic_f32.cu",
+                          "pa_device.cuh", "pa_internal.h"),
+    "pa_prefill_kernel": ("pa_prefill.cuh", "pa_prefill_host.cu", "pa_prefill_bf16.cu",
+                          "pa_sm100.cuh", "pa_device.cuh", "pa_internal.h"),
+}
 NCU_TRAFFIC = {
-    # (kernel source hash, workload, partition size): bytes per launch
-    ("a3a31c0ea957614b", "long_100k", 512): 409_742_592 + 3_251_456,
-    ("a3a31c0ea957614b", "gqa_8k", 512): 33_667_072 + 0,
+    # (kernel, source hash, workload, partition size, path): bytes per launch
+    ("pa_tc_kernel", "bfe3bf90a465831c", "long_100k", 512, "v2"): 409_722_880 + 3_057_664,
+    ("pa_prefill_kernel", "8a1964c324e4df01", "prefill_32k", 0, "prefill"):
+        1_354_604_000 + 193_199_872,
 }
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "paged_attention_decode_v2_gb300", "csrc", "*"))):
-        with open(f, "rb") as fh:
-            h.update(os.path.basename(f).encode())
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "paged_attention_decode_v2_gb300", "csrc", name), "rb") as fh:
+            h.update(name.encode())
             h.update(fh.read())
     return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str, P: int, path: str):
+    if kernel not in KERNEL_SOURCES:
+        return None
+    return NCU_TRAFFIC.get((kernel, kernel_source_hash(kernel), workload, P, path))
 
 
 def max_over_ranks(values, world, device=None):
@@ -293,7 +308,7 @@ def run_ours(args, rank, world, device):
 
     peak, peak_kind = measured_hbm_peak()
     achieved = alg_bytes / (t_dom * 1e-3) / 1e9
-    traffic = NCU_TRAFFIC.get((kernel_source_hash(), args.workload, P))
+    traffic = ncu_traffic(kname.split(" ")[0], args.workload, P, "v2" if path == 2 else "v1")
     result = {
         "metric": METRIC,
         "value": round(t_step * 1e3, 3),
@@ -476,7 +491,7 @@ def run_prefill(args, rank, world, device):
             "peak_source": f"{peak_kind} bf16_tflops (cuBLAS burst)",
             "unit": "TFLOP/s",
             "frac": round(flops / (t_step * 1e-3) / 1e12 / peak, 4),
-            "traffic": None,
+            "traffic": ncu_traffic("pa_prefill_kernel", w.name, 0, "prefill"),
             "algorithmic_flops_per_launch": flops,
             "launch_ms": round(t_step, 4),
         },
