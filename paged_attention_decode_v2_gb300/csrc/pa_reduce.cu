@@ -13,12 +13,17 @@
 // workspace needs no initialisation (the "shifted output" concern of the
 // paragraph on test_device_scan_warpspeed_shifted_output, same page).
 //
-// Grid: (head_dim / 32, num_heads, num_seqs); each CTA produces 32 output
-// elements of one row.  16 groups of 8 threads each fold a strided subset of
-// the partitions into a running (max, weight, weighted sum) -- the same
-// log-sum-exp identity applied incrementally -- and the groups are merged
-// at the end.  Every load of a group is independent of the running values,
-// so the partials are read with many loads in flight in one round.
+// Grid: (head_dim / S, num_heads, num_seqs); each CTA of 128 threads
+// produces S output elements of one row (S = 32, 64, 128 or 256, chosen per
+// launch so that large batches do not need many waves of tiny CTAs).  The
+// threads form 512 / S groups of S / 4 threads (one float4 column each);
+// group g folds partitions g, g + groups, ... into a running (max, weight,
+// weighted sum) -- the same log-sum-exp identity applied incrementally --
+// and the groups are merged at the end.  A thread loads a batch of its
+// partitions at once (statistics and partial output, all independent of the
+// running values) before it folds them, so a row is read in
+// ceil(n / (groups * batch)) rounds of memory latency (batches of 4, with
+// at most 64 registers a thread: eight CTAs resident per SM).
 #include "pa_device.cuh"
 
 namespace pa {
@@ -26,21 +31,44 @@ namespace pa {
 namespace {
 
 constexpr int kNT = 128;
-constexpr int kSlice = 32;               // output elements per CTA
-constexpr int kCols = kSlice / 4;        // float4 columns
-constexpr int kGroups = kNT / kCols;     // partition groups
+
+// Partitions a thread has in flight, and the CTAs per SM the register
+// budget is set for.  Few registers matter more than many loads in flight:
+// reduce CTAs that fit beside pass 1's CTAs on an SM are resident (waiting
+// on the grid dependency) before pass 1 ends.  Measured on GB300 over
+// batches of 4 / 8 / 16 loads with 4-8 CTAs per SM: 4 loads and at most 64
+// registers was the fastest on every workload.
+constexpr int kBatch = 4;
+constexpr int kMinBlocks = 8;
+
+__device__ __forceinline__ void store_out4(void* out, int64_t i, int32_t dtype, float4 v) {
+  if (dtype == PA_F32) {
+    *reinterpret_cast<float4*>(static_cast<float*>(out) + i) = v;
+  } else if (dtype == PA_BF16) {
+    __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + i) =
+        make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
+  } else {
+    __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + i) =
+        make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
+  }
+}
 
 }  // namespace
 
-template <int D>
-__global__ void __launch_bounds__(kNT) pa_reduce_kernel(const KernelArgs a) {
+template <int D, int S>
+__global__ void __launch_bounds__(kNT, kMinBlocks) pa_reduce_kernel(const KernelArgs a) {
+  constexpr int kCols = S / 4;           // float4 columns of the slice
+  constexpr int kGroups = kNT / kCols;   // partition groups
+  static_assert(kGroups >= 1 && kCols * kGroups == kNT, "slice width");
   __shared__ float4 acc_s[kGroups][kCols];
   __shared__ float m_s[kGroups], w_s[kGroups];
   __shared__ int nan_s[kGroups];
   const int tid = threadIdx.x;
   const int x = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int64_t row = static_cast<int64_t>(b) * a.num_heads + h;
-  const int d0 = x * kSlice;
+  const int d0 = x * S;
 
   // seq_lens is an input, not a pass-1 result: read it before waiting.
   const int32_t L = a.seq_lens[b];
@@ -50,42 +78,63 @@ __global__ void __launch_bounds__(kNT) pa_reduce_kernel(const KernelArgs a) {
 
   if (!seq_len_ok(a, L) || L == 0) {
     const float v = L == 0 ? 0.f : qnan();
-    if (tid < kSlice) store_out(a.out, row * D + d0 + tid, a.out_dtype, v);
+    for (int c = tid; c < kCols; c += kNT)
+      store_out4(a.out, row * D + d0 + 4 * c, a.out_dtype, make_float4(v, v, v, v));
     return;
   }
   const int n = (L + a.partition_size - 1) / a.partition_size;
   const float* __restrict__ ml = a.max_logits + row * a.num_partitions;
   const float* __restrict__ es = a.exp_sums + row * a.num_partitions;
-  const float* __restrict__ to = a.tmp_out + row * a.num_partitions * D + d0;
+  const float4* __restrict__ to =
+      reinterpret_cast<const float4*>(a.tmp_out + row * a.num_partitions * D + d0);
 
-  // Each group folds its partitions p = grp, grp + kGroups, ... into a
-  // running (max, weight, weighted sum); all loads of a group are independent,
-  // so a row of up to kGroups * 8 partitions is read in about one latency.
   const int col = tid % kCols, grp = tid / kCols;
   float m = -INFINITY, w = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   int nan_seen = 0;
-#pragma unroll 8
-  for (int p = grp; p < n; p += kGroups) {
-    const float mp = __ldg(ml + p);
-    const float sp = __ldg(es + p);
-    const float4 o = __ldg(reinterpret_cast<const float4*>(to + static_cast<int64_t>(p) * D) + col);
-    nan_seen |= isnan(mp);
-    if (mp > m) {
-      const float f = expf(m - mp);  // 0 when m is -inf
+  for (int base = grp; base < n; base += kGroups * kBatch) {
+    float mp[kBatch], sp[kBatch];
+    float4 o[kBatch];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const int p = base + i * kGroups;
+      if (p < n) {
+        mp[i] = __ldg(ml + p);
+        sp[i] = __ldg(es + p);
+        o[i] = __ldg(to + static_cast<int64_t>(p) * (D / 4) + col);
+      } else {
+        mp[i] = -INFINITY;
+        sp[i] = 0.f;
+        o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    // the batch's max moves the running reference once
+    float mb = m;
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      nan_seen |= isnan(mp[i]);
+      mb = fmaxf(mb, mp[i]);
+    }
+    if (mb > m) {
+      const float f = expf(m - mb);  // 0 when m is -inf
       acc.x *= f;
       acc.y *= f;
       acc.z *= f;
       acc.w *= f;
       w *= f;
-      m = mp;
+      m = mb;
     }
-    const float e = sp * expf(mp - m);
-    acc.x = fmaf(e, o.x, acc.x);
-    acc.y = fmaf(e, o.y, acc.y);
-    acc.z = fmaf(e, o.z, acc.z);
-    acc.w = fmaf(e, o.w, acc.w);
-    w += e;
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      if (base + i * kGroups < n) {
+        const float e = sp[i] * expf(mp[i] - m);
+        acc.x = fmaf(e, o[i].x, acc.x);
+        acc.y = fmaf(e, o[i].y, acc.y);
+        acc.z = fmaf(e, o[i].z, acc.z);
+        acc.w = fmaf(e, o[i].w, acc.w);
+        w += e;
+      }
+    }
   }
   acc_s[grp][col] = acc;
   if (col == 0) {
@@ -94,7 +143,7 @@ __global__ void __launch_bounds__(kNT) pa_reduce_kernel(const KernelArgs a) {
     nan_s[grp] = nan_seen;
   }
   __syncthreads();
-  if (tid < kSlice) {
+  for (int c = tid; c < kCols; c += kNT) {
     float M = -INFINITY;
     int poison = 0;
 #pragma unroll
@@ -102,21 +151,28 @@ __global__ void __launch_bounds__(kNT) pa_reduce_kernel(const KernelArgs a) {
       M = fmaxf(M, m_s[g]);
       poison |= nan_s[g];
     }
-    float total = 0.f, s = 0.f;
+    float total = 0.f;
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int g = 0; g < kGroups; ++g) {
       const float f = m_s[g] == -INFINITY ? 0.f : expf(m_s[g] - M);
+      const float4 v = acc_s[g][c];
       total = fmaf(w_s[g], f, total);
-      s = fmaf(reinterpret_cast<const float*>(&acc_s[g][tid / 4])[tid % 4], f, s);
+      s.x = fmaf(v.x, f, s.x);
+      s.y = fmaf(v.y, f, s.y);
+      s.z = fmaf(v.z, f, s.z);
+      s.w = fmaf(v.w, f, s.w);
     }
-    store_out(a.out, row * D + d0 + tid, a.out_dtype, poison ? qnan() : s / total);
+    const float4 r = poison ? make_float4(qnan(), qnan(), qnan(), qnan())
+                            : make_float4(s.x / total, s.y / total, s.z / total, s.w / total);
+    store_out4(a.out, row * D + d0 + 4 * c, a.out_dtype, r);
   }
 }
 
-template <int D>
-static cudaError_t launch_reduce_d(const KernelArgs& a, cudaStream_t s, bool pdl) {
+template <int D, int S>
+static cudaError_t launch_reduce_ds(const KernelArgs& a, cudaStream_t s, bool pdl) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(D / kSlice, a.num_heads, a.num_seqs);
+  cfg.gridDim = dim3(D / S, a.num_heads, a.num_seqs);
   cfg.blockDim = dim3(kNT, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
@@ -125,7 +181,37 @@ static cudaError_t launch_reduce_d(const KernelArgs& a, cudaStream_t s, bool pdl
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, pa_reduce_kernel<D>, a);
+  return cudaLaunchKernelEx(&cfg, pa_reduce_kernel<D, S>, a);
+}
+
+// Output elements per CTA: 32 (the most groups per row, for long rows of
+// small batches) unless that would take more than two waves of CTAs, in
+// which case the slice widens (fewer, fuller CTAs) up to the whole row.
+static int slice_width(const KernelArgs& a) {
+  int sms = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      sms <= 0)
+    sms = 148;
+  const int64_t rows = static_cast<int64_t>(a.num_seqs) * a.num_heads;
+  int S = 32;
+  while (S < a.head_dim && rows * (a.head_dim / S) > 2LL * sms * kMinBlocks) S *= 2;
+  return S;
+}
+
+template <int D>
+static cudaError_t launch_reduce_d(const KernelArgs& a, cudaStream_t s, bool pdl) {
+  switch (slice_width(a)) {
+    case 32: return launch_reduce_ds<D, 32>(a, s, pdl);
+    case 64: return launch_reduce_ds<D, 64>(a, s, pdl);
+    case 128:
+      if constexpr (D >= 128) return launch_reduce_ds<D, 128>(a, s, pdl);
+      break;
+    case 256:
+      if constexpr (D >= 256) return launch_reduce_ds<D, 256>(a, s, pdl);
+      break;
+  }
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_reduce(const KernelArgs& a, cudaStream_t s, bool pdl) {

@@ -68,6 +68,28 @@ def test_small_parity(name, w, _, parts, path, portable):
         assert_close(got, ref, tol, f"{name} {path} P={P} portable={portable}")
 
 
+# Batch sizes that make the reduce take each of its slice widths (32, 64,
+# 128 and 256 output elements per CTA for head_dim 256 on a 152-SM GPU; the
+# width widens as the batch's rows grow) with 16-token partitions, so that
+# rows have up to ~40 partitions and every thread folds several batches.
+REDUCE_SHAPES = [(1, 600), (16, 600), (32, 600), (128, 600)]
+
+
+@pytest.mark.parametrize("num_seqs,max_len", REDUCE_SHAPES,
+                         ids=[f"B{b}" for b, _ in REDUCE_SHAPES])
+def test_reduce_slice_widths(num_seqs, max_len):
+    w = wl.scaled(wl.WORKLOADS["mixed_32"], num_seqs=num_seqs, max_len=max_len)
+    bc = wl.make(w, poison=True)
+    ref = _ref(bc)
+    bg = bc.to("cuda")
+    for P in (16, 512):
+        got = run(bg, path="v2", partition_size=P)
+        assert_close(got, ref, TOL[w.dtype], f"B={num_seqs} P={P}")
+        # a bf16 output: the float32 result's bound plus half an ulp of the rounding
+        got16 = run(bg, path="v2", partition_size=P, out_dtype=torch.bfloat16)
+        assert np.all(np.abs(got16 - ref) <= 2e-3 + np.abs(bf16_round(ref)) * 2.0 ** -8)
+
+
 def test_v1_v2_agree():
     bc = wl.make(wl.scaled(wl.WORKLOADS["gqa_8k"], seq_len=5000), poison=True)
     bg = bc.to("cuda")
