@@ -60,7 +60,7 @@ KERNEL_SOURCES = {
 }
 NCU_TRAFFIC = {
     # (kernel, source hash, workload, partition size, path): bytes per launch
-    ("pa_tc_kernel", "bfe3bf90a465831c", "long_100k", 512, "v2"): 409_722_880 + 3_057_664,
+    ("pa_tc_kernel", "f0d1d45f3144f62e", "long_100k", 512, "v2"): 409_735_936 + 2_520_832,
     ("pa_prefill_kernel", "8a1964c324e4df01", "prefill_32k", 0, "prefill"):
         1_354_604_000 + 193_199_872,
 }

@@ -134,7 +134,8 @@ typedef struct pa_params {
  *   tmp_output   float32 [num_seqs, num_heads, NP, head_dim]
  *                o_p = sum exp(l_t - m_p) V_t / s_p
  * Only partitions p < ceil(seq_lens[b] / P) are written or read; the rest
- * may hold anything.
+ * may hold anything.  After pa_decode_v2 (not pa_decode_v2_partitions) a
+ * sequence with a single partition has no partials in the workspace.
  */
 
 /* Bytes of workspace pa_decode_v2 / pa_decode need for these parameters
@@ -159,8 +160,15 @@ PA_API pa_status_t pa_decode_v1(const pa_params_t* params, const void* q, const 
  * exp_sums and tmp_output into the workspace; pass 2 combines a row's
  * partitions with weights exp(m_p - max_p m_p) * s_p and writes `out`.
  * `workspace` must hold pa_workspace_size(params) bytes.
+ * The V1 / V2 choice is also made per sequence inside the pass-1 launch: a
+ * sequence of 1..partition_size tokens has a single partition, so pass 1
+ * writes its normalised result straight into `out` (V1's contract), writes
+ * no partials for it, and pass 2 skips its rows; longer sequences are split
+ * and reduced.  (pa_decode_v2_partitions below always writes the partials.)
  * Source: commit 4eb83a7e "qwen3_6_scripts", paragraph "Implementation
- * (paged_attention_v2_pytorch.py)", Phase 1 and Phase 2.
+ * (paged_attention_v2_pytorch.py)", Phase 1 and Phase 2; the per-sequence
+ * choice follows the V1 / V2 tiers of commit 1a4e1005 "paged_attn.py",
+ * change 1, with the partition size as the per-sequence threshold.
  */
 PA_API pa_status_t pa_decode_v2(const pa_params_t* params, const void* q, const void* k_cache,
                          const void* v_cache, const int32_t* block_tables,
@@ -170,10 +178,13 @@ PA_API pa_status_t pa_decode_v2(const pa_params_t* params, const void* q, const 
 /*
  * The two kernels of pa_decode_v2 as separate calls, for callers that want
  * to schedule or time them apart.  pa_decode_v2_partitions enqueues pass 1
- * (writes the workspace); pa_decode_v2_reduce enqueues pass 2 (reads the
- * workspace, writes `out`) and must follow pass 1 on the same stream with
- * the same arguments.  pa_decode_v2 is exactly the two in sequence, with
- * pass 2 launched as a programmatic dependent of pass 1.
+ * and writes the workspace's partials for every partition of every
+ * sequence (single-partition sequences included); pa_decode_v2_reduce
+ * enqueues pass 2 (reads the workspace, writes every row of `out`) and must
+ * follow pass 1 on the same stream with the same arguments.  Together they
+ * give pa_decode_v2's result; pa_decode_v2 itself launches pass 2 as a
+ * programmatic dependent of pass 1 and finishes single-partition sequences
+ * in pass 1.
  */
 PA_API pa_status_t pa_decode_v2_partitions(const pa_params_t* params, const void* q,
                                            const void* k_cache, const void* v_cache,

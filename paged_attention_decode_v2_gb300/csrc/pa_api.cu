@@ -195,6 +195,9 @@ pa_status_t pa_decode_v2(const pa_params_t* p, const void* q, const void* k_cach
   pa_status_t st = prepare_v2(p, q, k_cache, v_cache, block_tables, seq_lens, workspace,
                               workspace_bytes, out, true, true, &a);
   if (st != PA_OK || p->num_seqs == 0) return st;
+  // per-sequence choice inside the one pass-1 launch: sequences that fit one
+  // partition are finished there, the rest are split and reduced
+  a.single_direct = 1;
   if (launch_pass(p, a, true, stream) != cudaSuccess) return PA_ERR_CUDA;
   if (launch_reduce(a, stream, true) != cudaSuccess) return PA_ERR_CUDA;
   return PA_OK;

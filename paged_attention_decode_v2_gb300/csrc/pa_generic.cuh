@@ -109,6 +109,8 @@ __global__ void __launch_bounds__(256) pa_generic_kernel(const KernelArgs a) {
   const int32_t t_begin = kV2 ? part * a.partition_size : 0;
   if (kV2 && t_begin >= L) return;  // this sequence has no such partition
   const int32_t t_end = kV2 ? min(L, t_begin + a.partition_size) : L;
+  // a sequence that fits one partition is finished here (V1's contract)
+  const bool direct = kV2 && a.single_direct && L <= a.partition_size;
 
   const T* __restrict__ kc = static_cast<const T*>(a.k_cache);
   const T* __restrict__ vc = static_cast<const T*>(a.v_cache);
@@ -281,12 +283,12 @@ __global__ void __launch_bounds__(256) pa_generic_kernel(const KernelArgs a) {
       const float s = sm.s_run[hh];
       const float o = bad ? qnan() : (s > 0.f ? sm.acc[hh][d] / s : 0.f);
       const int64_t row = static_cast<int64_t>(b) * Hq + h0 + hh;
-      if constexpr (kV2)
+      if (kV2 && !direct)
         a.tmp_out[(row * a.num_partitions + part) * D + d] = o;
       else
         store_out(a.out, row * D + d, a.out_dtype, o);
     }
-    if constexpr (kV2) {
+    if (kV2 && !direct) {
       if (tid < nh) {
         const int64_t w = (static_cast<int64_t>(b) * Hq + h0 + tid) * a.num_partitions + part;
         a.max_logits[w] = bad ? qnan() : sm.m_run[tid] * kLn2;

@@ -38,6 +38,9 @@ struct KernelArgs {
   float scale_log2;        // scale * log2(e): logits are kept in base-2 units
   int32_t selftest_stall;  // PA_FLAG_SELFTEST_STALL was given
   int32_t split_x;         // PA_FLAG_SPLIT_X: the pages' V1 cache layout
+  int32_t single_direct;   // V2 pass 1 + reduce in one call: a sequence of at most
+                           // partition_size tokens is finished by pass 1 (written
+                           // straight into out) and the reduce skips its rows
 };
 
 // Everything the prefill kernel needs besides its tensor maps (pa_prefill.cuh).

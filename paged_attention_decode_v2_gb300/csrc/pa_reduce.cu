@@ -72,6 +72,8 @@ __global__ void __launch_bounds__(kNT, kMinBlocks) pa_reduce_kernel(const Kernel
 
   // seq_lens is an input, not a pass-1 result: read it before waiting.
   const int32_t L = a.seq_lens[b];
+  // a sequence of one partition was finished by pass 1 (single_direct)
+  if (a.single_direct && L >= 1 && L <= a.partition_size && seq_len_ok(a, L)) return;
 
   // Wait for pass 1 (a no-op unless launched as a programmatic dependent).
   cudaGridDependencySynchronize();

@@ -117,6 +117,8 @@ struct Item {
   int32_t t0, t1;  // this CTA's token range; empty when t0 >= t1
   bool len_ok;     // 0 <= seq_len <= max_seq_len
   bool any;        // the item's whole range (over all CTAs of a cluster) has tokens
+  bool direct;     // V2 with single_direct: the sequence fits this one partition, so
+                   // the item's result is the final output (written straight to out)
 };
 
 // Coordinates of item k (no global memory read).  With a compact work list
@@ -149,6 +151,7 @@ __device__ __forceinline__ Item item_coords(const KernelArgs& a, const int32_t* 
   it.t1 = it.t0;
   it.len_ok = false;
   it.any = false;
+  it.direct = false;
   return it;
 }
 
@@ -160,6 +163,7 @@ __device__ __forceinline__ void item_range(const KernelArgs& a, Item& it, int32_
   it.len_ok = seq_len_ok(a, L);
   it.t1 = !it.len_ok ? it.t0 : (v2 ? min(L, it.t0 + a.partition_size) : L);
   it.any = it.t0 < it.t1;
+  it.direct = v2 && a.single_direct && it.len_ok && L <= a.partition_size;
   if (cs > 1 && it.any) {
     const int ntiles = (it.t1 - it.t0 + kTile - 1) / kTile;
     const int lo = rank * ntiles / cs, hi = (rank + 1) * ntiles / cs;
@@ -643,7 +647,7 @@ __global__ void __launch_bounds__(tc::kThreads, CPS)
           O = fmaf(recv[(q * 8 + h) * dn + dl], f, O);
         }
         const float o = pz ? qnan() : O / S;
-        if constexpr (kV2) {
+        if (kV2 && !it.direct) {
           sm100::st_f32_policy(a.tmp_out + ((row0 + h) * a.num_partitions + it.part) * D + d, o,
                                keep_l2);
           if (rank == 0 && dl == 0) {
@@ -801,14 +805,14 @@ __global__ void __launch_bounds__(tc::kThreads, CPS)
         for (int h = 0; h < 8; ++h) {
           if (h >= G) break;
           const float o = poison ? qnan() : acc[j][h] / s_run[h];
-          if constexpr (kV2)
+          if (kV2 && !it.direct)
             sm100::st_f32_policy(a.tmp_out + ((row0 + h) * a.num_partitions + it.part) * D + d, o,
                                keep_l2);
           else
             store_out(a.out, (row0 + h) * D + d, a.out_dtype, o);
         }
       }
-      if (kV2 && tid < G) {
+      if (kV2 && !it.direct && tid < G) {
         const int64_t w = (row0 + tid) * a.num_partitions + it.part;
         float m = m_run[0], s = s_run[0];
 #pragma unroll

@@ -7,6 +7,8 @@ last token, block-table entries past the last block are -1), and the V2
 workspace is NaN-filled before each call, so reading anything the method
 does not use shows up as NaN.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -112,24 +114,75 @@ def test_dispatch_boundary():
         assert_close(got, _ref(bc), 2e-3, f"dispatch L={L}")
 
 
+def _partitions_then_reduce(bg, P, portable):
+    """pa_decode_v2_partitions then pa_decode_v2_reduce on a NaN-poisoned
+    workspace: returns (out, workspace)."""
+    params = pa.make_params(bg.q, bg.k_cache, bg.block_tables, max_seq_len=bg.max_seq_len,
+                            scale=bg.scale, partition_size=P, portable=portable,
+                            out_dtype=torch.float32)
+    ws = torch.empty(pa.workspace_size(params), dtype=torch.uint8, device="cuda")
+    ws.view(torch.float32)[64:].fill_(float("nan"))
+    pa.workspace_init(ws)
+    pa.decode_v2_partitions(bg.q, bg.k_cache, bg.v_cache, bg.block_tables, bg.seq_lens, ws,
+                            max_seq_len=bg.max_seq_len, scale=bg.scale, partition_size=P,
+                            out_dtype=torch.float32, portable=portable)
+    out = torch.full(tuple(bg.q.shape), float("nan"), dtype=torch.float32, device="cuda")
+    pa.decode_v2_reduce(params, bg.seq_lens, ws, out)
+    torch.cuda.synchronize()
+    assert pa.read_device_status(ws, clear=False) == pa.PA_OK
+    return out.double().cpu().numpy(), ws
+
+
 def test_workspace_intermediates_match_partitioned_oracle():
-    """Pass 1 alone: max_logits, exp_sums and tmp_output of every partition
-    that exists, against the oracle's Phase 1 in double."""
+    """Pass 1 alone (pa_decode_v2_partitions): max_logits, exp_sums and
+    tmp_output of every partition that exists, against the oracle's Phase 1
+    in double; then pass 2 alone (pa_decode_v2_reduce) against the oracle."""
     bc = wl.make(wl.scaled(wl.WORKLOADS["mixed_32"], num_seqs=4, max_len=2200), poison=True)
     P = 256
     _, ml_r, es_r, to_r = oracle.decode_partitioned(bc.q, bc.k_cache, bc.v_cache,
                                                     bc.block_tables, bc.seq_lens, bc.scale, P,
                                                     max_partitions=-(-bc.max_seq_len // P))
+    ref = _ref(bc)
     for portable in (False, True):
-        _, ws = run(bc.to("cuda"), path="v2", partition_size=P, portable=portable,
-                    return_ws=True)
+        out, ws = _partitions_then_reduce(bc.to("cuda"), P, portable)
         ml, es, to = workspace_views(ws, bc, P)
         live = np.isfinite(ml_r)
-        assert np.array_equal(np.isfinite(ml), live) or np.all(np.isfinite(ml[live]))
+        assert np.all(np.isfinite(ml[live])) and np.all(np.isfinite(to[live]))
         assert max_err(ml[live], ml_r[live]) <= 1e-4 * max(1.0, np.abs(ml_r[live]).max())
         rel = np.abs(es[live] - es_r[live]) / es_r[live]
         assert rel.max() <= 1e-4
         assert max_err(to[live], to_r[live]) <= 2e-3
+        assert_close(out, ref, 2e-3, f"partitions + reduce portable={portable}")
+
+
+def test_single_partition_sequences_finish_in_pass1():
+    """Per-sequence V1 / V2 choice inside pa_decode_v2: a sequence of at most
+    partition_size tokens is written straight into out by pass 1 (its
+    workspace slots stay untouched), longer ones go through the partials and
+    the reduce; every row matches the oracle."""
+    P = 512
+    lens = [1, 100, 512, 513, 2000, 300, 1024, 7]
+    w = dataclasses.replace(wl.scaled(wl.WORKLOADS["mixed_32"], num_seqs=len(lens)),
+                            seq_lens=lambda g: torch.tensor(lens, dtype=torch.int32))
+    bc = wl.make(w, poison=True)
+    ref = _ref(bc)
+    bg = bc.to("cuda")
+    for portable in (False, True):
+        got, ws = run(bg, path="v2", partition_size=P, portable=portable, return_ws=True)
+        assert_close(got, ref, 2e-3, f"per-sequence choice portable={portable}")
+        ml, es, to = workspace_views(ws, bc, P)
+        for b, L in enumerate(lens):
+            if L <= P:   # finished in pass 1: no partials written
+                assert np.all(np.isnan(ml[b])) and np.all(np.isnan(to[b])), (b, L)
+            else:        # split: every partition's partials written
+                n = -(-L // P)
+                assert np.all(np.isfinite(ml[b, :, :n])) and np.all(np.isfinite(to[b, :, :n]))
+        # the two-call form writes the partials of every sequence and agrees
+        got2, ws2 = _partitions_then_reduce(bg, P, portable)
+        assert_close(got2, ref, 2e-3, f"partitions + reduce portable={portable}")
+        assert max_err(got, got2) <= 2e-3
+        ml2, _, _ = workspace_views(ws2, bc, P)
+        assert all(np.all(np.isfinite(ml2[b, :, :-(-L // P)])) for b, L in enumerate(lens))
 
 
 def test_block_permutation_is_bit_identical():
