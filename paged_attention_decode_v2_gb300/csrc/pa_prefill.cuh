@@ -18,7 +18,7 @@
 //   QK^T  S[q, k] = sum_d Q[q, d] K[k, d]     M = 128 queries, N = 128 keys,
 //         into one of two tensor-memory buffers (the next tile's QK^T runs
 //         while the softmax warps work on this one);
-//   softmax (one thread per query row): tile max over the visible keys, the
+//   softmax (two threads per query row): tile max over the visible keys, the
 //         running reference max m moves (and the running sum and the output
 //         are rescaled by corr = 2^(m_old - m_new)) only when the tile max
 //         exceeds it by more than 2^8, so p = 2^(s - m) <= 256; p is rounded
@@ -27,10 +27,14 @@
 //         weights perturbed by at most one rounding each;
 //   P.V   O[q, d] += sum_k P[q, k] V[k, d]    M = 128, N = head_dim, K = keys,
 //         accumulated in tensor memory (V is the MN-major operand).
-// Roles (224 threads): warps 4 and 6 stream q, keys and values with TMA into
-// a ring of 16 KB stages (alternate stages each: a context key stage takes
-// one copy per cache block, so two warps issue them twice as fast); warp 5
-// issues the MMAs; warps 0-3 run the softmax and the epilogue.  Every wait is bounded; a wait that gives up makes the
+// Roles (352 threads): warps 8 and 10 stream q, keys and values with TMA
+// into a ring of 16 KB stages (alternate stages each: a context key stage
+// takes one copy per cache block, so two warps issue them twice as fast);
+// warp 9 issues the MMAs; warps 0-7 run the softmax and the epilogue, two
+// threads per query row (warps w and w + 4 read the same tensor-memory lanes):
+// one takes keys 0-63 of each tile and the first half of head_dim, the other
+// keys 64-127 and the second half; they agree on the row's reference max
+// through shared memory once per tile.  Every wait is bounded; a wait that gives up makes the
 // CTA's outputs NaN.
 #pragma once
 
@@ -46,7 +50,9 @@ namespace pa {
 
 namespace pf {
 
-constexpr int kThreads = 224;
+constexpr int kThreads = 352;
+constexpr int kSoftmaxThreads = 256; // warps 0-7
+constexpr int kProducer0 = 8, kMmaWarp = 9, kProducer1 = 10;
 constexpr int kTile = 128;          // queries per unit and keys per key tile
 constexpr int kStage = 16384;       // one ring stage
 constexpr int kMaxStages = 12;      // barrier slots in the control block
@@ -84,13 +90,14 @@ struct Ctrl {
   uint64_t qfull;              // q tile landed
   uint64_t qempty;             // q tile no longer read
   uint64_t s_full[2];          // a tile's logits ready (per buffer)
-  uint64_t p_ready;            // P written (128 softmax threads arrive)
+  uint64_t p_ready;            // P written (the 256 softmax threads arrive)
   uint64_t o_done[2];          // P.V of a tile completed (per P buffer)
   uint64_t tail[2];            // producer-private: a tail value stage landed
   uint64_t drain;              // abort path: all issued MMAs finished
   uint64_t never;              // self-test: nothing ever arrives here
   uint32_t tmem;
   int abort;
+  float xrow[kTile];           // per query row: one half's value for the other half
 };
 static_assert(sizeof(Ctrl) <= 1024, "control block");
 
@@ -196,7 +203,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     sm100::mbar_init(&c.qempty, 1);
     sm100::mbar_init(&c.s_full[0], 1);
     sm100::mbar_init(&c.s_full[1], 1);
-    sm100::mbar_init(&c.p_ready, 128);
+    sm100::mbar_init(&c.p_ready, kSoftmaxThreads);
     sm100::mbar_init(&c.o_done[0], 1);
     sm100::mbar_init(&c.o_done[1], 1);
     sm100::mbar_init(&c.tail[0], 1);
@@ -205,11 +212,11 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     sm100::mbar_init(&c.never, 1);
     c.abort = 0;
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     sm100::tmem_alloc(&c.tmem, kTmemCols);
     sm100::tmem_relinquish();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == kProducer0 && lane == 0) {
     sm100::tma_prefetch_desc(&qmap);
     sm100::tma_prefetch_desc(&knmap);
     sm100::tma_prefetch_desc(&vnmap);
@@ -223,14 +230,14 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
   const uint32_t tmem = c.tmem;
   volatile int* abort_flag = &c.abort;
 
-  if (warp == 4 || warp == 6) {
+  if (warp == kProducer0 || warp == kProducer1) {
     // ========================= producers ==========================================
     // Per unit: q, then keys of tile 0, then (keys of tile j, values of tile
     // j - 1) for j >= 1, then the last tile's values -- the order the MMA
     // warp consumes the ring in.  Both producer warps walk this sequence;
     // producer `pid` fills the stages g with g % 2 == pid (and loads q if
     // pid == 0).
-    const uint32_t pid = warp == 6 ? 1u : 0u;
+    const uint32_t pid = warp == kProducer1 ? 1u : 0u;
     uint64_t* my_tail = &c.tail[pid];
     uint64_t keep;  // q, the chunk's keys / values and the context: read by several units
     asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(keep));
@@ -368,7 +375,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       if (tail_pending >= 0) sm100::mbar_wait(my_tail, tn & 1, budget, nullptr);
       if (un > 0) sm100::mbar_wait(&c.qfull, (un - 1) & 1, budget, nullptr);
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ========================= MMA issuer =========================================
     // The whole warp runs the loop in convergent code; one elected lane
     // issues each MMA and commit.  Per unit: QK^T(0), then (QK^T(j),
@@ -458,14 +465,23 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       sm100::mbar_wait(&c.drain, 0, budget, nullptr);
     }
     __syncwarp();
-  } else if (warp < 4) {
-    // ========================= softmax + epilogue (warps 0-3) =====================
-    // Thread r owns query row r of the unit (tensor-memory lane r).  Every
-    // softmax thread runs the same iterations whatever happens; a failed
-    // wait only marks the abort, which ends later waits.
-    const int r = tid;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+  } else if (warp < 8) {
+    // ========================= softmax + epilogue (warps 0-7) =====================
+    // Thread (half, r) owns query row r of the unit (tensor-memory lane r) and
+    // keys 64 * half .. 64 * half + 63 of every tile, head_dim columns
+    // half * D / 2 .. of the output.  Per tile, half 1 publishes its partial
+    // max, half 0 forms the row's reference max (moving it lazily) and
+    // publishes it, and half 1 adopts it, so both halves scale their
+    // probabilities by the same reference.  Every softmax thread runs the same
+    // iterations and barriers whatever happens; a failed wait only marks the
+    // abort, which ends later waits.
+    const int half = tid >> 7;
+    const int r = tid & 127;
+    const int k0 = half * (kTile / 2);  // first key column of this half
+    const int d0 = half * (D / 2);      // first output column of this half
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const float sl2 = a.scale_log2;
+    auto pair_sync = [] { asm volatile("bar.sync 1, 256;" ::: "memory"); };
     uint32_t gt = 0;  // key tiles so far (logits buffer, s_full / o_done phases)
     for (int64_t k = blockIdx.x; k < units; k += gridDim.x) {
       const Unit u = unit_at(a, k);
@@ -497,7 +513,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         const uint32_t sbuf = tmem + lane_base + ((gt & 1) ? kS1Col : 0);
         float mx = -INFINITY;
 #pragma unroll 1
-        for (int c0 = 0; c0 < kTile; c0 += 16) {
+        for (int c0 = k0; c0 < k0 + kTile / 2; c0 += 16) {
           float sv[16];
           sm100::tmem_ld16(sbuf + c0, sv);
           sm100::tmem_wait_ld();
@@ -505,15 +521,31 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
           for (int e = 0; e < 16; ++e)
             if (c0 + e < vis) mx = fmaxf(mx, sv[e]);
         }
-        const float mt = mx * sl2;
-        const float m_new = fmaxf(m_ref, mt);
-        const bool move = m_new > m_ref + kRescaleLog2;
+        // the row's reference max, agreed by both halves
+        if (half == 1) c.xrow[r] = mx;
+        pair_sync();
         float corr = 1.f;
-        if (move) {
-          corr = m_ref == -INFINITY ? 0.f : exp2f(m_ref - m_new);
-          lsum *= corr;
-          m_ref = m_new;
+        bool move = false;
+        if (half == 0) {
+          const float mt = fmaxf(mx, c.xrow[r]) * sl2;
+          const float m_new = fmaxf(m_ref, mt);
+          move = m_new > m_ref + kRescaleLog2;
+          if (move) {
+            corr = m_ref == -INFINITY ? 0.f : exp2f(m_ref - m_new);
+            m_ref = m_new;
+          }
+          c.xrow[r] = m_ref;
         }
+        pair_sync();
+        if (half == 1) {
+          const float m_new = c.xrow[r];
+          move = m_new != m_ref;
+          if (move) {
+            corr = m_ref == -INFINITY ? 0.f : exp2f(m_ref - m_new);
+            m_ref = m_new;
+          }
+        }
+        if (move) lsum *= corr;
         const bool rescale = j > 0 && __any_sync(0xffffffffu, move);
         if (rescale) {
           // O must be complete up to the previous tile before it is rescaled
@@ -521,9 +553,9 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             c.abort = 1;
           sm100::tc_fence_after();
           __syncwarp();
-          // the warp's rows that moved their reference max rescale their O row
+          // the warp's rows that moved their reference max rescale their half of the O row
 #pragma unroll 1
-          for (int c0 = 0; c0 < D; c0 += 16) {
+          for (int c0 = d0; c0 < d0 + D / 2; c0 += 16) {
             float ov[16];
             sm100::tmem_ld16(tmem + lane_base + kOCol + c0, ov);
             sm100::tmem_wait_ld();
@@ -539,11 +571,12 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
           __syncwarp();
         }
         // p = 2^(s * scale * log2(e) - m_ref) for the visible keys, rounded to
-        // 16 bits into P (row r, 128-byte swizzled rows of two 64-key halves)
-        uint8_t* pbuf = ps + (gt & 1) * Lay::kPBytes;
+        // 16 bits into P (row r, 128-byte swizzled rows; this half's 64 keys
+        // are P's 64-key half number `half`)
+        uint8_t* pbuf = ps + (gt & 1) * Lay::kPBytes + half * kStage;
         const float neg_m = -m_ref;
 #pragma unroll 1
-        for (int c0 = 0; c0 < kTile; c0 += 32) {
+        for (int c0 = k0; c0 < k0 + kTile / 2; c0 += 32) {
           float sv[32];
           sm100::tmem_ld16(sbuf + c0, *reinterpret_cast<float(*)[16]>(&sv[0]));
           sm100::tmem_ld16(sbuf + c0 + 16, *reinterpret_cast<float(*)[16]>(&sv[16]));
@@ -557,9 +590,9 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
           }
 #pragma unroll
           for (int q8 = 0; q8 < 4; ++q8) {
-            const int key = c0 + q8 * 8;  // 8 keys = one 16-byte piece
-            const int piece = ((key % 64) / 8) ^ (r & 7);
-            *reinterpret_cast<uint4*>(pbuf + (key / 64) * kStage + r * 128 + piece * 16) =
+            const int key = (c0 - k0) + q8 * 8;  // 8 keys = one 16-byte piece
+            const int piece = (key / 8) ^ (r & 7);
+            *reinterpret_cast<uint4*>(pbuf + r * 128 + piece * 16) =
                 make_uint4(w[q8 * 4 + 0], w[q8 * 4 + 1], w[q8 * 4 + 2], w[q8 * 4 + 3]);
           }
         }
@@ -567,16 +600,26 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         sm100::tc_fence_before();
         sm100::mbar_arrive(&c.p_ready);
       }
-      // ---- epilogue of the unit: O / lsum into out ---------------------------------
+      // ---- epilogue of the unit: O / (both halves' sums) into out ------------------
+      if (half == 1) c.xrow[r] = lsum;
+      pair_sync();
+      float total = lsum;
+      if (half == 0) {
+        total = lsum + c.xrow[r];
+        c.xrow[r] = total;
+      }
+      pair_sync();
+      if (half == 1) total = c.xrow[r];
+      pair_sync();  // xrow is free for the next unit's first tile
       if (!sm100::mbar_wait(&c.o_done[(gt - 1) & 1], ((gt - 1) >> 1) & 1, budget, abort_flag))
         c.abort = 1;
       sm100::tc_fence_after();
       __syncwarp();
       const bool poison = bad || *abort_flag != 0;
-      const float inv = 1.f / lsum;
+      const float inv = 1.f / total;
       const int64_t orow = (static_cast<int64_t>(u.s0) + i) * a.num_heads + u.h;
 #pragma unroll 1
-      for (int c0 = 0; c0 < D; c0 += 16) {
+      for (int c0 = d0; c0 < d0 + D / 2; c0 += 16) {
         float ov[16];
         sm100::tmem_ld16(tmem + lane_base + kOCol + c0, ov);
         sm100::tmem_wait_ld();
@@ -594,7 +637,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
   sm100::tc_fence_before();
   __syncthreads();
   sm100::tc_fence_after();
-  if (warp == 5) sm100::tmem_dealloc(tmem, kTmemCols);
+  if (warp == kMmaWarp) sm100::tmem_dealloc(tmem, kTmemCols);
 }
 
 // Persistent launch: one CTA per SM (the kernel takes ~226 KB of shared
