@@ -496,29 +496,26 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         // visible keys of the tile form a prefix: all context keys, chunk keys
         // up to the row's own
         const int vis = ctx ? nk : max(0, min(nk, i - (j - u.nctx) * kTile + 1));
-        if (ctx) {  // context block ids: one outside the pool poisons the unit
-          const int nblk = (nk + BS - 1) / BS;
-          bool bl = false;
-          if (lane < nblk) {
-            const int32_t id = __ldg(a.block_tables +
-                                     static_cast<int64_t>(u.b) * a.max_blocks_per_seq +
-                                     j * (kTile / BS) + lane);
-            bl = id < 0 || id >= a.num_blocks;
-          }
-          bad |= __any_sync(0xffffffffu, bl);
-        }
+        // context block ids: one outside the pool poisons the unit.  The id is
+        // loaded here and tested after this tile's P is written, so the load's
+        // latency is not on the softmax's path.
+        int32_t blk_id = 0;
+        if (ctx && lane < (nk + BS - 1) / BS)
+          blk_id = __ldg(a.block_tables + static_cast<int64_t>(u.b) * a.max_blocks_per_seq +
+                         j * (kTile / BS) + lane);
         if (!sm100::mbar_wait(&c.s_full[gt & 1], (gt >> 1) & 1, budget, abort_flag)) c.abort = 1;
         sm100::tc_fence_after();
         __syncwarp();
         const uint32_t sbuf = tmem + lane_base + ((gt & 1) ? kS1Col : 0);
         float mx = -INFINITY;
 #pragma unroll 1
-        for (int c0 = k0; c0 < k0 + kTile / 2; c0 += 16) {
-          float sv[16];
-          sm100::tmem_ld16(sbuf + c0, sv);
+        for (int c0 = k0; c0 < k0 + kTile / 2; c0 += 32) {
+          float sv[32];
+          sm100::tmem_ld16(sbuf + c0, *reinterpret_cast<float(*)[16]>(&sv[0]));
+          sm100::tmem_ld16(sbuf + c0 + 16, *reinterpret_cast<float(*)[16]>(&sv[16]));
           sm100::tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
+          for (int e = 0; e < 32; ++e)
             if (c0 + e < vis) mx = fmaxf(mx, sv[e]);
         }
         // the row's reference max, agreed by both halves
@@ -599,6 +596,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         sm100::fence_proxy_async_smem();
         sm100::tc_fence_before();
         sm100::mbar_arrive(&c.p_ready);
+        if (ctx) bad |= __any_sync(0xffffffffu, blk_id < 0 || blk_id >= a.num_blocks);
       }
       // ---- epilogue of the unit: O / (both halves' sums) into out ------------------
       if (half == 1) c.xrow[r] = lsum;
