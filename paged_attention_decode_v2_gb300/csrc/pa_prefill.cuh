@@ -24,9 +24,11 @@
 //         exceeds it by more than 2^8, so p = 2^(s - m) <= 256; p is rounded
 //         to 16 bits for the MMA and the running sum adds the rounded
 //         values, so the result is an exact weighted mean of the values with
-//         weights perturbed by at most one rounding each;
+//         weights perturbed by at most one rounding each; P is written to
+//         tensor memory over the tile's logits;
 //   P.V   O[q, d] += sum_k P[q, k] V[k, d]    M = 128, N = head_dim, K = keys,
-//         accumulated in tensor memory (V is the MN-major operand).
+//         A = P from tensor memory, B = V from shared memory (MN-major),
+//         accumulated in tensor memory.
 // Roles (352 threads): warps 8 and 10 stream q, keys and values with TMA
 // into a ring of 16 KB stages (alternate stages each: a context key stage
 // takes one copy per cache block, so two warps issue them twice as fast);
@@ -34,8 +36,8 @@
 // threads per query row (warps w and w + 4 read the same tensor-memory lanes):
 // one takes keys 0-63 of each tile and the first half of head_dim, the other
 // keys 64-127 and the second half; they agree on the row's reference max
-// through shared memory once per tile.  Every wait is bounded; a wait that gives up makes the
-// CTA's outputs NaN.
+// through shared memory once per tile.  Every wait is bounded; a wait that
+// gives up makes the CTA's outputs NaN.
 #pragma once
 
 #include <algorithm>
@@ -64,18 +66,17 @@ constexpr long long kWaitBudget = 4000000000LL;    // cycles (about 2 s)
 constexpr long long kSelftestBudget = 20000000LL;  // cycles (about 10 ms)
 constexpr int kSmemLimit = 227 * 1024;
 
-// Shared memory: q (head_dim / 64 slices of [128 rows][128 B]), two P
-// buffers (each two 64-key halves of [128 rows][128 B]; tile t uses buffer
-// t % 2, so the softmax of the next tile never waits for this tile's P.V),
-// the ring, the control block.  Every operand tile starts on a 1024-byte
-// boundary (128-byte swizzle atoms).
+// Shared memory: q (head_dim / 64 slices of [128 rows][128 B]), the ring,
+// the control block.  Every operand tile starts on a 1024-byte boundary
+// (128-byte swizzle atoms).  P lives in tensor memory, not here: the P.V MMA
+// reads it as its A operand where the tile's logits were (below), which
+// keeps its 64 KB of writes and reads per tile off the shared-memory
+// bandwidth that the MMAs' operand reads and the TMA copies share.
 template <int D>
 struct Layout {
   static constexpr int kSlices = D / 64;
   static constexpr int kVTokens = kStage / (D * 2);  // keys per value stage
-  static constexpr int kPOff = kSlices * kStage;
-  static constexpr int kPBytes = 2 * kStage;  // one P buffer
-  static constexpr int kRingOff = kPOff + 2 * kPBytes;
+  static constexpr int kRingOff = kSlices * kStage;
   static constexpr int kStages =
       std::min(kMaxStages, (kSmemLimit - kRingOff - 2048) / kStage);
   static constexpr int kCtrlOff = kRingOff + kStages * kStage;
@@ -91,7 +92,7 @@ struct Ctrl {
   uint64_t qempty;             // q tile no longer read
   uint64_t s_full[2];          // a tile's logits ready (per buffer)
   uint64_t p_ready;            // P written (the 256 softmax threads arrive)
-  uint64_t o_done[2];          // P.V of a tile completed (per P buffer)
+  uint64_t o_done[2];          // P.V of a tile completed (by tile parity)
   uint64_t tail[2];            // producer-private: a tail value stage landed
   uint64_t drain;              // abort path: all issued MMAs finished
   uint64_t never;              // self-test: nothing ever arrives here
@@ -187,7 +188,6 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
   extern __shared__ __align__(16) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (sm100::smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* qs = smem;
-  uint8_t* ps = smem + Lay::kPOff;
   uint8_t* ring = smem + Lay::kRingOff;
   Ctrl& c = *reinterpret_cast<Ctrl*>(smem + Lay::kCtrlOff);
 
@@ -385,7 +385,6 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     constexpr uint32_t id_qk = sm100::idesc_f16(kBf16, false, false, 128, kTile);
     constexpr uint32_t id_pv = sm100::idesc_f16(kBf16, false, true, 128, D);
     const uint32_t q_base = sm100::smem_u32(qs);
-    const uint32_t p_base = sm100::smem_u32(ps);
     const uint32_t ring_base = sm100::smem_u32(ring);
     uint32_t g = 0, un = 0, gt = 0, pn = 0;
     bool ok = true;
@@ -412,7 +411,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     };
     auto pv = [&](const Unit& u, int j) -> bool {
       if (!__all_sync(kAll, sm100::mbar_wait(&c.p_ready, pn & 1, budget, abort_flag))) return false;
-      const uint32_t pb = pn & 1;  // P buffer of this tile
+      const uint32_t pb = pn & 1;  // logits buffer of this tile, which now holds its P
       ++pn;
       sm100::tc_fence_after();
       const int nk = tile_keys(u, j);
@@ -427,12 +426,12 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         const int toks = min(kVT, nk - v * kVT);
         for (int r = 0; r < toks; r += 16) {
           const int key = v * kVT + r;
-          const uint64_t ad =
-              sm100::smem_desc(p_base + pb * Lay::kPBytes + (key / 64) * kStage + ((key % 64) / 16) * 32,
-                               16, 1024, sm100::kSw128);
+          // P of keys 64 * h .. 64 * h + 63 is in columns 64 * h .. 64 * h + 31
+          // of the tile's logits buffer, two keys per 32-bit column
+          const uint32_t at = tmem + (pb ? kS1Col : 0) + (key / 64) * 64 + (key % 64) / 2;
           const uint64_t bd = sm100::smem_desc(st + (r / vbs) * vbs * D * 2 + (r % vbs) * 128,
                                                vbs * 128, 1024, sm100::kSw128);
-          sm100::mma_f16_elect(tmem + kOCol, ad, bd, id_pv, (j | v | r) != 0);
+          sm100::mma_f16_ts_elect(tmem + kOCol, at, bd, id_pv, (j | v | r) != 0);
         }
         sm100::mma_commit_elect(&c.empty[slot]);
         ++g;
@@ -561,16 +560,13 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
             sm100::tmem_st16(tmem + lane_base + kOCol + c0, ov);
           }
           sm100::tmem_wait_st();
-        } else if (gt >= 2) {
-          // this tile's P buffer was last read by the P.V two tiles back
-          if (!sm100::mbar_wait(&c.o_done[gt & 1], ((gt - 2) >> 1) & 1, budget, abort_flag))
-            c.abort = 1;
-          __syncwarp();
         }
         // p = 2^(s * scale * log2(e) - m_ref) for the visible keys, rounded to
-        // 16 bits into P (row r, 128-byte swizzled rows; this half's 64 keys
-        // are P's 64-key half number `half`)
-        uint8_t* pbuf = ps + (gt & 1) * Lay::kPBytes + half * kStage;
+        // 16 bits and packed two keys per 32-bit column into this half's first
+        // 32 logit columns (keys k0 + 2c, k0 + 2c + 1 -> column k0 + c), over
+        // logits this thread has already read.  The P.V that reads P is issued
+        // before the MMA that next writes this buffer (the QK^T two tiles on),
+        // and the tensor core runs them in order.
         const float neg_m = -m_ref;
 #pragma unroll 1
         for (int c0 = k0; c0 < k0 + kTile / 2; c0 += 32) {
@@ -578,22 +574,16 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
           sm100::tmem_ld16(sbuf + c0, *reinterpret_cast<float(*)[16]>(&sv[0]));
           sm100::tmem_ld16(sbuf + c0 + 16, *reinterpret_cast<float(*)[16]>(&sv[16]));
           sm100::tmem_wait_ld();
-          uint32_t w[16];
+          float w[16];
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
             const float p0 = c0 + e < vis ? ex2_approx(fmaf(sv[e], sl2, neg_m)) : 0.f;
             const float p1 = c0 + e + 1 < vis ? ex2_approx(fmaf(sv[e + 1], sl2, neg_m)) : 0.f;
-            w[e / 2] = pack2_16(p0, p1, lsum, static_cast<T*>(nullptr));
+            w[e / 2] = __uint_as_float(pack2_16(p0, p1, lsum, static_cast<T*>(nullptr)));
           }
-#pragma unroll
-          for (int q8 = 0; q8 < 4; ++q8) {
-            const int key = (c0 - k0) + q8 * 8;  // 8 keys = one 16-byte piece
-            const int piece = (key / 8) ^ (r & 7);
-            *reinterpret_cast<uint4*>(pbuf + r * 128 + piece * 16) =
-                make_uint4(w[q8 * 4 + 0], w[q8 * 4 + 1], w[q8 * 4 + 2], w[q8 * 4 + 3]);
-          }
+          sm100::tmem_st16(sbuf + k0 + (c0 - k0) / 2, w);
         }
-        sm100::fence_proxy_async_smem();
+        sm100::tmem_wait_st();
         sm100::tc_fence_before();
         sm100::mbar_arrive(&c.p_ready);
         if (ctx) bad |= __any_sync(0xffffffffu, blk_id < 0 || blk_id >= a.num_blocks);
