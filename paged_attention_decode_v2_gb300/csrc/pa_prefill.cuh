@@ -29,14 +29,14 @@
 //   P.V   O[q, d] += sum_k P[q, k] V[k, d]    M = 128, N = head_dim, K = keys,
 //         A = P from tensor memory, B = V from shared memory (MN-major),
 //         accumulated in tensor memory.
-// Roles (352 threads): warps 8 and 10 stream q, keys and values with TMA
-// into a ring of 16 KB stages (alternate stages each: a context key stage
-// takes one copy per cache block, so two warps issue them twice as fast);
-// warp 9 issues the MMAs; warps 0-7 run the softmax and the epilogue, two
-// threads per query row (warps w and w + 4 read the same tensor-memory lanes):
-// one takes keys 0-63 of each tile and the first half of head_dim, the other
-// keys 64-127 and the second half; they agree on the row's reference max
-// through shared memory once per tile.  Every wait is bounded; a wait that
+// Roles: warps 9 .. 8 + kProducers stream q, keys and values with TMA into a
+// ring of 16 KB stages (each issues every kProducers-th stage: a context key
+// stage takes one copy per cache block, and one warp issues copies at a
+// limited rate); warp 8 issues the MMAs; warps 0-7 run the softmax and the
+// epilogue, two threads per query row (warps w and w + 4 read the same
+// tensor-memory lanes): one takes keys 0-63 of each tile and the first half
+// of head_dim, the other keys 64-127 and the second half; they agree on the
+// row's reference max through shared memory once per tile.  Every wait is bounded; a wait that
 // gives up makes the CTA's outputs NaN.
 #pragma once
 
@@ -52,9 +52,10 @@ namespace pa {
 
 namespace pf {
 
-constexpr int kThreads = 352;
+constexpr int kProducers = 3;        // producer warps (each issues every kProducers-th stage)
+constexpr int kThreads = 288 + 32 * kProducers;
 constexpr int kSoftmaxThreads = 256; // warps 0-7
-constexpr int kProducer0 = 8, kMmaWarp = 9, kProducer1 = 10;
+constexpr int kMmaWarp = 8;         // warps 9 .. 8 + kProducers are the producers
 constexpr int kTile = 128;          // queries per unit and keys per key tile
 constexpr int kStage = 16384;       // one ring stage
 constexpr int kMaxStages = 12;      // barrier slots in the control block
@@ -93,7 +94,7 @@ struct Ctrl {
   uint64_t s_full[2];          // a tile's logits ready (per buffer)
   uint64_t p_ready;            // P written (the 256 softmax threads arrive)
   uint64_t o_done[2];          // P.V of a tile completed (by tile parity)
-  uint64_t tail[2];            // producer-private: a tail value stage landed
+  uint64_t tail[kProducers];   // producer-private: a tail value stage landed
   uint64_t drain;              // abort path: all issued MMAs finished
   uint64_t never;              // self-test: nothing ever arrives here
   uint32_t tmem;
@@ -206,8 +207,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     sm100::mbar_init(&c.p_ready, kSoftmaxThreads);
     sm100::mbar_init(&c.o_done[0], 1);
     sm100::mbar_init(&c.o_done[1], 1);
-    sm100::mbar_init(&c.tail[0], 1);
-    sm100::mbar_init(&c.tail[1], 1);
+    for (int p = 0; p < kProducers; ++p) sm100::mbar_init(&c.tail[p], 1);
     sm100::mbar_init(&c.drain, 1);
     sm100::mbar_init(&c.never, 1);
     c.abort = 0;
@@ -216,7 +216,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     sm100::tmem_alloc(&c.tmem, kTmemCols);
     sm100::tmem_relinquish();
   }
-  if (warp == kProducer0 && lane == 0) {
+  if (warp == kMmaWarp + 1 && lane == 0) {
     sm100::tma_prefetch_desc(&qmap);
     sm100::tma_prefetch_desc(&knmap);
     sm100::tma_prefetch_desc(&vnmap);
@@ -230,14 +230,14 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
   const uint32_t tmem = c.tmem;
   volatile int* abort_flag = &c.abort;
 
-  if (warp == kProducer0 || warp == kProducer1) {
+  if (warp > kMmaWarp) {
     // ========================= producers ==========================================
     // Per unit: q, then keys of tile 0, then (keys of tile j, values of tile
     // j - 1) for j >= 1, then the last tile's values -- the order the MMA
-    // warp consumes the ring in.  Both producer warps walk this sequence;
-    // producer `pid` fills the stages g with g % 2 == pid (and loads q if
-    // pid == 0).
-    const uint32_t pid = warp == kProducer1 ? 1u : 0u;
+    // warp consumes the ring in.  Every producer warp walks this sequence;
+    // producer `pid` fills the stages g with g % kProducers == pid (and loads
+    // q if pid == 0).
+    const uint32_t pid = static_cast<uint32_t>(warp - kMmaWarp - 1);
     uint64_t* my_tail = &c.tail[pid];
     uint64_t keep;  // q, the chunk's keys / values and the context: read by several units
     asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(keep));
@@ -245,14 +245,18 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     int tail_pending = -1;
     bool ok = true;
 
-    // TMA row of each lane's block in context tile j (lanes past the tile:
-    // 0, unused); a block id outside the pool becomes a negative row, which
-    // TMA fills with zeros instead of reading memory.
-    auto ctx_rows = [&](const Unit& u, int j) -> int32_t {
-      const int nblk = (tile_keys(u, j) + BS - 1) / BS;
-      if (lane >= nblk) return 0;
-      const int32_t id = __ldg(a.block_tables + static_cast<int64_t>(u.b) * a.max_blocks_per_seq +
-                               j * (kTile / BS) + lane);
+    // Block id of each lane's block in context tile j (lanes past the tile
+    // or tiles past the context: -1, unused).  Loaded a tile ahead of its
+    // use, so the table read's latency is hidden behind the current tile's
+    // copies; ctx_row turns it into a TMA row only where it is used.
+    auto ctx_id = [&](const Unit& u, int j) -> int32_t {
+      if (j >= u.nctx || lane >= (tile_keys(u, j) + BS - 1) / BS) return -1;
+      return __ldg(a.block_tables + static_cast<int64_t>(u.b) * a.max_blocks_per_seq +
+                   j * (kTile / BS) + lane);
+    };
+    // TMA row of a block id; an id outside the pool becomes a negative row,
+    // which TMA fills with zeros instead of reading memory.
+    auto ctx_row = [&](const Unit& u, int32_t id) -> int32_t {
       const int kvh = u.h / a.group;
       return (id < 0 || id >= a.num_blocks) ? -BS : (id * a.num_kv_heads + kvh) * BS;
     };
@@ -263,7 +267,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       const bool ctx = j < u.nctx;
       const int nblk = (nk + BS - 1) / BS;
       for (int sl = 0; sl < kSl; ++sl, ++g) {
-        if ((g & 1u) != pid) continue;
+        if (g % kProducers != pid) continue;
         const int slot = g % NST;
         if (!__all_sync(0xffffffffu, sm100::mbar_wait(&c.empty[slot], ((g / NST) & 1) ^ 1, budget,
                                                         abort_flag)))
@@ -297,7 +301,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       const int vbs = ctx ? BS : 16;  // rows per copy (cache block / 16 chunk rows)
       const int nv = (nk + kVT - 1) / kVT;
       for (int v = 0; v < nv; ++v, ++g) {
-        if ((g & 1u) != pid) continue;
+        if (g % kProducers != pid) continue;
         const int slot = g % NST;
         if (!__all_sync(0xffffffffu, sm100::mbar_wait(&c.empty[slot], ((g / NST) & 1) ^ 1, budget,
                                                         abort_flag)))
@@ -358,8 +362,10 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
         ++un;
       }
       int32_t yprev = 0;
+      int32_t id = ctx_id(u, 0);
       for (int j = 0; j < u.ntiles && ok; ++j) {
-        const int32_t y = j < u.nctx ? ctx_rows(u, j) : 0;
+        const int32_t y = j < u.nctx ? ctx_row(u, id) : 0;
+        id = ctx_id(u, j + 1);  // next tile's ids, first used in the next iteration
         ok = issue_k(u, j, y);
         if (ok && j > 0) ok = issue_v(u, j - 1, yprev);
         yprev = y;
@@ -370,7 +376,7 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       if (lane == 0) c.abort = 1;
       // copies already issued must land before the CTA may exit
       for (uint32_t gg = g > NST ? g - NST : 0; gg < g; ++gg)
-        if ((gg & 1u) == pid && static_cast<int>(gg % NST) != tail_pending)
+        if (gg % kProducers == pid && static_cast<int>(gg % NST) != tail_pending)
           sm100::mbar_wait(&c.full[gg % NST], (gg / NST) & 1, budget, nullptr);
       if (tail_pending >= 0) sm100::mbar_wait(my_tail, tn & 1, budget, nullptr);
       if (un > 0) sm100::mbar_wait(&c.qfull, (un - 1) & 1, budget, nullptr);
