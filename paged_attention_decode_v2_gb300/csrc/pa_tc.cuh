@@ -238,6 +238,17 @@ __global__ void __launch_bounds__(tc::kThreads, CPS)
   // grid's results before reading them.
   asm volatile("griddepcontrol.launch_dependents;");
 
+  // Without a compact work list the producer's first item needs nothing the
+  // set-up writes: its length and first block ids are loaded now, so the
+  // load latency overlaps the set-up below.
+  int32_t pre_L = 0, pre_raw = 0;
+  const bool pre = warp == 4 && !compact && cid < grid_items;
+  if (pre) {
+    const Item it0 = item_coords(a, nullptr, cid, kV2);
+    pre_L = __ldg(a.seq_lens + it0.b);
+    pre_raw = load_block_id<BS>(a, it0.b, it0.t0, lane);
+  }
+
   // ---- set-up -----------------------------------------------------------------
   if (tid == 0) {
     for (int s = 0; s < NST; ++s) {
@@ -352,9 +363,9 @@ __global__ void __launch_bounds__(tc::kThreads, CPS)
     int32_t raw = 0;
     if (k < total_items) {
       it = item_coords(a, prefix, k, kV2);
-      const int32_t L = __ldg(a.seq_lens + it.b);
+      const int32_t L = pre ? pre_L : __ldg(a.seq_lens + it.b);
       const int32_t t_spec = it.t0;
-      raw = load_block_id<BS>(a, it.b, t_spec, lane);
+      raw = pre ? pre_raw : load_block_id<BS>(a, it.b, t_spec, lane);
       item_range(a, it, L, kV2, rank, cs);
       if (it.t0 < it.t1 && it.t0 != t_spec) raw = load_block_id<BS>(a, it.b, it.t0, lane);
       if (it.t0 >= it.t1) {
