@@ -60,7 +60,7 @@ KERNEL_SOURCES = {
 }
 NCU_TRAFFIC = {
     # (kernel, source hash, workload, partition size, path): bytes per launch
-    ("pa_tc_kernel", "f0d1d45f3144f62e", "long_100k", 512, "v2"): 409_735_936 + 2_520_832,
+    ("pa_tc_kernel", "0dd502d08f18dbc0", "long_100k", 512, "v2"): 409_752_576 + 2_527_232,
     ("pa_prefill_kernel", "4b9a914867ec8ff7", "prefill_32k", 0, "prefill"):
         1_360_045_000 + 195_833_856,
 }
