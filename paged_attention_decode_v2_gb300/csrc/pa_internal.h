@@ -63,6 +63,7 @@ struct PrefillArgs {
   int32_t out_dtype;    // pa_dtype_t
   float scale_log2;     // scale * log2(e)
   int32_t qtiles;       // ceil(max_query_len / 128)
+  int32_t cost_levels;  // > 0: walk units by cost, from this level down (0: by query tile)
   int32_t selftest_stall;
 };
 

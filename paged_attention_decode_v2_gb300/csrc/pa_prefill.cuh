@@ -10,9 +10,10 @@
 // paged_attn.py" item 1 (the context comes from the cache) and "Prefill
 // (flash_attn_func)" (causal=True).
 //
-// Work unit: (sequence, query head, 128-query tile of the chunk).  Units are
-// walked last query tile first (the tiles that see the most keys start
-// first) by a persistent grid of one CTA per SM.  Per unit the key tiles
+// Work unit: (sequence, query head, 128-query tile of the chunk).  A
+// persistent grid of one CTA per SM walks the units longest first: last
+// query tile first, or, for batches whose contexts differ, by cost (key
+// tiles) -- see Walk.  Per unit the key tiles
 // (128 keys each) are the context tiles, then the chunk's tiles up to the
 // diagonal one; each tile runs
 //   QK^T  S[q, k] = sum_d Q[q, d] K[k, d]     M = 128 queries, N = 128 keys,
@@ -115,13 +116,12 @@ struct Unit {
   int ntiles;      // context tiles + chunk tiles up to the diagonal
 };
 
-__device__ __forceinline__ Unit unit_at(const PrefillArgs& a, int64_t k) {
-  const int64_t per = static_cast<int64_t>(a.num_seqs) * a.num_heads;
+// Unit (sequence b, query head h, query tile qt).
+__device__ __forceinline__ Unit unit_of(const PrefillArgs& a, int b, int h, int qt) {
   Unit u;
-  u.qt = a.qtiles - 1 - static_cast<int>(k / per);
-  const int64_t rem = k % per;
-  u.b = static_cast<int>(rem / a.num_heads);
-  u.h = static_cast<int>(rem % a.num_heads);
+  u.qt = qt;
+  u.b = b;
+  u.h = h;
   u.s0 = __ldg(a.query_start + u.b);
   const int32_t s1 = __ldg(a.query_start + u.b + 1);
   u.n = s1 - u.s0;
@@ -136,6 +136,73 @@ __device__ __forceinline__ Unit unit_at(const PrefillArgs& a, int64_t k) {
   u.nctx = (u.C + kTile - 1) / kTile;
   u.ntiles = u.nctx + u.qt + 1;
   return u;
+}
+
+// The units one CTA processes, in order; every role walks the same sequence.
+//  * default: index k = blockIdx.x, + gridDim.x, ... over (query tile
+//    descending, sequence, head) -- last query tiles first, which is
+//    longest first when every sequence has the same context;
+//  * cost order (a.cost_levels > 0, batches of uneven contexts): the units
+//    sorted by cost -- key tiles, nctx + qt + 1 -- from the highest level
+//    down, then by sequence and head, and this CTA takes every gridDim.x-th
+//    one, so the longest units start first (a longest-first static
+//    schedule).  Each role scans the (level, sequence) pairs in order;
+//    the host enables it only when there are few of them.
+struct Walk {
+  int64_t k = 0;   // default order: next index
+  int c = 0;       // cost order: current level, sequence, its query tile
+  int b = 0, qt = 0;
+  int h = 0;       //   next head of the current pair for this CTA
+  int64_t n0 = 0;  //   units of the pairs before the current one
+  bool pair = false;
+};
+
+__device__ __forceinline__ Walk walk_begin(const PrefillArgs& a) {
+  Walk w;
+  w.k = blockIdx.x;
+  w.c = a.cost_levels;
+  w.b = -1;
+  return w;
+}
+
+// kCost: the cost order (a.cost_levels > 0); a template parameter so that
+// the default walk compiles to the plain index stride.
+template <bool kCost>
+__device__ __forceinline__ bool walk_next(const PrefillArgs& a, Walk& w, Unit& u) {
+  if constexpr (!kCost) {
+    const int64_t per = static_cast<int64_t>(a.num_seqs) * a.num_heads;
+    const int64_t units = per * a.qtiles;
+    while (w.k < units) {
+      const int64_t k = w.k;
+      w.k += gridDim.x;
+      const int64_t rem = k % per;
+      u = unit_of(a, static_cast<int>(rem / a.num_heads), static_cast<int>(rem % a.num_heads),
+                  a.qtiles - 1 - static_cast<int>(k / per));
+      if (u.run) return true;
+    }
+    return false;
+  } else {
+    while (true) {
+      if (w.pair && w.h < a.num_heads) {
+        u = unit_of(a, w.b, w.h, w.qt);
+        w.h += gridDim.x;
+        return true;
+      }
+      if (w.pair) w.n0 += a.num_heads;
+      if (++w.b >= a.num_seqs) {
+        w.b = 0;
+        if (--w.c < 1) return false;
+      }
+      // does sequence b have a unit of cost c, i.e. query tile c - 1 - nctx?
+      const Unit s = unit_of(a, w.b, 0, 0);
+      w.qt = w.c - 1 - s.nctx;
+      w.pair = s.run && w.qt >= 0 && w.qt * kTile < s.n;
+      if (w.pair) {
+        const int64_t g = gridDim.x;
+        w.h = static_cast<int>(((static_cast<int64_t>(blockIdx.x) - w.n0) % g + g) % g);
+      }
+    }
+  }
 }
 
 // Keys of key tile j of unit u (context tile or chunk tile).
@@ -170,7 +237,7 @@ __device__ __forceinline__ uint32_t pack2_16(float p0, float p1, float& sum, __h
 // block slice-major); qmap / knmap / vnmap: q, k, v as (64, heads, T,
 // head_dim / 64) with boxes (64, 1, 128, 1) for a q or key slice of 128
 // rows and (64, 1, 16, head_dim / 64) for 16 value rows slice-major.
-template <typename T, int D, int BS>
+template <typename T, int D, int BS, bool kCost>
 __global__ void __launch_bounds__(pf::kThreads, 1)
     pa_prefill_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap qmap,
                       const __grid_constant__ CUtensorMap knmap,
@@ -193,7 +260,6 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
   Ctrl& c = *reinterpret_cast<Ctrl*>(smem + Lay::kCtrlOff);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t units = static_cast<int64_t>(a.qtiles) * a.num_seqs * a.num_heads;
 
   if (tid == 0) {
     for (int s = 0; s < NST; ++s) {
@@ -346,9 +412,9 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       return true;
     };
 
-    for (int64_t k = blockIdx.x; k < units && ok; k += gridDim.x) {
-      const Unit u = unit_at(a, k);
-      if (!u.run) continue;
+    Walk wk = walk_begin(a);
+    Unit u;
+    while (ok && walk_next<kCost>(a, wk, u)) {
       // q tile (rows past the chunk belong to other sequences or lie past T,
       // where TMA fills zeros; their rows are never stored)
       if (pid == 0) {
@@ -446,9 +512,9 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
       return true;
     };
 
-    for (int64_t k = blockIdx.x; k < units && ok; k += gridDim.x) {
-      const Unit u = unit_at(a, k);
-      if (!u.run) continue;
+    Walk wk = walk_begin(a);
+    Unit u;
+    while (ok && walk_next<kCost>(a, wk, u)) {
       ok = __all_sync(kAll, sm100::mbar_wait(&c.qfull, un & 1, budget, abort_flag));
       if (!ok) break;
       ++un;
@@ -488,9 +554,9 @@ __global__ void __launch_bounds__(pf::kThreads, 1)
     const float sl2 = a.scale_log2;
     auto pair_sync = [] { asm volatile("bar.sync 1, 256;" ::: "memory"); };
     uint32_t gt = 0;  // key tiles so far (logits buffer, s_full / o_done phases)
-    for (int64_t k = blockIdx.x; k < units; k += gridDim.x) {
-      const Unit u = unit_at(a, k);
-      if (!u.run) continue;
+    Walk wk = walk_begin(a);
+    Unit u;
+    while (walk_next<kCost>(a, wk, u)) {
       const int i = u.qt * kTile + r;  // this row's place in the chunk
       const bool row_ok = i < u.n;
       float m_ref = -INFINITY, lsum = 0.f;
@@ -641,12 +707,15 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, const CUtensorMap (&m)[5], in
                              cudaStream_t s) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
-  auto kern = pa_prefill_kernel<T, D, BS>;
+  auto kern = a.cost_levels > 0 ? pa_prefill_kernel<T, D, BS, true>
+                                 : pa_prefill_kernel<T, D, BS, false>;
   static bool configured[128] = {};
   if (!configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         pf::Layout<D>::kSmem);
-    if (e != cudaSuccess) return e;
+    for (auto k : {pa_prefill_kernel<T, D, BS, true>, pa_prefill_kernel<T, D, BS, false>}) {
+      cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           pf::Layout<D>::kSmem);
+      if (e != cudaSuccess) return e;
+    }
     configured[dev] = true;
   }
   const int64_t units = static_cast<int64_t>(a.qtiles) * a.num_seqs * a.num_heads;

@@ -118,6 +118,11 @@ extern "C" pa_status_t pa_prefill(const pa_prefill_params_t* p, const void* q, c
   a.out_dtype = p->out_dtype;
   a.scale_log2 = p->scale * 1.442695040888963407360f;
   a.qtiles = (p->max_query_len + 127) / 128;
+  // Units cost up to ceil(max_ctx_len / 128) + qtiles key tiles.  Batches of
+  // several sequences are walked by cost (longest first), as long as the
+  // (level, sequence) pairs every role scans stay few.
+  const int64_t levels = (static_cast<int64_t>(p->max_ctx_len) + 127) / 128 + a.qtiles;
+  a.cost_levels = (p->num_seqs > 1 && levels * p->num_seqs <= 8192) ? static_cast<int32_t>(levels) : 0;
   a.selftest_stall = (p->flags & PA_FLAG_SELFTEST_STALL) ? 1 : 0;
   const cudaError_t e = p->kv_dtype == PA_BF16 ? launch_prefill_bf16(a, m, sms, stream)
                                                : launch_prefill_f16(a, m, sms, stream);
