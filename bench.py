@@ -60,9 +60,9 @@ KERNEL_SOURCES = {
 }
 NCU_TRAFFIC = {
     # (kernel, source hash, workload, partition size, path): bytes per launch
-    ("pa_tc_kernel", "0dd502d08f18dbc0", "long_100k", 512, "v2"): 409_752_576 + 2_527_232,
-    ("pa_prefill_kernel", "4b9a914867ec8ff7", "prefill_32k", 0, "prefill"):
-        1_360_045_000 + 195_833_856,
+    ("pa_tc_kernel", "f21390805cd42d76", "long_100k", 512, "v2"): 409_751_552 + 2_804_736,
+    ("pa_prefill_kernel", "7b7a4020ad366a00", "prefill_32k", 0, "prefill"):
+        1_354_648_000 + 194_301_696,
 }
 
 

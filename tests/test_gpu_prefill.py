@@ -153,6 +153,26 @@ def test_prefill_bad_inputs():
     assert np.all(got[s[3]:s[4]] == 7.0)
 
 
+def test_prefill_unit_orders():
+    """Both unit walks of the kernel cover every unit exactly once.  A batch
+    with few (cost level, sequence) pairs is walked by cost; 65 sequences
+    with contexts near 16K tokens (129+ levels x 65 sequences > 8192 pairs)
+    take the query-tile order.  Mixed chunk and context lengths, a 1-token
+    chunk and an empty chunk in each."""
+    g = torch.Generator().manual_seed(31)
+    for nseq, ctx_hi, new_hi in ((6, 3000, 260), (65, 16400, 40)):
+        ctx = [int(x) for x in torch.randint(0, ctx_hi, (nseq,), generator=g)]
+        new = [int(x) for x in torch.randint(1, new_hi, (nseq,), generator=g)]
+        ctx[0], new[0] = ctx_hi, 1
+        new[1] = 0
+        pb = wl.make_prefill(wl.prefill_problem(dtype=torch.bfloat16, ctx=tuple(ctx),
+                                                new=tuple(new), Hq=4, Hkv=2, D=128, BS=16,
+                                                seed=nseq), poison=True)
+        levels = -(-pb.max_ctx_len // 128) + -(-pb.max_query_len // 128)
+        assert (levels * nseq <= 8192) == (nseq == 6)
+        _check(pb, _run(pb), _ref(pb), f"{nseq} sequences")
+
+
 def test_prefill_empty_chunks_and_contexts():
     pb = wl.make_prefill(wl.prefill_problem(dtype=torch.bfloat16, ctx=(0, 64, 0), new=(0, 5, 1),
                                             Hq=4, Hkv=4, D=128, BS=16, seed=2), poison=True)
