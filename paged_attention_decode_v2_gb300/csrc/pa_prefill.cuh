@@ -42,6 +42,7 @@
 #pragma once
 
 #include <algorithm>
+#include <atomic>
 #include <type_traits>
 
 #include <cuda.h>
@@ -709,14 +710,15 @@ cudaError_t launch_prefill_t(const PrefillArgs& a, const CUtensorMap (&m)[5], in
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
   auto kern = a.cost_levels > 0 ? pa_prefill_kernel<T, D, BS, true>
                                  : pa_prefill_kernel<T, D, BS, false>;
-  static bool configured[128] = {};
-  if (!configured[dev]) {
+  // set once per device; concurrent first calls set the same attributes
+  static std::atomic<bool> configured[128];
+  if (!configured[dev].load(std::memory_order_acquire)) {
     for (auto k : {pa_prefill_kernel<T, D, BS, true>, pa_prefill_kernel<T, D, BS, false>}) {
       cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            pf::Layout<D>::kSmem);
       if (e != cudaSuccess) return e;
     }
-    configured[dev] = true;
+    configured[dev].store(true, std::memory_order_release);
   }
   const int64_t units = static_cast<int64_t>(a.qtiles) * a.num_seqs * a.num_heads;
   if (units == 0) return cudaSuccess;

@@ -46,6 +46,7 @@
 #pragma once
 
 #include <algorithm>
+#include <atomic>
 #include <type_traits>
 
 #include <cuda.h>
@@ -851,14 +852,15 @@ __global__ void __launch_bounds__(tc::kThreads, CPS)
 // the one-CTA-per-SM variant clusters of up to 16 CTAs.
 template <typename T, int D, int BS, bool V2, int NST, int CPS>
 cudaError_t configure_tc(int dev) {
-  static bool configured[128] = {};
-  if (configured[dev]) return cudaSuccess;
+  // set once per device; concurrent first calls set the same attributes
+  static std::atomic<bool> configured[128];
+  if (configured[dev].load(std::memory_order_acquire)) return cudaSuccess;
   auto kern = pa_tc_kernel<T, D, BS, V2, NST, CPS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        tc::Layout<D, NST>::kSmemCompact);
   if (e == cudaSuccess && NST == tc::kDeepStages)
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  if (e == cudaSuccess) configured[dev] = true;
+  if (e == cudaSuccess) configured[dev].store(true, std::memory_order_release);
   return e;
 }
 
@@ -895,7 +897,8 @@ cudaError_t launch_tc_variant(const KernelArgs& a, const CUtensorMap& km, const 
 // resident-cluster counts are queried once per device and size.
 template <typename T, int D, int BS, bool V2>
 int fit_cluster(int want, int64_t need) {
-  static int resident[128][5];  // [device][log2 size], 0 = not queried yet
+  // [device][log2 size], 0 = not queried yet; concurrent first calls store the same count
+  static std::atomic<int> resident[128][5];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 1;
   if (configure_tc<T, D, BS, V2, tc::kDeepStages, 1>(dev) != cudaSuccess) return 1;
@@ -904,7 +907,8 @@ int fit_cluster(int want, int64_t need) {
   while ((2 << lg) <= want && lg < 4) ++lg;  // log2 of the largest power of two <= want
   for (; lg >= 1; --lg) {
     const int cs = 1 << lg;
-    if (resident[dev][lg] == 0) {
+    int r = resident[dev][lg].load(std::memory_order_relaxed);
+    if (r == 0) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(static_cast<unsigned>(cs), 1, 1);
       cfg.blockDim = dim3(tc::kThreads, 1, 1);
@@ -921,9 +925,10 @@ int fit_cluster(int want, int64_t need) {
         cudaGetLastError();  // a refused size is not an error of the decode call
         n = 0;
       }
-      resident[dev][lg] = n > 0 ? n : -1;
+      r = n > 0 ? n : -1;
+      resident[dev][lg].store(r, std::memory_order_relaxed);
     }
-    if (resident[dev][lg] >= need) return cs;
+    if (r >= need) return cs;
   }
   return 1;
 }

@@ -9,6 +9,7 @@
 // laid out slice-major; q is viewed as (head_dim, num_seqs * num_heads)
 // rows with an 8-row box (one KV head's query rows).  All use the 128-byte
 // swizzle the MMA descriptors expect.
+#include <atomic>
 #include <mutex>
 
 #include <cuda.h>
@@ -44,20 +45,24 @@ struct DeviceInfo {
   int num_sms = 0;
 };
 
-const DeviceInfo& device_info() {
-  static DeviceInfo cache[128];
-  static const DeviceInfo none;
+// Per-device attributes, queried on first use.  Callers on several host
+// threads may race to fill an entry; they store the same values, and the
+// entry is published by its atomic state after the SM count.
+DeviceInfo device_info() {
+  static std::atomic<int> state[128];
+  static std::atomic<int> num_sms[128];
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return none;
-  DeviceInfo& d = cache[dev];
-  if (!d.state) {
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return DeviceInfo{};
+  int st = state[dev].load(std::memory_order_acquire);
+  if (!st) {
     int major = 0, sms = 0;
     cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    d.num_sms = sms;
-    d.state = (major == 10 && sms > 0) ? 1 : 2;
+    num_sms[dev].store(sms, std::memory_order_relaxed);
+    st = (major == 10 && sms > 0) ? 1 : 2;
+    state[dev].store(st, std::memory_order_release);
   }
-  return d;
+  return DeviceInfo{st, num_sms[dev].load(std::memory_order_relaxed)};
 }
 
 }  // namespace
@@ -84,7 +89,7 @@ cudaError_t encode_tiled(CUtensorMap* map, pa_dtype_t dtype, uint32_t rank, cons
 }
 
 int sm100_num_sms() {
-  const DeviceInfo& d = device_info();
+  const DeviceInfo d = device_info();
   return d.state == 1 ? d.num_sms : 0;
 }
 
