@@ -229,6 +229,48 @@ def test_repeat_runs_are_bit_identical():
             assert np.array_equal(run(bg, path=path, portable=portable), first)
 
 
+def test_concurrent_host_threads():
+    """Calls are thread-safe: four host threads, each with its own stream,
+    workspace and batch, decode concurrently (ctypes releases the GIL during
+    the calls); every result is bit-identical to the same batch decoded alone
+    and matches the oracle."""
+    import threading
+    batches = [wl.make(wl.scaled(wl.WORKLOADS["mixed_32"], num_seqs=3, max_len=L))
+               for L in (900, 3000, 9000, 20000)]
+    refs = [_ref(b) for b in batches]
+    alone = [run(b.to("cuda"), path="decode") for b in batches]
+    results, errors = {}, []
+
+    def worker(i):
+        try:
+            bg = batches[i].to("cuda")
+            stream = torch.cuda.Stream()
+            params = pa.make_params(bg.q, bg.k_cache, bg.block_tables, max_seq_len=bg.max_seq_len,
+                                    scale=bg.scale, out_dtype=torch.float32)
+            ws = pa.alloc_workspace(params, device="cuda")
+            out = torch.empty(tuple(bg.q.shape), dtype=torch.float32, device="cuda")
+            torch.cuda.synchronize()
+            with torch.cuda.stream(stream):
+                for _ in range(20):
+                    pa.decode(bg.q, bg.k_cache, bg.v_cache, bg.block_tables, bg.seq_lens, out, ws,
+                              max_seq_len=bg.max_seq_len, scale=bg.scale, stream=stream)
+            stream.synchronize()
+            assert pa.read_device_status(ws) == pa.PA_OK
+            results[i] = out.double().cpu().numpy()
+        except Exception as e:  # reported below, in the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(len(batches))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for i in range(len(batches)):
+        assert np.array_equal(results[i], alone[i])
+        assert_close(results[i], refs[i], 2e-3, f"thread {i}")
+
+
 def test_bf16_output():
     bc = wl.make(wl.scaled(wl.WORKLOADS["gqa_8k"], seq_len=2100), poison=True)
     ref = _ref(bc)
