@@ -60,9 +60,9 @@ KERNEL_SOURCES = {
 }
 NCU_TRAFFIC = {
     # (kernel, source hash, workload, partition size, path): bytes per launch
-    ("pa_tc_kernel", "f21390805cd42d76", "long_100k", 512, "v2"): 409_751_552 + 2_804_736,
-    ("pa_prefill_kernel", "7b7a4020ad366a00", "prefill_32k", 0, "prefill"):
-        1_354_648_000 + 194_301_696,
+    ("pa_tc_kernel", "dab6dd48ef38a186", "long_100k", 512, "v2"): 409_728_256 + 2_795_008,
+    ("pa_prefill_kernel", "686df58de52966ca", "prefill_32k", 0, "prefill"):
+        1_354_087_424 + 194_575_616,
 }
 
 
