@@ -198,9 +198,9 @@ PA_API pa_status_t pa_decode_v2_reduce(const pa_params_t* params, const int32_t*
 /*
  * Dispatch: V2 when max_seq_len > v1_max_seq_len (8192 by default), else
  * V1.  The workspace is only touched (and only required) when V2 runs.
- * Source: commit 1a4e1005 "paged_attn.py", change 1 ("For sequences > 8192
- * tokens ... V2"), and commit 4eb83a7e "qwen3_6_scripts", paragraph
- * "forward_decode: V2 enabled via original heuristic".
+ * Source: commit 1a4e1005 "paged_attn.py", change 1 (V2 for sequences
+ * longer than 8192 tokens), and commit 4eb83a7e "qwen3_6_scripts",
+ * paragraph "forward_decode: V2 enabled via original heuristic".
  */
 PA_API pa_status_t pa_decode(const pa_params_t* params, const void* q, const void* k_cache,
                       const void* v_cache, const int32_t* block_tables, const int32_t* seq_lens,
