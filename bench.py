@@ -271,16 +271,20 @@ def run_ours(args, rank, world, device):
     # pa_decode_host: q, block table and lengths copied in from pinned host
     # memory, the step, the result copied back, and the wait -- all inside
     # the timed region; the caches and the workspace stay resident.
-    q_h = batch.q.cpu().pin_memory()
-    bt_h = batch.block_tables.cpu().pin_memory()
-    sl_h = batch.seq_lens.cpu().pin_memory()
-    out_h = torch.empty(tuple(out.shape), dtype=out.dtype).pin_memory()
     # the same path as the device-timed step (pa_decode's threshold, or V1 / V2
     # forced through it)
     v1max = {"v1": max(batch.max_seq_len, 1), "v2": 1}.get(args.path, pa.DEFAULT_V1_MAX_SEQ_LEN)
     hparams = pa.make_params(batch.q, batch.k_cache, batch.block_tables,
                              max_seq_len=batch.max_seq_len, scale=batch.scale, partition_size=P,
                              out_dtype=out.dtype, v1_max_seq_len=v1max)
+    # the host inputs live in a pinned mirror of the staging layout, so the
+    # call moves them in one copy
+    _, q_h, bt_h, sl_h = pa.alloc_host_mirror(hparams, batch.q.dtype, *batch.q.shape,
+                                              batch.block_tables.shape[1])
+    q_h.copy_(batch.q.cpu())
+    bt_h.copy_(batch.block_tables.cpu())
+    sl_h.copy_(batch.seq_lens.cpu())
+    out_h = torch.empty(tuple(out.shape), dtype=out.dtype).pin_memory()
     staging = pa.alloc_host_staging(hparams, device=device)
     ws_host = ws if pa.decode_path(hparams) == 2 else None
     e2e_s = []

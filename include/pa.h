@@ -251,13 +251,21 @@ PA_API pa_status_t pa_decode_v2_static(const pa_params_t* params, const void* q,
  *              boundary) and may hold anything between calls.
  *   host buffers: page-locked memory (cudaHostAlloc / pinned tensors) makes
  *              the copies asynchronous DMA; pageable memory also works, with
- *              the copies staged by the CUDA driver.
+ *              the copies staged by the CUDA driver.  When block_tables_host
+ *              and seq_lens_host sit at the staging offsets from q_host (a
+ *              host mirror of the staging layout, pa_host_staging_offsets),
+ *              the three inputs move in one copy.
  * Errors: the checks of pa_decode, a null or misaligned staging buffer
  * (PA_ERR_INVALID_ARG / PA_ERR_MISALIGNED), staging_bytes too small
  * (PA_ERR_WORKSPACE_TOO_SMALL), all before anything is enqueued; a failed
  * copy or wait gives PA_ERR_CUDA.
  */
 PA_API size_t pa_host_staging_size(const pa_params_t* params);
+/* Byte offsets within the staging layout: offsets[0] = q (0), [1] =
+ * block_tables, [2] = seq_lens, [3] = out, [4] = total (= staging size).
+ * PA_ERR_INVALID_ARG for invalid parameters or a null array.  Pure host
+ * function. */
+PA_API pa_status_t pa_host_staging_offsets(const pa_params_t* params, size_t offsets[5]);
 PA_API pa_status_t pa_decode_host(const pa_params_t* params, const void* q_host,
                                   const void* k_cache, const void* v_cache,
                                   const int32_t* block_tables_host, const int32_t* seq_lens_host,

@@ -40,7 +40,8 @@ DEFAULT_V1_MAX_SEQ_LEN = 8192
 EXPORTS = ("pa_workspace_size", "pa_decode_v1", "pa_decode_v2", "pa_decode_v2_partitions",
            "pa_decode_v2_reduce", "pa_decode", "pa_decode_path", "pa_status_string",
            "pa_workspace_init", "pa_read_device_status", "pa_version", "pa_decode_v2_static",
-           "pa_decode_kernel", "pa_host_staging_size", "pa_decode_host", "pa_prefill")
+           "pa_decode_kernel", "pa_host_staging_size", "pa_host_staging_offsets",
+           "pa_decode_host", "pa_prefill")
 PA_STATIC_WORKSPACE_BYTES = 16 << 20
 
 
@@ -133,6 +134,8 @@ def lib() -> ctypes.CDLL:
             L.pa_decode_v2_static.restype = ctypes.c_int
             L.pa_host_staging_size.argtypes = [PP]
             L.pa_host_staging_size.restype = ctypes.c_size_t
+            L.pa_host_staging_offsets.argtypes = [PP, ctypes.POINTER(ctypes.c_size_t)]
+            L.pa_host_staging_offsets.restype = ctypes.c_int
             L.pa_decode_host.argtypes = [PP, P, P, P, P, P, P, ctypes.c_size_t, P, ctypes.c_size_t,
                                          P, P]
             L.pa_decode_host.restype = ctypes.c_int
@@ -337,6 +340,32 @@ def alloc_host_staging(params: Params, device=None):
     if n == 0:
         raise PaError(PA_ERR_INVALID_ARG, "pa_host_staging_size")
     return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def host_staging_offsets(params: Params):
+    """``pa_host_staging_offsets``: byte offsets of q, block_tables, seq_lens
+    and out in the staging layout, and its total size."""
+    arr = (ctypes.c_size_t * 5)()
+    st = lib().pa_host_staging_offsets(ctypes.byref(params), arr)
+    if st != PA_OK:
+        raise PaError(st, "pa_host_staging_offsets")
+    return tuple(int(x) for x in arr)
+
+
+def alloc_host_mirror(params: Params, q_dtype, num_seqs: int, num_heads: int, head_dim: int,
+                      max_blocks_per_seq: int):
+    """A pinned host buffer with the staging layout, and CPU tensors viewing
+    its q, block_tables and seq_lens regions.  Inputs written there are moved
+    by :func:`decode_host` in one copy."""
+    import torch
+    off = host_staging_offsets(params)
+    buf = torch.zeros(off[4], dtype=torch.uint8).pin_memory()
+    esz = torch.tensor([], dtype=q_dtype).element_size()
+    nq = num_seqs * num_heads * head_dim
+    q = buf[:nq * esz].view(q_dtype).view(num_seqs, num_heads, head_dim)
+    bt = buf[off[1]:off[1] + num_seqs * max_blocks_per_seq * 4].view(torch.int32)
+    sl = buf[off[2]:off[2] + num_seqs * 4].view(torch.int32)
+    return buf, q, bt.view(num_seqs, max_blocks_per_seq), sl
 
 
 def decode_host(q, k_cache, v_cache, block_tables, seq_lens, out, workspace, staging, *,

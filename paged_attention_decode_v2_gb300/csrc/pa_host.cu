@@ -53,6 +53,17 @@ size_t pa_host_staging_size(const pa_params_t* p) {
   return staging_layout(p).total;
 }
 
+pa_status_t pa_host_staging_offsets(const pa_params_t* p, size_t offsets[5]) {
+  if (!offsets || check_params(p, false) != PA_OK) return PA_ERR_INVALID_ARG;
+  const Staging s = staging_layout(p);
+  offsets[0] = 0;
+  offsets[1] = s.bt_off;
+  offsets[2] = s.sl_off;
+  offsets[3] = s.out_off;
+  offsets[4] = s.total;
+  return PA_OK;
+}
+
 pa_status_t pa_decode_host(const pa_params_t* p, const void* q_host, const void* k_cache,
                            const void* v_cache, const int32_t* block_tables_host,
                            const int32_t* seq_lens_host, void* workspace, size_t workspace_bytes,
@@ -82,12 +93,21 @@ pa_status_t pa_decode_host(const pa_params_t* p, const void* q_host, const void*
   int32_t* sl_d = reinterpret_cast<int32_t*>(base + s.sl_off);
   void* out_d = base + s.out_off;
   if (p->num_seqs > 0) {
-    if (cudaMemcpyAsync(q_d, q_host, s.q_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
-        cudaMemcpyAsync(bt_d, block_tables_host, s.bt_bytes, cudaMemcpyHostToDevice, stream) !=
-            cudaSuccess ||
-        cudaMemcpyAsync(sl_d, seq_lens_host, s.sl_bytes, cudaMemcpyHostToDevice, stream) !=
-            cudaSuccess)
+    const char* qh = static_cast<const char*>(q_host);
+    const bool mirrored = reinterpret_cast<const char*>(block_tables_host) == qh + s.bt_off &&
+                          reinterpret_cast<const char*>(seq_lens_host) == qh + s.sl_off;
+    if (mirrored) {  // the host inputs already have the staging layout: one copy
+      if (cudaMemcpyAsync(q_d, q_host, s.sl_off + s.sl_bytes, cudaMemcpyHostToDevice, stream) !=
+          cudaSuccess)
+        return PA_ERR_CUDA;
+    } else if (cudaMemcpyAsync(q_d, q_host, s.q_bytes, cudaMemcpyHostToDevice, stream) !=
+                   cudaSuccess ||
+               cudaMemcpyAsync(bt_d, block_tables_host, s.bt_bytes, cudaMemcpyHostToDevice,
+                               stream) != cudaSuccess ||
+               cudaMemcpyAsync(sl_d, seq_lens_host, s.sl_bytes, cudaMemcpyHostToDevice, stream) !=
+                   cudaSuccess) {
       return PA_ERR_CUDA;
+    }
   }
   st = pa_decode(p, q_d, k_cache, v_cache, bt_d, sl_d, workspace, workspace_bytes, out_d, stream);
   if (st != PA_OK) return st;

@@ -190,3 +190,11 @@ def test_host_staging_size_and_checks(L):
     assert call(None, want) == pa.PA_ERR_INVALID_ARG
     assert call(ctypes.c_void_p(0x10008), want) == pa.PA_ERR_MISALIGNED
     assert call(ctypes.c_void_p(0x10000), want - 1) == pa.PA_ERR_WORKSPACE_TOO_SMALL
+    # the offsets of the same layout (for a host mirror of it)
+    off = pa.host_staging_offsets(p)
+    assert off == (0, r(2 * 24 * 256 * 2), r(2 * 24 * 256 * 2) + r(2 * 6250 * 4),
+                   r(2 * 24 * 256 * 2) + r(2 * 6250 * 4) + r(2 * 4), want)
+    assert L.pa_host_staging_offsets(ctypes.byref(p), None) == pa.PA_ERR_INVALID_ARG
+    bad = (ctypes.c_size_t * 5)()
+    assert L.pa_host_staging_offsets(ctypes.byref(params(num_heads=25)), bad) == \
+        pa.PA_ERR_INVALID_ARG

@@ -434,6 +434,16 @@ def test_decode_from_host_buffers_matches_device_call():
                        bc.seq_lens.pin_memory(), out_h, ws, staging, max_seq_len=bc.max_seq_len,
                        scale=bc.scale, v1_max_seq_len=v1max)
         assert np.array_equal(out_h.double().numpy(), ref), f"path {pa.decode_path(params)}"
+        # the inputs in a pinned mirror of the staging layout (one copy in)
+        _, qm, btm, slm = pa.alloc_host_mirror(params, bc.q.dtype, *bc.q.shape,
+                                               bc.block_tables.shape[1])
+        qm.copy_(bc.q)
+        btm.copy_(bc.block_tables)
+        slm.copy_(bc.seq_lens)
+        out_h.fill_(float("nan"))
+        pa.decode_host(qm, bg.k_cache, bg.v_cache, btm, slm, out_h, ws, staging,
+                       max_seq_len=bc.max_seq_len, scale=bc.scale, v1_max_seq_len=v1max)
+        assert np.array_equal(out_h.double().numpy(), ref), "mirrored host inputs"
         if ws is not None:
             assert pa.read_device_status(ws) == pa.PA_OK
 
