@@ -13,8 +13,8 @@ every timed step a 256 MiB read sweep evicts L2 (reads, so that no dirty
 lines are left to be written back while the step runs).
 
 `--impl reference` times the float64 CPU oracle on the host cores instead
-(the reference arm): each step computes a bounded sample of the step's
-query-head rows, scaled to a full step.
+(the reference arm): each step is the whole batch when the run fits its
+budget (--ref-budget-s), else an even spread of rows scaled to a full step.
 
 Multi-GPU (`torchrun --nproc-per-node N bench.py --gpus N`): every rank runs
 its own replica of the batch on its own GPU (the decode step has no
@@ -135,6 +135,16 @@ class ClockSampler:
     def mark(self, name):
         self.marks.append((name, time.time()))
 
+    def wait_first(self, timeout=5.0):
+        """Wait (bounded) until nvidia-smi has printed its first sample, so
+        the GPU loops that follow are covered from their start."""
+        t0 = time.time()
+        while self.proc and not self.lines and time.time() - t0 < timeout:
+            time.sleep(0.01)
+
+    def count(self, t0, t1):
+        return sum(1 for ts, _ in self.lines if t0 <= ts <= t1)
+
     def stop(self):
         if self.proc:
             self.proc.terminate()
@@ -164,6 +174,22 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
                 "samples": len(sm)}
+
+
+def hold_until_sampled(sampler, t0, step_fn, device, min_samples=5, max_s=3.0):
+    """Repeat ``step_fn`` (untimed) until the clock sampler holds at least
+    ``min_samples`` samples since ``t0`` or ``max_s`` seconds have passed, so
+    the clock record covers the GPU under this load even when the timed
+    loops last only milliseconds.  Returns the number of extra steps run."""
+    if sampler.proc is None:
+        return 0
+    n, t_hold = 0, time.time()
+    while sampler.count(t0, time.time()) < min_samples and time.time() - t_hold < max_s:
+        for _ in range(20):
+            step_fn()
+        torch.cuda.synchronize(device)
+        n += 20
+    return n
 
 
 def gpu_id_for_smi(device) -> str:
@@ -225,6 +251,8 @@ def run_ours(args, rank, world, device):
     sampler = ClockSampler(gpu_id_for_smi(device))
     if rank == 0:
         sampler.start()
+        sampler.wait_first()
+    t_gpu0 = time.time()
     for _ in range(args.warmup):
         flush.zero_()
         step()
@@ -279,8 +307,8 @@ def run_ours(args, rank, world, device):
                              out_dtype=out.dtype, v1_max_seq_len=v1max)
     # the host inputs live in a pinned mirror of the staging layout, so the
     # call moves them in one copy
-    _, q_h, bt_h, sl_h = pa.alloc_host_mirror(hparams, batch.q.dtype, *batch.q.shape,
-                                              batch.block_tables.shape[1])
+    mbuf, q_h, bt_h, sl_h = pa.alloc_host_mirror(hparams, batch.q.dtype, *batch.q.shape,
+                                                 batch.block_tables.shape[1])
     q_h.copy_(batch.q.cpu())
     bt_h.copy_(batch.block_tables.cpu())
     sl_h.copy_(batch.seq_lens.cpu())
@@ -299,6 +327,45 @@ def run_ours(args, rank, world, device):
     assert torch.equal(out_h, out.cpu()), "host-buffer step differs from the device step"
     h2d = q_h.numel() * q_h.element_size() + bt_h.numel() * 4 + sl_h.numel() * 4
     d2h = out_h.numel() * out_h.element_size()
+
+    # ---- the end-to-end step taken apart ----------------------------------
+    # The same operations pa_decode_host enqueues (one copy of the mirrored
+    # inputs into the staging buffer, the decode on the staged inputs, the
+    # copy of the result back), issued one by one with stream events between
+    # them, then the host's wait: device time of each part, and the host time
+    # that is not device time (call overheads and the wait's wake-up).
+    offs = pa.host_staging_offsets(hparams)
+    n_in = offs[2] + sl_h.numel() * 4
+    mirror_u8 = mbuf[:n_in]
+    q_d = staging[:offs[1]].view(batch.q.dtype)[:batch.q.numel()].view(tuple(batch.q.shape))
+    bt_d = staging[offs[1]:offs[2]].view(torch.int32)[:bt_h.numel()].view(tuple(bt_h.shape))
+    sl_d = staging[offs[2]:offs[3]].view(torch.int32)[:sl_h.numel()]
+    out_d = staging[offs[3]:].view(out.dtype)[:out.numel()].view(tuple(out.shape))
+    parts = {"h2d": [], "step": [], "d2h": [], "host_not_device": []}
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        torch.cuda.synchronize(device)
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        t0 = time.perf_counter()
+        e[0].record(stream)
+        staging[:n_in].copy_(mirror_u8, non_blocking=True)
+        e[1].record(stream)
+        pa.decode(q_d, batch.k_cache, batch.v_cache, bt_d, sl_d, out_d, ws_host,
+                  max_seq_len=batch.max_seq_len, scale=batch.scale, partition_size=P,
+                  v1_max_seq_len=v1max)
+        e[2].record(stream)
+        out_h.copy_(out_d, non_blocking=True)
+        e[3].record(stream)
+        torch.cuda.synchronize(device)
+        wall = time.perf_counter() - t0
+        if i >= args.warmup:
+            parts["h2d"].append(e[0].elapsed_time(e[1]))
+            parts["step"].append(e[1].elapsed_time(e[2]))
+            parts["d2h"].append(e[2].elapsed_time(e[3]))
+            parts["host_not_device"].append(wall * 1e3 - e[0].elapsed_time(e[3]))
+    assert torch.equal(out_h, out.cpu()), "the step taken apart differs from the device step"
+    hold = hold_until_sampled(sampler, t_gpu0, step, device) if rank == 0 else 0
+    t_gpu1 = time.time()
     if rank == 0:
         sampler.stop()
 
@@ -356,11 +423,20 @@ def run_ours(args, rank, world, device):
         },
         "reduce_us": round(statistics.mean(red_ms) * 1e3, 3) if red_ms else None,
         "e2e": {"value": round(t_e2e * 1e3, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h,
+                "parts_us": {k: round(statistics.mean(v) * 1e3, 3) for k, v in parts.items()},
+                "parts_how": "the operations of pa_decode_host issued one by one with stream "
+                             "events between them: h2d = one copy of the pinned mirrored inputs, "
+                             "step = pa_decode on the staged inputs, d2h = the result back, "
+                             "host_not_device = host wall time minus the events' span"},
         "gpu_launches": launches_per_step * args.steps,
     }
     if rank == 0:
-        result["clocks"] = sampler.summary(t_start, t_end)
+        result["clocks"] = sampler.summary(t_gpu0, t_gpu1)
+        result["clocks"]["window"] = (
+            "whole GPU run: warm-up, timed steps, kernels timed apart, end-to-end loops"
+            + (f", plus {hold} untimed steps until 5 samples" if hold else ""))
+        result["clocks"]["timed_region_samples"] = sampler.count(t_start, t_end)
         if world == 1 and not args.no_cpu_baseline:
             result["cpu_baseline"] = cpu_baseline(batch, args.cpu_rows, args.cpu_seconds)
     return result
@@ -414,6 +490,8 @@ def run_prefill(args, rank, world, device):
     sampler = ClockSampler(gpu_id_for_smi(device))
     if rank == 0:
         sampler.start()
+        sampler.wait_first()
+    t_gpu0 = time.time()
     for _ in range(args.warmup):
         flush()
         step(pb.q, pb.k, pb.v, pb.query_start, pb.ctx_lens, pb.block_tables, out)
@@ -456,6 +534,11 @@ def run_prefill(args, rank, world, device):
             e2e_s.append(time.perf_counter() - t0)
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_h.numel() * out_h.element_size()
+    hold = 0
+    if rank == 0:
+        hold = hold_until_sampled(sampler, t_gpu0, lambda: step(
+            pb.q, pb.k, pb.v, pb.query_start, pb.ctx_lens, pb.block_tables, out), device)
+    t_gpu1 = time.time()
     if rank == 0:
         sampler.stop()
     assert torch.isfinite(out).all().item(), "non-finite output"
@@ -504,7 +587,11 @@ def run_prefill(args, rank, world, device):
         "gpu_launches": args.steps,
     }
     if rank == 0:
-        result["clocks"] = sampler.summary(t_start, t_end)
+        result["clocks"] = sampler.summary(t_gpu0, t_gpu1)
+        result["clocks"]["window"] = (
+            "whole GPU run: warm-up, timed steps, end-to-end loop"
+            + (f", plus {hold} untimed steps until 5 samples" if hold else ""))
+        result["clocks"]["timed_region_samples"] = sampler.count(t_start, t_end)
         if world == 1 and not args.no_cpu_baseline:
             result["cpu_baseline"] = cpu_baseline_prefill(pb, args.cpu_rows, args.cpu_seconds)
     return result
@@ -586,13 +673,13 @@ def cpu_baseline(batch, nrows, seconds):
 
 
 def run_reference(args, rank, world):
-    """The reference arm: the float64 oracle, as it stands, on the host cores.
-    Each step computes one query-head row over at most --ref-tokens of its
-    tokens (rows taken in turn); the time is scaled by the step's total
-    (row x token) work over the sample's."""
+    """The reference arm: the float64 oracle, as it stands, on all host
+    cores.  A decode step is the whole batch (every query-head row) when
+    the run fits --ref-budget-s, else an even spread of rows scaled to the
+    step's work; a prefill step computes 8 spread rows scaled by
+    visible-key work (a whole prefill step takes minutes on the host)."""
     if rank != 0:
         return None
-    import dataclasses
     import oracle
     if args.workload in wl.PREFILL_WORKLOADS:
         pb = wl.make_prefill(wl.PREFILL_WORKLOADS[args.workload])
@@ -617,29 +704,39 @@ def run_reference(args, rank, world):
     w = wl.WORKLOADS[args.workload]
     P = args.partition_size or w.partition_sizes[0]
     bc = wl.make(w, device="cpu")
-    T = max(1, args.ref_tokens)
-    sample = dataclasses.replace(bc, seq_lens=bc.seq_lens.clamp(max=T))
-    lens = bc.seq_lens.tolist()
     total_rows = w.num_seqs * w.num_heads
-    total_work = sum(lens) * w.num_heads
+    # Whole steps (every query-head row of the batch) when the run fits the
+    # budget; otherwise each step computes an even spread of rows, as many as
+    # fit, and its time is scaled by the step's row x token work.
+    t_full = _oracle_rows(bc, None)
+    n_all = args.warmup + args.steps
+    lens = bc.seq_lens.tolist()
+    if t_full * n_all <= args.ref_budget_s:
+        rows, scale_f = None, 1.0
+        how = f"whole steps: all {total_rows} query-head rows of the batch"
+    else:
+        k = max(1, int(total_rows * args.ref_budget_s / (t_full * n_all)))
+        rows = [int(i * total_rows / k) for i in range(k)]
+        work = sum(lens[r // w.num_heads] for r in rows)
+        scale_f = sum(lens) * w.num_heads / max(1, work)
+        how = (f"{k} of {total_rows} query-head rows per step (evenly spread), scaled by the "
+               f"step's row x token work")
     times = []
-    for i in range(args.warmup + args.steps):
-        row = (i * 7) % total_rows
-        work = min(lens[row // w.num_heads], T)
-        dt = _oracle_rows(sample, [row])
-        if i >= args.warmup and work > 0:
-            times.append(dt * total_work / work)
+    for i in range(n_all):
+        dt = _oracle_rows(bc, rows)
+        if i >= args.warmup:
+            times.append(dt * scale_f)
     t = statistics.mean(times)
     v = round(t * 1e6, 1)
+    cores = oracle.max_threads()
     return {
         "impl": "reference",
         "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "partition_size": P},
-        "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"per step one of {total_rows} query-head rows over at most "
-                                   f"{T} tokens, scaled to the step's full row x token work"},
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": how},
         "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -659,8 +756,8 @@ def main():
                     help="host time the oracle baseline runs for (whole repetitions)")
     ap.add_argument("--cpu-rows", type=int, default=24,
                     help="query-head rows the CPU baseline computes")
-    ap.add_argument("--ref-tokens", type=int, default=4096,
-                    help="tokens of one query-head row per reference-arm step")
+    ap.add_argument("--ref-budget-s", type=float, default=150.0,
+                    help="host seconds the reference arm may spend in all its steps")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

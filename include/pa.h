@@ -221,8 +221,10 @@ PA_API pa_status_t pa_decode(const pa_params_t* params, const void* q, const voi
  *     enqueued (16 MiB covers, e.g., one 24-head, head_dim-256 sequence of
  *     up to about 340K tokens at partition_size 512).
  *   - The first call on a device looks up the array's device address (with
- *     that device current) and caches it; make that first call before any
- *     stream capture.
+ *     that device current) and caches it for the current context; a new
+ *     context on that device (after cudaDeviceReset, or a driver-API context
+ *     the caller made current) looks it up again.  Make the first call in a
+ *     context before any stream capture.
  *   - All calls on a device share the array, and it keeps the last call's
  *     contents (nothing in it needs to start at zero).  Calls that overlap on
  *     the GPU race on it: order them on one stream.
@@ -257,8 +259,11 @@ PA_API pa_status_t pa_decode_v2_static(const pa_params_t* params, const void* q,
  *              the three inputs move in one copy.
  * Errors: the checks of pa_decode, a null or misaligned staging buffer
  * (PA_ERR_INVALID_ARG / PA_ERR_MISALIGNED), staging_bytes too small
- * (PA_ERR_WORKSPACE_TOO_SMALL), all before anything is enqueued; a failed
- * copy or wait gives PA_ERR_CUDA.
+ * (PA_ERR_WORKSPACE_TOO_SMALL), misaligned caches (PA_ERR_MISALIGNED), all
+ * before anything is enqueued; a failed copy, launch or wait gives
+ * PA_ERR_CUDA.  An error found after the copies were queued is returned only
+ * once the stream has finished, so no copy still uses the host buffers when
+ * the call returns.
  */
 PA_API size_t pa_host_staging_size(const pa_params_t* params);
 /* Byte offsets within the staging layout: offsets[0] = q (0), [1] =

@@ -86,12 +86,21 @@ pa_status_t pa_decode_host(const pa_params_t* p, const void* q_host, const void*
     return PA_ERR_INVALID_ARG;
   }
   if (!k_cache || !v_cache) return PA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(k_cache) % 16 || reinterpret_cast<uintptr_t>(v_cache) % 16)
+    return PA_ERR_MISALIGNED;
 
   uint8_t* base = static_cast<uint8_t*>(staging);
   void* q_d = base;
   int32_t* bt_d = reinterpret_cast<int32_t*>(base + s.bt_off);
   int32_t* sl_d = reinterpret_cast<int32_t*>(base + s.sl_off);
   void* out_d = base + s.out_off;
+  // From here on copies may be queued that read the caller's host buffers:
+  // an error return first waits for the stream, so that no copy still reads
+  // (or writes) them after the call has returned.
+  auto fail = [&](pa_status_t e) {
+    cudaStreamSynchronize(stream);
+    return e;
+  };
   if (p->num_seqs > 0) {
     const char* qh = static_cast<const char*>(q_host);
     const bool mirrored = reinterpret_cast<const char*>(block_tables_host) == qh + s.bt_off &&
@@ -99,21 +108,21 @@ pa_status_t pa_decode_host(const pa_params_t* p, const void* q_host, const void*
     if (mirrored) {  // the host inputs already have the staging layout: one copy
       if (cudaMemcpyAsync(q_d, q_host, s.sl_off + s.sl_bytes, cudaMemcpyHostToDevice, stream) !=
           cudaSuccess)
-        return PA_ERR_CUDA;
+        return fail(PA_ERR_CUDA);
     } else if (cudaMemcpyAsync(q_d, q_host, s.q_bytes, cudaMemcpyHostToDevice, stream) !=
                    cudaSuccess ||
                cudaMemcpyAsync(bt_d, block_tables_host, s.bt_bytes, cudaMemcpyHostToDevice,
                                stream) != cudaSuccess ||
                cudaMemcpyAsync(sl_d, seq_lens_host, s.sl_bytes, cudaMemcpyHostToDevice, stream) !=
                    cudaSuccess) {
-      return PA_ERR_CUDA;
+      return fail(PA_ERR_CUDA);
     }
   }
   st = pa_decode(p, q_d, k_cache, v_cache, bt_d, sl_d, workspace, workspace_bytes, out_d, stream);
-  if (st != PA_OK) return st;
+  if (st != PA_OK) return fail(st);
   if (p->num_seqs > 0 &&
       cudaMemcpyAsync(out_host, out_d, s.out_bytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
-    return PA_ERR_CUDA;
+    return fail(PA_ERR_CUDA);
   if (cudaStreamSynchronize(stream) != cudaSuccess) return PA_ERR_CUDA;
   return PA_OK;
 }

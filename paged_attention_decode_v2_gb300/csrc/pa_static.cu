@@ -18,6 +18,8 @@
 // between them) race on it: order them on one stream.
 #include <mutex>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime_api.h>
 
 #include "pa.h"
@@ -28,22 +30,74 @@ namespace {
 static __device__ __align__(256) unsigned char g_static_ws[PA_STATIC_WORKSPACE_BYTES];
 
 constexpr int kMaxDevices = 128;
+
+// The driver calls that name the current context, looked up once through the
+// runtime (the library links no driver library of its own).
+struct CtxCalls {
+  PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  PFN_cuCtxGetId_v12000 get_id = nullptr;
+};
+
+const CtxCalls& ctx_calls() {
+  static std::once_flag once;
+  static CtxCalls c;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      c.get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      c.get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  return c;
+}
+
+// Unique id of the calling thread's current context (0 if there is none
+// yet, or the driver cannot tell).
+unsigned long long current_ctx_id() {
+  const CtxCalls& c = ctx_calls();
+  if (!c.get_current || !c.get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (c.get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+  if (c.get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
 std::mutex g_mu;
-void* g_ws_addr[kMaxDevices];  // device address of g_static_ws, per device
+struct Cached {
+  unsigned long long ctx = 0;  // context the address belongs to (0: none cached)
+  void* addr = nullptr;
+};
+Cached g_ws[kMaxDevices];
 
 // Host code cannot use g_static_ws's address directly (on the host it names
-// a stand-in, not device memory), so look it up once per device, with that
-// device current, and cache it.
+// a stand-in, not device memory), so it is looked up with the device
+// current and cached.  The module, and so the address, belongs to one
+// context: the cache is keyed on the current context's unique id, and a new
+// context on the device (after cudaDeviceReset, or a driver-API context
+// made current by the caller) gets its own lookup.
 pa_status_t static_ws_address(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_ws_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_static_ws) != cudaSuccess || !p) return PA_ERR_CUDA;
-    g_ws_addr[dev] = p;
+  unsigned long long ctx = current_ctx_id();
+  if (ctx != 0 && g_ws[dev].ctx == ctx) {
+    *out = g_ws[dev].addr;
+    return PA_OK;
   }
-  *out = g_ws_addr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_static_ws) != cudaSuccess || !p) return PA_ERR_CUDA;
+  // the lookup makes the device's primary context current if nothing was
+  if (ctx == 0) ctx = current_ctx_id();
+  g_ws[dev].ctx = ctx;  // 0 when the id is unknown: looked up again next call
+  g_ws[dev].addr = p;
+  *out = p;
   return PA_OK;
 }
 

@@ -451,7 +451,30 @@ def pin_prefill_tiled_is_direct(orc):
         _close(tiled, direct, 1e-13, f"tiled prefill, tile {tile}")
 
 
+# --------------------------------------------------------------------------
+# the subset mode (rows=) the full-size tests and the CPU baseline use
+# --------------------------------------------------------------------------
+def pin_rows_subset(orc):
+    """Asking for a list of rows (any order, repeats allowed) gives exactly
+    those rows of the full output, bit for bit: the subset mode computes the
+    same rows, not different ones, and puts row r of the request at r."""
+    b = problem(dtype=torch.bfloat16, lens=(37, 1, 64, 20), Hq=6, Hkv=2, D=16, BS=8, seed=61)
+    full = _run(orc, b).reshape(-1, 16)
+    rows = [23, 0, 5, 5, 17, 6, 12, 1, 22]
+    sub = orc.decode(b.q, b.k_cache, b.v_cache, b.block_tables, b.seq_lens, b.scale, rows=rows)
+    assert sub.shape == (len(rows), 16), sub.shape
+    assert np.array_equal(sub, full[rows]), "decode rows= differs from the full output's rows"
+    pb = wl.make_prefill(wl.prefill_problem(dtype=torch.float16, ctx=(19, 0), new=(7, 5), Hq=4,
+                                            Hkv=2, D=8, BS=4, seed=62), poison=True)
+    fullp = _prefill(orc, pb).reshape(-1, 8)
+    rows = [47, 3, 3, 0, 28, 30, 11]
+    subp = _prefill(orc, pb, rows=rows)
+    assert subp.shape == (len(rows), 8), subp.shape
+    assert np.array_equal(subp, fullp[rows]), "prefill rows= differs from the full output's rows"
+
+
 ALL_PINS = [
+    pin_rows_subset,
     pin_prefill_brute_force,
     pin_prefill_one_token_is_decode,
     pin_prefill_no_context_is_causal,

@@ -190,6 +190,12 @@ def test_host_staging_size_and_checks(L):
     assert call(None, want) == pa.PA_ERR_INVALID_ARG
     assert call(ctypes.c_void_p(0x10008), want) == pa.PA_ERR_MISALIGNED
     assert call(ctypes.c_void_p(0x10000), want - 1) == pa.PA_ERR_WORKSPACE_TOO_SMALL
+    # misaligned caches are refused before the host-to-device copies are queued
+    odd = ctypes.c_void_p(0x10008)
+    for k, v in ((odd, fake), (fake, odd)):
+        assert L.pa_decode_host(ctypes.byref(p), fake, k, v, fake, fake, fake, 1 << 30,
+                                ctypes.c_void_p(0x10000), want, fake, None) == \
+            pa.PA_ERR_MISALIGNED
     # the offsets of the same layout (for a host mirror of it)
     off = pa.host_staging_offsets(p)
     assert off == (0, r(2 * 24 * 256 * 2), r(2 * 24 * 256 * 2) + r(2 * 6250 * 4),

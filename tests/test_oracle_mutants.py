@@ -38,6 +38,12 @@ MUTANTS = [
     ("phase2_first_max_only", "if (m[p] > gmax) gmax = m[p];", "gmax = m[0];"),
     ("rescale_sign", "const double wgt = exp(m[p] - gmax) * sp[p] / total;",
      "const double wgt = exp(gmax - m[p]) * sp[p] / total;"),
+    # subset mode: the requested rows are ignored, or placed in reverse order
+    ("rows_ignored", "const int64_t row = rows ? rows[r] : r;\n    const int b = (int)(row",
+     "const int64_t row = r;\n    const int b = (int)(row"),
+    ("prefill_rows_reversed",
+     "const int64_t row = rows ? rows[r] : r;\n    const int64_t t = row",
+     "const int64_t row = rows ? rows[n - 1 - r] : r;\n    const int64_t t = row"),
     # paged prefix prefill
     ("prefill_causal_exclusive", "const int64_t nvis = (int64_t)C + (t - qs) + 1;",
      "const int64_t nvis = (int64_t)C + (t - qs);"),

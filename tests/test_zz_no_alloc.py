@@ -4,22 +4,27 @@ Some callers cannot allocate device memory where they decode (a plugin of a
 host runtime that owns every device allocation, a C program without an
 allocator, a real-time loop that must not stall on one).  For them
 pa_decode_v2_static runs V2 with a fixed workspace the library keeps in
-device memory.  This file checks, through the C ABI, that it gives the same
-output as pa_decode_v2 with a caller-provided workspace, on two calls in a
-row (the second call sees whatever the first left in the shared array), and
-that oversized parameters are refused before anything runs.
+device memory.  This file checks, through the C ABI, that on two calls in a
+row (the second call sees whatever the first left in the shared array) its
+output matches the float64 oracle on NaN-poisoned inputs, and pa_decode_v2
+with a caller-provided workspace, within the parity tolerance; that a block
+id outside the pool turns exactly that sequence's rows into NaN; and that
+oversized parameters are refused before anything runs.
 
 The file is named to be collected last, so a run that stops at the first
 failure has already run every other test; it also passes on its own.
 """
 import ctypes
 
+import numpy as np
 import pytest
 import torch
 
+import oracle
 import paged_attention_decode_v2_gb300 as pa
 from paged_attention_decode_v2_gb300 import workloads as wl
 from gpu_helpers import TOL, max_err
+from oracle_pins import problem
 
 pytestmark = pytest.mark.gpu
 
@@ -44,25 +49,50 @@ def _reference_v2(b, P):
     return out
 
 
-def test_static_workspace_matches_decode_v2_on_two_calls():
+def test_static_workspace_matches_oracle_and_decode_v2_on_two_calls():
     from paged_attention_decode_v2_gb300 import build
     build.build()
     assert torch.cuda.is_available()
     # two different batches: the second call runs on what the first left behind
     batches = [
-        (wl.make(wl.scaled(wl.WORKLOADS["mixed_32"], num_seqs=6, max_len=20000), device="cuda",
-                 poison=True), 512),
-        (wl.make(wl.scaled(wl.WORKLOADS["gqa_8k"], seq_len=12345), device="cuda", poison=True),
-         1024),
+        (wl.make(wl.scaled(wl.WORKLOADS["mixed_32"], num_seqs=6, max_len=20000), poison=True),
+         512),
+        (wl.make(wl.scaled(wl.WORKLOADS["gqa_8k"], seq_len=12345), poison=True), 1024),
     ]
-    for b, P in batches:
+    for bc, P in batches:
+        ref = oracle.decode(bc.q, bc.k_cache, bc.v_cache, bc.block_tables, bc.seq_lens,
+                            bc.scale)
+        b = bc.to("cuda")
         want = _reference_v2(b, P)
         got = torch.full(tuple(b.q.shape), float("nan"), dtype=torch.float32, device="cuda")
         assert _call_static(b, got, P) == pa.PA_OK
         torch.cuda.synchronize()
-        assert torch.isfinite(got).all().item()
-        err = max_err(got.double().cpu().numpy(), want.double().cpu().numpy())
+        g = got.double().cpu().numpy()
+        assert np.all(np.isfinite(g))
+        err = max_err(g, ref)
+        assert err <= TOL[b.q.dtype], f"static workspace differs from the oracle by {err}"
+        err = max_err(g, want.double().cpu().numpy())
         assert err <= TOL[b.q.dtype], f"static workspace differs from decode_v2 by {err}"
+
+
+def test_static_workspace_bad_block_id_gives_nan_rows():
+    """A block id outside the pool makes exactly that sequence's rows NaN
+    (the call reports no device status); the other rows match the oracle."""
+    lens = (900, 700, 1300)
+    good = problem(dtype=torch.bfloat16, lens=lens, Hq=8, Hkv=2, D=128, BS=16, seed=31)
+    ref = oracle.decode(good.q, good.k_cache, good.v_cache, good.block_tables, good.seq_lens,
+                        good.scale)
+    bad = problem(dtype=torch.bfloat16, lens=lens, Hq=8, Hkv=2, D=128, BS=16, seed=31)
+    bad.block_tables[1, 20] = bad.k_cache.shape[0] + 3      # token 320 of sequence 1
+    b = bad.to("cuda")
+    got = torch.zeros(tuple(b.q.shape), dtype=torch.float32, device="cuda")
+    assert _call_static(b, got, 256) == pa.PA_OK
+    torch.cuda.synchronize()
+    g = got.double().cpu().numpy()
+    assert np.all(np.isnan(g[1]))
+    for s in (0, 2):
+        assert np.all(np.isfinite(g[s]))
+        assert max_err(g[s], ref[s]) <= TOL[torch.bfloat16]
 
 
 def test_static_workspace_rejects_oversized_parameters():
