@@ -213,8 +213,16 @@ def run_ours(args, rank, world, device):
                             out_dtype=torch.float32)
     path = pa.decode_path(params) if args.path == "decode" else (1 if args.path == "v1" else 2)
     family = pa.decode_kernel(params)
+    # kernel launches of the step on this path (V2: one when pass 1 merges its
+    # own partials, two with the dependent reduce kernel)
+    launches_per_step = pa.decode_launches(pa.make_params(
+        batch.q, batch.k_cache, batch.block_tables, max_seq_len=batch.max_seq_len,
+        scale=batch.scale, partition_size=P, out_dtype=torch.float32,
+        v1_max_seq_len=max(batch.max_seq_len, 1) if path == 1 else 1))
+    one_launch_v2 = path == 2 and launches_per_step == 1
     kname = ("pa_tc_kernel" if family == 2 else "pa_generic_kernel") + \
-        (" (V2 pass 1)" if path == 2 else " (V1)")
+        (" (V2 in one launch: pass 1 + merge)" if one_launch_v2 else
+         " (V2 pass 1)" if path == 2 else " (V1)")
     ws = pa.alloc_workspace(params, device=device)
     out = torch.empty(tuple(batch.q.shape), dtype=torch.float32, device=device)
     flush_buf = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=device)
@@ -246,7 +254,6 @@ def run_ours(args, rank, world, device):
 
     kv_bytes = batch.kv_bytes()
     alg_bytes = kv_bytes + batch.q_bytes()
-    launches_per_step = 2 if path == 2 else 1
 
     sampler = ClockSampler(gpu_id_for_smi(device))
     if rank == 0:
@@ -275,9 +282,12 @@ def run_ours(args, rank, world, device):
         torch.distributed.barrier()
     t_end = time.time()
     step_ms = [a.elapsed_time(b) for a, b in ev]
+    out_step = out.clone()   # the step's result (the two-call form below rewrites out)
 
-    # ---- the dominant kernel alone (V2 pass 1), same region shape -----------
-    dom_ms, red_ms = [], []
+    # ---- the dominant kernel: the step itself when it is one launch; with two
+    # launches, V2 pass 1 alone.  The two-call form (pass 1, then the reduce)
+    # is timed for V2 either way, as context.
+    dom_ms, red_ms, p1_ms = [], [], []
     if path == 2:
         evp = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
         for i in range(args.steps):
@@ -289,10 +299,9 @@ def run_ours(args, rank, world, device):
             pa.decode_v2_reduce(params, batch.seq_lens, ws, out)
             evp[i][2].record(stream)
         torch.cuda.synchronize(device)
-        dom_ms = [e[0].elapsed_time(e[1]) for e in evp]
+        p1_ms = [e[0].elapsed_time(e[1]) for e in evp]
         red_ms = [e[1].elapsed_time(e[2]) for e in evp]
-    else:
-        dom_ms = step_ms
+    dom_ms = p1_ms if (path == 2 and not one_launch_v2) else step_ms
     t_dom_end = time.time()
 
     # ---- end to end through the C ABI with host buffers ---------------------
@@ -324,16 +333,18 @@ def run_ours(args, rank, world, device):
                        params=hparams, stream=stream)
         if i >= args.warmup:
             e2e_s.append(time.perf_counter() - t0)
-    assert torch.equal(out_h, out.cpu()), "host-buffer step differs from the device step"
+    assert torch.equal(out_h, out_step.cpu()), "host-buffer step differs from the device step"
     h2d = q_h.numel() * q_h.element_size() + bt_h.numel() * 4 + sl_h.numel() * 4
     d2h = out_h.numel() * out_h.element_size()
 
     # ---- the end-to-end step taken apart ----------------------------------
-    # The same operations pa_decode_host enqueues (one copy of the mirrored
-    # inputs into the staging buffer, the decode on the staged inputs, the
-    # copy of the result back), issued one by one with stream events between
-    # them, then the host's wait: device time of each part, and the host time
-    # that is not device time (call overheads and the wait's wake-up).
+    # The operations pa_decode_host enqueues (one copy of the mirrored inputs
+    # into the staging buffer, the decode on the staged inputs, the copy of
+    # the result back), issued one by one with stream events between them
+    # while the GPU is still busy with a ~0.5 ms spin, so that every part is
+    # queued before the first starts and the events hold device time only.
+    # The rest of the end-to-end time (e2e minus the three parts) is host
+    # time: issuing the copies and the launch, and the wait's wake-up.
     offs = pa.host_staging_offsets(hparams)
     n_in = offs[2] + sl_h.numel() * 4
     mirror_u8 = mbuf[:n_in]
@@ -341,12 +352,11 @@ def run_ours(args, rank, world, device):
     bt_d = staging[offs[1]:offs[2]].view(torch.int32)[:bt_h.numel()].view(tuple(bt_h.shape))
     sl_d = staging[offs[2]:offs[3]].view(torch.int32)[:sl_h.numel()]
     out_d = staging[offs[3]:].view(out.dtype)[:out.numel()].view(tuple(out.shape))
-    parts = {"h2d": [], "step": [], "d2h": [], "host_not_device": []}
+    parts = {"h2d": [], "step": [], "d2h": []}
     for i in range(args.warmup + args.steps):
         flush.zero_()
-        torch.cuda.synchronize(device)
+        torch.cuda._sleep(1_000_000)
         e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-        t0 = time.perf_counter()
         e[0].record(stream)
         staging[:n_in].copy_(mirror_u8, non_blocking=True)
         e[1].record(stream)
@@ -357,20 +367,18 @@ def run_ours(args, rank, world, device):
         out_h.copy_(out_d, non_blocking=True)
         e[3].record(stream)
         torch.cuda.synchronize(device)
-        wall = time.perf_counter() - t0
         if i >= args.warmup:
             parts["h2d"].append(e[0].elapsed_time(e[1]))
             parts["step"].append(e[1].elapsed_time(e[2]))
             parts["d2h"].append(e[2].elapsed_time(e[3]))
-            parts["host_not_device"].append(wall * 1e3 - e[0].elapsed_time(e[3]))
-    assert torch.equal(out_h, out.cpu()), "the step taken apart differs from the device step"
+    assert torch.equal(out_h, out_step.cpu()), "the step taken apart differs from the device step"
     hold = hold_until_sampled(sampler, t_gpu0, step, device) if rank == 0 else 0
     t_gpu1 = time.time()
     if rank == 0:
         sampler.stop()
 
     assert pa.read_device_status(ws) == pa.PA_OK, "device status not OK after the bench"
-    assert torch.isfinite(out).all().item(), "non-finite output"
+    assert torch.isfinite(out_step).all().item(), "non-finite output"
 
     # reduce over ranks: max of times
     t_step, t_dom, t_e2e = max_over_ranks(
@@ -398,7 +406,9 @@ def run_ours(args, rank, world, device):
                         f"{w.num_heads} q / {w.num_kv_heads} kv heads, head_dim {w.head_dim}, "
                         f"{str(w.dtype).replace('torch.', '')} KV, block {w.block_size}",
             "partition_size": P,
-            "path": ("V2 (partition kernel + LSE reduce)" if path == 2 else "V1 single pass") +
+            "path": ("V2 in one launch (partition kernel merging its own partials)"
+                     if one_launch_v2 else
+                     "V2 (partition kernel + LSE reduce)" if path == 2 else "V1 single pass") +
                     (" via pa_decode" if args.path == "decode" else " forced"),
             "accumulate": "f32",
             "l2": (f"inputs larger than L2 (KV {kv_bytes / 1e6:.1f} MB > 129 MB), and a "
@@ -421,14 +431,20 @@ def run_ours(args, rank, world, device):
             "algorithmic_bytes_per_launch": alg_bytes,
             "launch_us": round(t_dom * 1e3, 3),
         },
-        "reduce_us": round(statistics.mean(red_ms) * 1e3, 3) if red_ms else None,
+        "two_call_form_us": ({"pass1": round(statistics.mean(p1_ms) * 1e3, 3),
+                              "reduce": round(statistics.mean(red_ms) * 1e3, 3)}
+                             if red_ms else None),
         "e2e": {"value": round(t_e2e * 1e3, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
-                "parts_us": {k: round(statistics.mean(v) * 1e3, 3) for k, v in parts.items()},
-                "parts_how": "the operations of pa_decode_host issued one by one with stream "
-                             "events between them: h2d = one copy of the pinned mirrored inputs, "
-                             "step = pa_decode on the staged inputs, d2h = the result back, "
-                             "host_not_device = host wall time minus the events' span"},
+                "parts_us": dict(
+                    {k: round(statistics.mean(v) * 1e3, 3) for k, v in parts.items()},
+                    host=round(t_e2e * 1e3 - sum(statistics.mean(v) * 1e3
+                                                 for v in parts.values()), 3)),
+                "parts_how": "device time of the operations of pa_decode_host queued one by one "
+                             "behind a GPU spin with stream events between them: h2d = one copy "
+                             "of the pinned mirrored inputs, step = pa_decode on the staged "
+                             "inputs, d2h = the result back; host = e2e minus the three "
+                             "(issuing the copies and launch, the wait's wake-up)"},
         "gpu_launches": launches_per_step * args.steps,
     }
     if rank == 0:

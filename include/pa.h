@@ -72,7 +72,8 @@ typedef enum pa_status {
   PA_ERR_CUDA = 5,                /* a CUDA launch or copy failed             */
   PA_ERR_DEVICE_TIMEOUT = 6,      /* device status: a bounded wait gave up    */
   PA_ERR_BAD_BLOCK_ID = 7,        /* device status: block id outside the pool */
-  PA_ERR_BAD_SEQ_LEN = 8          /* device status: seq_len outside 0..max    */
+  PA_ERR_BAD_SEQ_LEN = 8,         /* device status: seq_len outside 0..max    */
+  PA_ERR_WORKSPACE_NOT_INIT = 9   /* device status: pa_workspace_init missing */
 } pa_status_t;
 
 typedef enum pa_dtype { PA_F32 = 0, PA_BF16 = 1, PA_F16 = 2 } pa_dtype_t;
@@ -128,19 +129,28 @@ typedef struct pa_params {
  *
  * Workspace (V2 only), NP = ceil(max_seq_len / partition_size), each region
  * starting on a 256-byte boundary, in this order:
- *   status       int32 word at offset 0 (then padding to 256 bytes)
+ *   control      1024 bytes (PA_WORKSPACE_CONTROL_BYTES), whatever the
+ *                parameters: the int32 status word at offset 0, an
+ *                initialisation marker at offset 4, and from offset 256 the
+ *                counters of the one-launch V2 step
  *   max_logits   float32 [num_seqs, num_heads, NP]   m_p, natural-log units
  *   exp_sums     float32 [num_seqs, num_heads, NP]   s_p = sum exp(l_t - m_p)
  *   tmp_output   float32 [num_seqs, num_heads, NP, head_dim]
  *                o_p = sum exp(l_t - m_p) V_t / s_p
  * Only partitions p < ceil(seq_lens[b] / P) are written or read; the rest
- * may hold anything.  After pa_decode_v2 (not pa_decode_v2_partitions) a
- * sequence with a single partition has no partials in the workspace.
+ * may hold anything.  pa_decode_v2_partitions leaves every partition's
+ * partials as defined above.  After pa_decode_v2 a sequence with a single
+ * partition has no partials in the workspace.
+ * The control block must be initialised once, by pa_workspace_init, before
+ * the first V2 call; every V2 call leaves it ready for the next one, with
+ * any parameters.
  */
+#define PA_WORKSPACE_CONTROL_BYTES ((size_t)1024)
 
 /* Bytes of workspace pa_decode_v2 / pa_decode need for these parameters
- * (0 if the parameters are invalid).  Depends only on num_seqs, num_heads,
- * head_dim, max_seq_len and partition_size. */
+ * (0 if the parameters are invalid): the control block plus the partials.
+ * Depends only on num_seqs, num_heads, head_dim, max_seq_len and
+ * partition_size. */
 PA_API size_t pa_workspace_size(const pa_params_t* params);
 
 /*
@@ -155,11 +165,25 @@ PA_API pa_status_t pa_decode_v1(const pa_params_t* params, const void* q, const 
                          const int32_t* seq_lens, void* out, cudaStream_t stream);
 
 /*
- * V2: split-KV in two kernels.  Pass 1 runs one CTA per (sequence, KV-head
- * group, partition of partition_size tokens) and writes max_logits,
- * exp_sums and tmp_output into the workspace; pass 2 combines a row's
- * partitions with weights exp(m_p - max_p m_p) * s_p and writes `out`.
- * `workspace` must hold pa_workspace_size(params) bytes.
+ * V2: split-KV.  Pass 1 runs per (sequence, KV-head group, partition of
+ * partition_size tokens) and writes max_logits, exp_sums and tmp_output into
+ * the workspace; pass 2 combines a row's partitions with weights
+ * exp(m_p - max_p m_p) * s_p and writes `out`.
+ * `workspace` must hold pa_workspace_size(params) bytes, its control block
+ * initialised by pa_workspace_init.
+ * One launch: when the tensor-core kernel runs as a persistent grid with at
+ * least one CTA per reduce unit (num_seqs * num_heads * head_dim / 32 units:
+ * few long sequences, e.g. one 100K-token sequence), pass 2 runs in the same
+ * launch.  Each CTA, after its partitions, counts itself finished in the
+ * workspace; CTAs that finish once every CTA of the grid has started take
+ * reduce units and run them when all are finished (no cooperative launch
+ * and no wait on a CTA that has not started; the order of every sum is
+ * fixed, so results are bit-identical from run to run).  Other batches and
+ * the CUDA-core path use two kernels, pass 2 launched as a programmatic
+ * dependent of pass 1 (pa_decode_launches() tells which).  In a workspace
+ * that pa_workspace_init never initialised the one-launch step reduces
+ * nothing: the status word reads PA_ERR_WORKSPACE_NOT_INIT and the rows of
+ * sequences longer than one partition are NaN.
  * The V1 / V2 choice is also made per sequence inside the pass-1 launch: a
  * sequence of 1..partition_size tokens has a single partition, so pass 1
  * writes its normalised result straight into `out` (V1's contract), writes
@@ -281,6 +305,12 @@ PA_API pa_status_t pa_decode_host(const pa_params_t* params, const void* q_host,
  * the parameters are invalid.  Pure host function. */
 PA_API int pa_decode_path(const pa_params_t* params);
 
+/* Kernel launches one pa_decode call makes for these parameters on the
+ * current device: 1 (V1, or V2 in one launch), 2 (V2 as pass 1 and a
+ * dependent pass 2), 0 for invalid parameters or an empty batch.  Host
+ * function; it queries the current device like pa_decode_kernel. */
+PA_API int pa_decode_launches(const pa_params_t* params);
+
 /* Which kernels the decode calls use for these parameters on the current
  * device: 2 = tensor-core kernels (TMA + tcgen05; bf16 / f16 caches, at most
  * 8 query heads per KV head, head_dim 128 or 256 with block_size 16 or 32,
@@ -292,8 +322,11 @@ PA_API int pa_decode_kernel(const pa_params_t* params);
 /* Static description of a status code (never NULL). */
 PA_API const char* pa_status_string(pa_status_t status);
 
-/* Zero the workspace's status word (enqueued on `stream`).  Call once after
- * allocating a workspace; device errors then accumulate in it until read. */
+/* Initialise the workspace's control block (enqueued on `stream`): zero the
+ * status word and the arrival counters and write the initialisation marker
+ * (the first min(workspace_bytes, PA_WORKSPACE_CONTROL_BYTES) bytes).  Call
+ * once after allocating a workspace, before its first V2 call; device
+ * errors then accumulate in the status word until read. */
 PA_API pa_status_t pa_workspace_init(void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* Diagnostic: copy the status word to *status (PA_OK or the last device

@@ -29,6 +29,7 @@ PA_ERR_CUDA = 5
 PA_ERR_DEVICE_TIMEOUT = 6
 PA_ERR_BAD_BLOCK_ID = 7
 PA_ERR_BAD_SEQ_LEN = 8
+PA_ERR_WORKSPACE_NOT_INIT = 9
 
 PA_F32, PA_BF16, PA_F16 = 0, 1, 2
 PA_FLAG_PORTABLE = 1
@@ -41,7 +42,7 @@ EXPORTS = ("pa_workspace_size", "pa_decode_v1", "pa_decode_v2", "pa_decode_v2_pa
            "pa_decode_v2_reduce", "pa_decode", "pa_decode_path", "pa_status_string",
            "pa_workspace_init", "pa_read_device_status", "pa_version", "pa_decode_v2_static",
            "pa_decode_kernel", "pa_host_staging_size", "pa_host_staging_offsets",
-           "pa_decode_host", "pa_prefill")
+           "pa_decode_host", "pa_prefill", "pa_decode_launches")
 PA_STATIC_WORKSPACE_BYTES = 16 << 20
 
 
@@ -121,6 +122,8 @@ def lib() -> ctypes.CDLL:
             L.pa_decode.restype = ctypes.c_int
             L.pa_decode_kernel.argtypes = [PP]
             L.pa_decode_kernel.restype = ctypes.c_int
+            L.pa_decode_launches.argtypes = [PP]
+            L.pa_decode_launches.restype = ctypes.c_int
             L.pa_decode_path.argtypes = [PP]
             L.pa_decode_path.restype = ctypes.c_int
             L.pa_status_string.argtypes = [ctypes.c_int]
@@ -199,6 +202,11 @@ def decode_path(params: Params) -> int:
 def decode_kernel(params: Params) -> int:
     """2: tensor-core kernels, 1: CUDA-core kernels, 0: invalid parameters."""
     return int(lib().pa_decode_kernel(ctypes.byref(params)))
+
+
+def decode_launches(params: Params) -> int:
+    """Kernel launches one ``pa_decode`` call makes (1 or 2; 0 if invalid)."""
+    return int(lib().pa_decode_launches(ctypes.byref(params)))
 
 
 def _stream(stream):
@@ -404,7 +412,7 @@ def decode_host(q, k_cache, v_cache, block_tables, seq_lens, out, workspace, sta
 
 def alloc_workspace(params: Params, device=None):
     """A CUDA uint8 tensor sized for ``params`` (allocated by torch), with its
-    status word zeroed."""
+    control block initialised by :func:`workspace_init`."""
     import torch
     n = workspace_size(params)
     if n == 0:

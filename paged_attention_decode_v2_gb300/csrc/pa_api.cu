@@ -110,7 +110,7 @@ WorkspaceLayout workspace_layout(int64_t num_seqs, int64_t num_heads, int64_t he
                                  int64_t np) {
   WorkspaceLayout w;
   const size_t rows = static_cast<size_t>(num_seqs) * static_cast<size_t>(num_heads);
-  w.max_logits_off = kAlign;  // the status word owns the first 256 bytes
+  w.max_logits_off = kCtrlBytes;  // the control block comes first
   w.exp_sums_off = w.max_logits_off + round_up(rows * np * sizeof(float));
   w.tmp_out_off = w.exp_sums_off + round_up(rows * np * sizeof(float));
   w.total = w.tmp_out_off + round_up(rows * np * head_dim * sizeof(float));
@@ -183,6 +183,15 @@ pa_status_t prepare_v2(const pa_params_t* p, const void* q, const void* k, const
   return PA_OK;
 }
 
+// Whether the V2 step runs as one launch (the pass-1 grid running pass 2
+// itself): the tensor-core kernel serves these parameters as a persistent
+// grid with at least one CTA per reduce unit (pa_internal.h).
+bool one_launch_v2(const pa_params_t* p, int64_t np) {
+  if (!tc_applicable(p)) return false;
+  return one_launch_plan(p->num_seqs, p->num_heads, p->num_kv_heads, p->head_dim, np,
+                         sm100_num_sms());
+}
+
 }  // namespace
 
 extern "C" {
@@ -198,6 +207,11 @@ pa_status_t pa_decode_v2(const pa_params_t* p, const void* q, const void* k_cach
   // per-sequence choice inside the one pass-1 launch: sequences that fit one
   // partition are finished there, the rest are split and reduced
   a.single_direct = 1;
+  if (one_launch_v2(p, a.num_partitions)) {
+    // pass 2 runs in the pass-1 grid: one launch
+    a.fused = 1;
+    return launch_pass(p, a, true, stream) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  }
   if (launch_pass(p, a, true, stream) != cudaSuccess) return PA_ERR_CUDA;
   if (launch_reduce(a, stream, true) != cudaSuccess) return PA_ERR_CUDA;
   return PA_OK;
@@ -237,6 +251,14 @@ pa_status_t pa_decode(const pa_params_t* p, const void* q, const void* k_cache,
   return pa_decode_v1(p, q, k_cache, v_cache, block_tables, seq_lens, out, stream);
 }
 
+int pa_decode_launches(const pa_params_t* p) {
+  if (check_params(p, false) != PA_OK) return 0;
+  if (p->num_seqs == 0) return 0;
+  if (p->max_seq_len <= threshold(p)) return 1;
+  if (check_params(p, true) != PA_OK) return 0;
+  return one_launch_v2(p, num_partitions(p)) ? 1 : 2;
+}
+
 int pa_decode_kernel(const pa_params_t* p) {
   if (check_params(p, false) != PA_OK) return 0;
   return tc_applicable(p) ? 2 : 1;
@@ -253,6 +275,7 @@ const char* pa_status_string(pa_status_t s) {
     case PA_ERR_DEVICE_TIMEOUT: return "device wait timed out";
     case PA_ERR_BAD_BLOCK_ID: return "block id outside the pool";
     case PA_ERR_BAD_SEQ_LEN: return "sequence length outside 0..max_seq_len";
+    case PA_ERR_WORKSPACE_NOT_INIT: return "workspace not initialised (pa_workspace_init)";
   }
   return "unknown status";
 }
@@ -260,7 +283,12 @@ const char* pa_status_string(pa_status_t s) {
 pa_status_t pa_workspace_init(void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   if (!workspace || workspace_bytes < sizeof(int32_t)) return PA_ERR_INVALID_ARG;
   if (!aligned(workspace, kAlign)) return PA_ERR_MISALIGNED;
-  if (cudaMemsetAsync(workspace, 0, sizeof(int32_t), stream) != cudaSuccess) return PA_ERR_CUDA;
+  const size_t n = workspace_bytes < kCtrlBytes ? workspace_bytes : kCtrlBytes;
+  if (cudaMemsetAsync(workspace, 0, n, stream) != cudaSuccess) return PA_ERR_CUDA;
+  if (n >= kMarkerOffset + 4 &&
+      cudaMemsetAsync(static_cast<char*>(workspace) + kMarkerOffset, kMarkerByte, 4, stream) !=
+          cudaSuccess)
+    return PA_ERR_CUDA;
   return PA_OK;
 }
 

@@ -85,6 +85,22 @@ __device__ __forceinline__ void store_out(void* out, int64_t i, int32_t dtype, f
     static_cast<__half*>(out)[i] = __float2half_rn(v);
 }
 
+// Store 4 consecutive output elements starting at element i (a multiple of
+// 4) in the requested output type.
+__device__ __forceinline__ void store_out4(void* out, int64_t i, int32_t dtype, float4 v) {
+  if (dtype == PA_F32) {
+    *reinterpret_cast<float4*>(static_cast<float*>(out) + i) = v;
+  } else if (dtype == PA_BF16) {
+    __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + i) =
+        make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
+  } else {
+    __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + i) =
+        make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
+  }
+}
+
 // Store 16 consecutive output elements starting at element i (a multiple of
 // 16; the output 16-byte aligned) in the requested output type.
 __device__ __forceinline__ void store_row16(void* out, int64_t i, int32_t dtype,

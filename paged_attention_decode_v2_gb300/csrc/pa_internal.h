@@ -41,7 +41,50 @@ struct KernelArgs {
   int32_t single_direct;   // V2 pass 1 + reduce in one call: a sequence of at most
                            // partition_size tokens is finished by pass 1 (written
                            // straight into out) and the reduce skips its rows
+  int32_t fused;           // V2 in one launch: the pass-1 grid runs pass 2 itself
+                           // after its streaming (pa_grid_reduce.cuh)
 };
+
+// The workspace starts with a control block of fixed size: the status word,
+// an initialisation marker, and the words of the one-launch V2 step (start
+// counter, finished counters, reduce-unit queue).  It sits at the same place
+// with the same size whatever the parameters; pa_workspace_init zeroes it and
+// writes the marker, and a one-launch V2 step run on a workspace without the
+// marker merges nothing: it reports PA_ERR_WORKSPACE_NOT_INIT and the rows it
+// would have reduced become NaN.
+constexpr size_t kCtrlBytes = PA_WORKSPACE_CONTROL_BYTES;
+constexpr size_t kMarkerOffset = 4;
+constexpr size_t kSyncOffset = 256;
+constexpr int kMarkerByte = 0x5A;
+constexpr int32_t kMarker = 0x5A5A5A5A;
+
+// Persistent grid of the tensor-core pass-1 kernel for `items` work items
+// (0 when there are fewer items than SMs: the one-CTA-per-SM shape runs
+// instead).  At most two CTAs per SM; with a dense item walk (`compact`
+// false) the grid is sized so every CTA does the same number of rounds.
+inline int64_t tc_persistent_grid(int64_t items, bool compact, int num_sms) {
+  if (items < num_sms) return 0;
+  const int64_t slots = static_cast<int64_t>(num_sms) * 2;
+  int64_t grid = items < slots ? items : slots;
+  if (!compact && items > slots) {
+    const int64_t rounds = (items + slots - 1) / slots;
+    grid = (items + rounds - 1) / rounds;
+  }
+  return grid;
+}
+
+// Whether the V2 step runs as one launch: the persistent tensor-core grid
+// takes at most one reduce unit (query row x 32 elements of head_dim) per
+// CTA, so its own CTAs run pass 2 in one round after their streaming; other
+// batches use the dependent reduce kernel, which has more CTAs in flight.
+inline bool one_launch_plan(int64_t num_seqs, int64_t num_heads, int64_t num_kv_heads,
+                            int64_t head_dim, int64_t np, int num_sms) {
+  const int64_t items = num_seqs * num_kv_heads * np;
+  const bool compact = num_seqs > 1 && num_seqs <= 1024;  // the kernel's compact work list
+  const int64_t grid = tc_persistent_grid(items, compact, num_sms);
+  // a unit holds the statistics of up to 4096 partitions
+  return grid > 0 && np <= 4096 && num_seqs * num_heads * (head_dim / 32) <= grid;
+}
 
 // Everything the prefill kernel needs besides its tensor maps (pa_prefill.cuh).
 struct PrefillArgs {

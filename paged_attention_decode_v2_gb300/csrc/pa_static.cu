@@ -12,9 +12,12 @@
 // The array below lives in the library's device image: every GPU on which
 // libpa.so's code is loaded holds PA_STATIC_WORKSPACE_BYTES of device memory
 // for it until the process exits.  All calls on a device share it and it
-// keeps whatever the last call left there; V2 only reads back what the same
-// call wrote, so nothing in it has to start at zero.  Two calls that overlap
-// on the GPU (different streams, or different host threads, without ordering
+// keeps whatever the last call left there.  V2 only reads back the partials
+// the same call wrote; the one part that must be initialised is the control
+// block (the counters of the one-launch step), which the first call in a
+// context initialises on its stream and every launch leaves ready for the
+// next.  Two calls that overlap on the
+// GPU (different streams, or different host threads, without ordering
 // between them) race on it: order them on one stream.
 #include <mutex>
 
@@ -81,8 +84,10 @@ Cached g_ws[kMaxDevices];
 // current and cached.  The module, and so the address, belongs to one
 // context: the cache is keyed on the current context's unique id, and a new
 // context on the device (after cudaDeviceReset, or a driver-API context
-// made current by the caller) gets its own lookup.
-pa_status_t static_ws_address(void** out) {
+// made current by the caller) gets its own lookup.  With each lookup the
+// control block (status word, marker and counters) is initialised on
+// `stream`, as pa_workspace_init does for a caller's workspace.
+pa_status_t static_ws_address(void** out, cudaStream_t stream) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_mu);
@@ -93,6 +98,7 @@ pa_status_t static_ws_address(void** out) {
   }
   void* p = nullptr;
   if (cudaGetSymbolAddress(&p, g_static_ws) != cudaSuccess || !p) return PA_ERR_CUDA;
+  if (pa_workspace_init(p, pa::kCtrlBytes, stream) != PA_OK) return PA_ERR_CUDA;
   // the lookup makes the device's primary context current if nothing was
   if (ctx == 0) ctx = current_ctx_id();
   g_ws[dev].ctx = ctx;  // 0 when the id is unknown: looked up again next call
@@ -114,7 +120,7 @@ extern "C" pa_status_t pa_decode_v2_static(const pa_params_t* params, const void
   if (need > PA_STATIC_WORKSPACE_BYTES) return PA_ERR_WORKSPACE_TOO_SMALL;
   if (params->num_seqs == 0) return PA_OK;
   void* ws = nullptr;
-  const pa_status_t st = static_ws_address(&ws);
+  const pa_status_t st = static_ws_address(&ws, stream);
   if (st != PA_OK) return st;
   return pa_decode_v2(params, q, k_cache, v_cache, block_tables, seq_lens, ws,
                       PA_STATIC_WORKSPACE_BYTES, out, stream);

@@ -52,6 +52,7 @@
 #include <cuda.h>
 
 #include "pa_device.cuh"
+#include "pa_grid_reduce.cuh"
 #include "pa_sm100.cuh"
 
 namespace pa {
@@ -104,9 +105,12 @@ struct Ctrl {
   uint64_t drain;              // abort path: all issued MMAs finished
   uint64_t never;              // self-test: nothing ever arrives here
   uint64_t comb_ready;         // cluster: every CTA's partial sums have landed here
+  uint64_t red_bar;            // one-launch V2: a reduce unit's tile of partials landed
   int64_t total_items;         // work items to enumerate
   uint32_t tmem;
   int abort;                   // some wait gave up
+  int ws_ok;                   // one-launch V2: the workspace carries the init marker
+  int red_word[3];             // one-launch V2: thread 0's broadcasts in the reduce
   int scan[8];                 // per-warp totals of the work-list scan
   float red[2][4][8];          // cross-warp max / sum of the softmax warps
 };
@@ -115,6 +119,7 @@ static_assert(sizeof(Ctrl) <= 1024, "control block");
 // One work item, decoded the same way by every role.
 struct Item {
   int b, kvh, part;
+  int32_t L;       // the sequence's length
   int32_t t0, t1;  // this CTA's token range; empty when t0 >= t1
   bool len_ok;     // 0 <= seq_len <= max_seq_len
   bool any;        // the item's whole range (over all CTAs of a cluster) has tokens
@@ -150,6 +155,7 @@ __device__ __forceinline__ Item item_coords(const KernelArgs& a, const int32_t* 
   }
   it.t0 = v2 ? it.part * a.partition_size : 0;
   it.t1 = it.t0;
+  it.L = 0;
   it.len_ok = false;
   it.any = false;
   it.direct = false;
@@ -161,6 +167,7 @@ __device__ __forceinline__ Item item_coords(const KernelArgs& a, const int32_t* 
 // the range's 128-token tiles (the whole range when cs == 1).
 __device__ __forceinline__ void item_range(const KernelArgs& a, Item& it, int32_t L, bool v2,
                                            int rank, int cs) {
+  it.L = L;
   it.len_ok = seq_len_ok(a, L);
   it.t1 = !it.len_ok ? it.t0 : (v2 ? min(L, it.t0 + a.partition_size) : L);
   it.any = it.t0 < it.t1;
@@ -205,7 +212,8 @@ template <typename T, int D, int BS, bool kV2, int NST, int CPS>
 __global__ void __launch_bounds__(tc::kThreads, CPS)
     pa_tc_kernel(const KernelArgs a, const __grid_constant__ CUtensorMap kmap,
                  const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap qmap,
-                 int64_t grid_items, int compact, int cluster, long long budget) {
+                 const __grid_constant__ CUtensorMap pmap, int64_t grid_items, int compact,
+                 int cluster, long long budget) {
   using namespace tc;
   using Lay = Layout<D, NST>;
   static_assert(D == 128 || D == 256, "head_dim");
@@ -251,6 +259,7 @@ __global__ void __launch_bounds__(tc::kThreads, CPS)
   }
 
   // ---- set-up -----------------------------------------------------------------
+  unsigned long long started = 0;  // thread 0, one-launch V2: the start word as it was
   if (tid == 0) {
     for (int s = 0; s < NST; ++s) {
       sm100::mbar_init(&c.full[s], 1);
@@ -268,12 +277,23 @@ __global__ void __launch_bounds__(tc::kThreads, CPS)
     sm100::mbar_init(&c.never, 1);
     if (kClusters) sm100::mbar_init(&c.comb_ready, 1);
     c.abort = 0;
+    // one-launch V2: the counters are usable only in an initialised workspace;
+    // the CTA counts itself started (the result is first used at the end)
+    if (kV2 && a.fused) {
+      sm100::mbar_init(&c.red_bar, 1);
+      c.ws_ok = __ldcg(a.status + kMarkerOffset / 4) == kMarker;
+      if (c.ws_ok)
+        started = gridred::count_started(a);
+      else
+        set_status(a.status, PA_ERR_WORKSPACE_NOT_INIT);
+    }
   }
   if (warp == 5) {
     sm100::tmem_alloc(&c.tmem, kTmemCols);
     sm100::tmem_relinquish();
   }
   if (warp == 4 && lane == 0) {
+    if (kV2 && a.fused) sm100::tma_prefetch_desc(&pmap);
     sm100::tma_prefetch_desc(&kmap);
     sm100::tma_prefetch_desc(&vmap);
     sm100::tma_prefetch_desc(&qmap);
@@ -844,6 +864,13 @@ __global__ void __launch_bounds__(tc::kThreads, CPS)
   __syncthreads();
   sm100::tc_fence_after();
   if (warp == 5) sm100::tmem_dealloc(tmem, kTmemCols);
+  // one-launch V2 (persistent shape only): pass 2 by this grid, once every
+  // CTA has stored its partials; the ring is free scratch now
+  static_assert(sizeof(gridred::UnitScratch) <= NST * kStageBytes, "reduce scratch in the ring");
+  if (kV2 && !kClusters && a.fused)
+    gridred::grid_reduce<D>(a, c.ws_ok != 0, started, c.red_word,
+                            *reinterpret_cast<gridred::UnitScratch*>(ring), &pmap, &c.red_bar, tid,
+                            budget);
   // no CTA leaves while a peer may still read its shared memory
   if (cs > 1) sm100::cluster_sync_all();
 }
@@ -866,8 +893,8 @@ cudaError_t configure_tc(int dev) {
 
 template <typename T, int D, int BS, bool V2, int NST, int CPS>
 cudaError_t launch_tc_variant(const KernelArgs& a, const CUtensorMap& km, const CUtensorMap& vm,
-                              const CUtensorMap& qm, int64_t items, unsigned grid, int compact,
-                              int cs, cudaStream_t s) {
+                              const CUtensorMap& qm, const CUtensorMap& pm, int64_t items,
+                              unsigned grid, int compact, int cs, cudaStream_t s) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
   auto kern = pa_tc_kernel<T, D, BS, V2, NST, CPS>;
@@ -889,7 +916,7 @@ cudaError_t launch_tc_variant(const KernelArgs& a, const CUtensorMap& km, const 
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = cs > 1 ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kern, a, km, vm, qm, items, compact, cs, budget);
+  return cudaLaunchKernelEx(&cfg, kern, a, km, vm, qm, pm, items, compact, cs, budget);
 }
 
 // Largest cluster size <= want (a power of two) of which at least `need`
@@ -935,13 +962,15 @@ int fit_cluster(int want, int64_t need) {
 
 template <typename T, int D, int BS>
 cudaError_t launch_tc_t(const KernelArgs& a, const CUtensorMap& km, const CUtensorMap& vm,
-                        const CUtensorMap& qm, bool v2, int num_sms, cudaStream_t s) {
+                        const CUtensorMap& qm, const CUtensorMap& pm, bool v2, int num_sms,
+                        cudaStream_t s) {
   // upper bound of the work items: every (sequence, KV head[, partition])
   const int64_t items = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads *
                         (v2 ? a.num_partitions : 1);
   if (items == 0) return cudaSuccess;
   const int compact = (v2 && a.num_seqs > 1 && a.num_seqs <= tc::kMaxCompactSeqs) ? 1 : 0;
-  if (items < num_sms) {
+  const int64_t persistent = tc_persistent_grid(items, compact != 0, num_sms);
+  if (persistent == 0) {
     // Few items: one deep-ring CTA per SM, and when at most half the SMs
     // would be busy, each item is shared by a cluster of cs CTAs (up to 16)
     // that split its 128-token tiles and merge their partial results -- as
@@ -955,38 +984,31 @@ cudaError_t launch_tc_t(const KernelArgs& a, const CUtensorMap& km, const CUtens
                                   : fit_cluster<T, D, BS, false>(want, items))
                             : 1;
     const unsigned grid = static_cast<unsigned>(items * cs);
-    return v2 ? launch_tc_variant<T, D, BS, true, tc::kDeepStages, 1>(a, km, vm, qm, items, grid, compact, cs, s)
-              : launch_tc_variant<T, D, BS, false, tc::kDeepStages, 1>(a, km, vm, qm, items, grid, compact, cs,
+    return v2 ? launch_tc_variant<T, D, BS, true, tc::kDeepStages, 1>(a, km, vm, qm, pm, items, grid, compact, cs, s)
+              : launch_tc_variant<T, D, BS, false, tc::kDeepStages, 1>(a, km, vm, qm, pm, items, grid, compact, cs,
                                                           s);
   }
-  // Persistent grid: at most two CTAs per SM.  When the items are all the
-  // same size (not a compact work list) the grid is sized so every CTA does
-  // the same number of rounds, e.g. 392 items -> 196 CTAs x 2 rounds instead
-  // of 304 CTAs of which only 88 do a second round.
-  const int64_t slots = static_cast<int64_t>(num_sms) * 2;
-  int64_t grid64 = items < slots ? items : slots;
-  if (!compact && items > slots) {
-    const int64_t rounds = (items + slots - 1) / slots;
-    grid64 = (items + rounds - 1) / rounds;
-  }
-  const unsigned grid = static_cast<unsigned>(grid64);
-  return v2 ? launch_tc_variant<T, D, BS, true, 5, 2>(a, km, vm, qm, items, grid, compact, 1, s)
-            : launch_tc_variant<T, D, BS, false, 5, 2>(a, km, vm, qm, items, grid, compact, 1, s);
+  // Persistent grid: at most two CTAs per SM, every CTA doing the same number
+  // of rounds when the items are all the same size (tc_persistent_grid).
+  const unsigned grid = static_cast<unsigned>(persistent);
+  return v2 ? launch_tc_variant<T, D, BS, true, 5, 2>(a, km, vm, qm, pm, items, grid, compact, 1, s)
+            : launch_tc_variant<T, D, BS, false, 5, 2>(a, km, vm, qm, pm, items, grid, compact, 1, s);
 }
 
 template <typename T>
 cudaError_t launch_tc_dtype(const KernelArgs& a, const CUtensorMap& km, const CUtensorMap& vm,
-                            const CUtensorMap& qm, bool v2, int num_sms, cudaStream_t s) {
+                            const CUtensorMap& qm, const CUtensorMap& pm, bool v2, int num_sms,
+                            cudaStream_t s) {
   if (a.head_dim == 256 && a.block_size == 16)
-    return launch_tc_t<T, 256, 16>(a, km, vm, qm, v2, num_sms, s);
+    return launch_tc_t<T, 256, 16>(a, km, vm, qm, pm, v2, num_sms, s);
   if (a.head_dim == 256 && a.block_size == 32)
-    return launch_tc_t<T, 256, 32>(a, km, vm, qm, v2, num_sms, s);
+    return launch_tc_t<T, 256, 32>(a, km, vm, qm, pm, v2, num_sms, s);
   if (a.head_dim == 128 && a.block_size == 16)
-    return launch_tc_t<T, 128, 16>(a, km, vm, qm, v2, num_sms, s);
+    return launch_tc_t<T, 128, 16>(a, km, vm, qm, pm, v2, num_sms, s);
   if (a.head_dim == 128 && a.block_size == 32)
-    return launch_tc_t<T, 128, 32>(a, km, vm, qm, v2, num_sms, s);
+    return launch_tc_t<T, 128, 32>(a, km, vm, qm, pm, v2, num_sms, s);
   if (a.head_dim == 128 && a.block_size == 64)
-    return launch_tc_t<T, 128, 64>(a, km, vm, qm, v2, num_sms, s);
+    return launch_tc_t<T, 128, 64>(a, km, vm, qm, pm, v2, num_sms, s);
   return cudaErrorInvalidValue;
 }
 

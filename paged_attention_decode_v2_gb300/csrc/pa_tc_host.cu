@@ -20,9 +20,11 @@
 namespace pa {
 
 cudaError_t launch_tc_bf16(const KernelArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                           const CUtensorMap& qmap, bool v2, int num_sms, cudaStream_t s);
+                           const CUtensorMap& qmap, const CUtensorMap& pmap, bool v2, int num_sms,
+                           cudaStream_t s);
 cudaError_t launch_tc_f16(const KernelArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                          const CUtensorMap& qmap, bool v2, int num_sms, cudaStream_t s);
+                          const CUtensorMap& qmap, const CUtensorMap& pmap, bool v2, int num_sms,
+                          cudaStream_t s);
 
 namespace {
 
@@ -147,9 +149,24 @@ cudaError_t launch_tc(const KernelArgs& a, pa_dtype_t kv, bool v2, cudaStream_t 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
+  // The partials as [rows][NP][head_dim] floats, a box of 32 elements x up to
+  // 256 partitions of one row: only the one-launch V2 grid reads it (its
+  // reduce units); otherwise a copy of the q map stands in, never used.
+  CUtensorMap pmap = qmap;
+  if (a.fused) {
+    const cuuint64_t np = static_cast<cuuint64_t>(a.num_partitions);
+    const cuuint64_t dims[3] = {D, np, static_cast<cuuint64_t>(a.num_seqs) * a.num_heads};
+    const cuuint64_t strides[2] = {D * 4, np * D * 4};
+    const cuuint32_t box[3] = {32, static_cast<cuuint32_t>(np < 256 ? np : 256), 1};
+    const cuuint32_t es[3] = {1, 1, 1};
+    if (enc(&pmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, a.tmp_out, dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   const int sms = device_info().num_sms;
-  return kv == PA_BF16 ? launch_tc_bf16(a, kmap, vmap, qmap, v2, sms, s)
-                       : launch_tc_f16(a, kmap, vmap, qmap, v2, sms, s);
+  return kv == PA_BF16 ? launch_tc_bf16(a, kmap, vmap, qmap, pmap, v2, sms, s)
+                       : launch_tc_f16(a, kmap, vmap, qmap, pmap, v2, sms, s);
 }
 
 }  // namespace pa

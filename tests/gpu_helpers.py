@@ -10,6 +10,7 @@ import paged_attention_decode_v2_gb300 as pa
 TOL = {torch.float32: 1e-5, torch.bfloat16: 2e-3, torch.float16: 2e-3}
 
 
+CONTROL_BYTES = 1024        # the workspace's control block (status, marker, counters)
 GUARD_BYTES = 4096          # canary region on each side of out and the workspace
 GUARD_F = -4096.0           # canary of out's guards (exact in f32, bf16 and f16)
 GUARD_B = 0xA5              # canary byte of the workspace's guards
@@ -52,8 +53,8 @@ def run(batch, path="decode", partition_size=512, portable=False, out_dtype=torc
     if workspace is None and path in ("v2", "decode"):
         n = pa.workspace_size(params)
         ws_whole, workspace = _guarded(n, torch.uint8, GUARD_B, b.q.device)
-        workspace.view(torch.float32)[64:].fill_(float("nan"))   # poison all but the status
-        pa.workspace_init(workspace)
+        workspace.view(torch.float32).fill_(float("nan"))        # poison everything,
+        pa.workspace_init(workspace)                              # then the control block
     kw = dict(max_seq_len=b.max_seq_len, scale=b.scale, portable=portable)
     if path == "v1":
         pa.decode_v1(b.q, b.k_cache, b.v_cache, b.block_tables, b.seq_lens, out, **kw)
@@ -101,10 +102,21 @@ def workspace_views(ws, batch, partition_size):
     NP = max(1, -(-batch.max_seq_len // partition_size))
     r = lambda x: (x + 255) // 256 * 256
     f = ws.view(torch.float32)
-    o_ml = 256
+    o_ml = CONTROL_BYTES
     o_es = o_ml + r(B * H * NP * 4)
     o_to = o_es + r(B * H * NP * 4)
     ml = f[o_ml // 4:o_ml // 4 + B * H * NP].view(B, H, NP)
     es = f[o_es // 4:o_es // 4 + B * H * NP].view(B, H, NP)
     to = f[o_to // 4:o_to // 4 + B * H * NP * D].view(B, H, NP, D)
     return ml.double().cpu().numpy(), es.double().cpu().numpy(), to.double().cpu().numpy()
+
+
+def control_words(ws):
+    """The control block's words: (marker, epoch, CTAs started, finished
+    counters [2], unit queues [2]) of the one-launch V2 step."""
+    w = ws[:CONTROL_BYTES].view(torch.int32).cpu().numpy().astype(np.int64) & 0xFFFFFFFF
+    start = int(w[64]) | (int(w[65]) << 32)
+    return int(w[1]), start >> 32, start & 0xFFFFFFFF, w[66:68].tolist(), w[68:70].tolist()
+
+
+MARKER = 0x5A5A5A5A

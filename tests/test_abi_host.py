@@ -47,9 +47,12 @@ def params(**kw):
     return pa.Params(**base)
 
 
+CONTROL = 1024          # status word, init marker and one-launch counters
+
+
 def expected_ws(B, H, D, NP):
     r = lambda x: (x + 255) // 256 * 256
-    return 256 + 2 * r(B * H * NP * 4) + r(B * H * NP * D * 4)
+    return CONTROL + 2 * r(B * H * NP * 4) + r(B * H * NP * D * 4)
 
 
 def test_workspace_size_formula(L):
@@ -70,10 +73,10 @@ def test_workspace_matches_the_pages_sizing(L):
                max_seq_len=c["max_seq_len"], partition_size=c["partition_size"],
                max_blocks_per_seq=c["max_seq_len"] // 16, num_blocks=c["max_seq_len"] // 16)
     total = pa.workspace_size(p)
-    # regions: status (256) | max_logits | exp_sums | tmp_output, each 256-aligned
+    # regions: control block | max_logits | exp_sums | tmp_output, each 256-aligned
     r = lambda x: (x + 255) // 256 * 256
     assert printed["exp_sums_bytes"] == c["num_seqs"] * c["num_heads"] * c["num_partitions"] * 4
-    tmp = total - 256 - 2 * r(printed["exp_sums_bytes"])
+    tmp = total - CONTROL - 2 * r(printed["exp_sums_bytes"])
     assert tmp == 2 * printed["tmp_output_bytes_2B"]          # float32 partials
     assert tmp // 4 == printed["tmp_output_elements"]
 
@@ -90,8 +93,25 @@ def test_dispatch_threshold(L):
     assert pa.decode_path(params(num_kv_heads=7)) == 0
 
 
+def test_decode_launches(L):
+    """pa_decode_launches: V1 is one launch; V2 is one launch where the
+    tensor-core kernel runs a persistent grid with a CTA per reduce unit (one
+    100K-token sequence, 24 heads), else two; invalid parameters and empty
+    batches make none."""
+    assert L.pa_decode_launches(ctypes.byref(params(max_seq_len=8192))) == 1
+    assert L.pa_decode_launches(ctypes.byref(params(num_heads=25))) == 0
+    assert L.pa_decode_launches(ctypes.byref(params(num_seqs=0))) == 0
+    v2 = L.pa_decode_launches(ctypes.byref(params()))
+    assert v2 == (1 if pa.decode_kernel(params()) == 2 else 2)
+    # the CUDA-core path keeps the dependent reduce kernel
+    assert L.pa_decode_launches(ctypes.byref(params(flags=pa.PA_FLAG_PORTABLE))) == 2
+    # more reduce units (32 rows x 8 slices of 32) than the persistent grid's CTAs
+    big = params(num_seqs=32, max_blocks_per_seq=6250)
+    assert L.pa_decode_launches(ctypes.byref(big)) == 2
+
+
 def test_status_strings(L):
-    for code in range(0, 9):
+    for code in range(0, 10):
         s = pa.status_string(code)
         assert s and s != "unknown status"
     assert pa.status_string(99) == "unknown status"

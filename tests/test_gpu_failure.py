@@ -14,6 +14,7 @@ import torch
 import oracle
 import paged_attention_decode_v2_gb300 as pa
 from paged_attention_decode_v2_gb300 import workloads as wl
+from gpu_helpers import MARKER, control_words
 
 pytestmark = pytest.mark.gpu
 
@@ -38,6 +39,35 @@ def test_wait_that_runs_out_reports_timeout_and_context_survives():
     assert torch.isnan(out).all().item()
 
     # the context is still usable: a normal call succeeds and is correct
+    pa.decode_v2(bg.q, bg.k_cache, bg.v_cache, bg.block_tables, bg.seq_lens, out, ws, **kw)
+    torch.cuda.synchronize()
+    assert pa.read_device_status(ws) == pa.PA_OK
+    ref = oracle.decode(bc.q, bc.k_cache, bc.v_cache, bc.block_tables, bc.seq_lens, bc.scale)
+    assert float(np.max(np.abs(out.double().cpu().numpy() - ref))) <= 2e-3
+
+
+def test_one_launch_step_with_a_wait_that_runs_out():
+    """The one-launch V2 step (pass 2 in the pass-1 grid) with every CTA's
+    waits running out: the grid still meets at its end, the outputs are NaN,
+    the status reads PA_ERR_DEVICE_TIMEOUT, the control block is ready for
+    the next launch (epoch advanced, start count back at zero), and the next
+    call is exact."""
+    bc = wl.make(wl.scaled(wl.WORKLOADS["long_100k"], seq_len=30000), poison=True)
+    bg = bc.to("cuda")
+    P = 512
+    params = pa.make_params(bg.q, bg.k_cache, bg.block_tables, max_seq_len=bg.max_seq_len,
+                            scale=bg.scale, partition_size=P, out_dtype=torch.float32)
+    assert pa.decode_launches(params) == 1
+    ws = pa.alloc_workspace(params)
+    kw = dict(max_seq_len=bg.max_seq_len, scale=bg.scale, partition_size=P)
+    out = torch.zeros(tuple(bg.q.shape), dtype=torch.float32, device="cuda")
+    pa.decode_v2(bg.q, bg.k_cache, bg.v_cache, bg.block_tables, bg.seq_lens, out, ws,
+                 flags=pa.PA_FLAG_SELFTEST_STALL, **kw)
+    torch.cuda.synchronize()
+    assert pa.read_device_status(ws) == pa.PA_ERR_DEVICE_TIMEOUT
+    assert torch.isnan(out).all().item()
+    marker, epoch, started, _, _ = control_words(ws)
+    assert marker == MARKER and epoch == 1 and started == 0
     pa.decode_v2(bg.q, bg.k_cache, bg.v_cache, bg.block_tables, bg.seq_lens, out, ws, **kw)
     torch.cuda.synchronize()
     assert pa.read_device_status(ws) == pa.PA_OK

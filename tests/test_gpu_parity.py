@@ -16,7 +16,8 @@ import torch
 import oracle
 import paged_attention_decode_v2_gb300 as pa
 from paged_attention_decode_v2_gb300 import workloads as wl
-from gpu_helpers import TOL, assert_close, bf16_round, max_err, run, workspace_views
+from gpu_helpers import (MARKER, TOL, assert_close, bf16_round, control_words, max_err, run,
+                         workspace_views)
 from oracle_pins import problem
 
 pytestmark = pytest.mark.gpu
@@ -87,6 +88,9 @@ def test_reduce_slice_widths(num_seqs, max_len):
     for P in (16, 512):
         got = run(bg, path="v2", partition_size=P)
         assert_close(got, ref, TOL[w.dtype], f"B={num_seqs} P={P}")
+        # the reduce kernel itself (pa_decode_v2 folds it into pass 1 here)
+        got2, _ = _partitions_then_reduce(bg, P, False)
+        assert_close(got2, ref, TOL[w.dtype], f"B={num_seqs} P={P} two calls")
         # a bf16 output: the float32 result's bound plus half an ulp of the rounding
         got16 = run(bg, path="v2", partition_size=P, out_dtype=torch.bfloat16)
         assert np.all(np.abs(got16 - ref) <= 2e-3 + np.abs(bf16_round(ref)) * 2.0 ** -8)
@@ -140,7 +144,7 @@ def _partitions_then_reduce(bg, P, portable):
                             scale=bg.scale, partition_size=P, portable=portable,
                             out_dtype=torch.float32)
     ws = torch.empty(pa.workspace_size(params), dtype=torch.uint8, device="cuda")
-    ws.view(torch.float32)[64:].fill_(float("nan"))
+    ws.view(torch.float32).fill_(float("nan"))
     pa.workspace_init(ws)
     pa.decode_v2_partitions(bg.q, bg.k_cache, bg.v_cache, bg.block_tables, bg.seq_lens, ws,
                             max_seq_len=bg.max_seq_len, scale=bg.scale, partition_size=P,
@@ -523,3 +527,136 @@ def test_split_x_layout(dtype, D, BS):
         assert np.array_equal(g, want), f"split-x {path} differs from the standard layout"
         assert_close(g, ref, TOL[dtype], f"split-x {path}")
         assert pa.read_device_status(ws) == pa.PA_OK
+
+
+# ---------------------------------------------------------------------------
+# V2 in one launch: the pass-1 grid runs pass 2 itself after its streaming
+# ---------------------------------------------------------------------------
+def _one_launch_cases():
+    lens = [20000, 1, 0, 512, 513, 9000]
+    mixed = dataclasses.replace(
+        wl.WORKLOADS["mixed_32"], name="mixed_small_heads", num_seqs=len(lens), num_heads=8,
+        num_kv_heads=2, head_dim=128, block_size=16, pool_blocks=None,
+        seq_lens=lambda g: torch.tensor(lens, dtype=torch.int32))
+    return [(wl.scaled(wl.WORKLOADS["long_100k"], seq_len=30000), 512),   # 59 partitions
+            (mixed, 128),                       # lengths 0 .. 20000: direct, zero and split rows
+            (wl.scaled(wl.WORKLOADS["long_100k"], seq_len=60000), 1024)]  # two rounds of items
+
+
+@pytest.mark.parametrize("case", [0, 1, 2], ids=["one_long_sequence", "mixed_lengths",
+                                                 "two_rounds"])
+def test_one_launch_back_to_back_then_graph_replay(case):
+    """pa_decode_v2 as one launch: two steps in a row on one NaN-poisoned
+    workspace with different q and lengths, then the step captured in a CUDA
+    graph and replayed twice with new inputs; every step against the oracle,
+    and after each launch the control block ready for the next (marker
+    intact, epoch advanced by one, start count back at zero)."""
+    w, P = _one_launch_cases()[case]
+    bc = wl.make(w, poison=True)
+    bg = bc.to("cuda")
+    params = pa.make_params(bc.q, bc.k_cache, bc.block_tables, max_seq_len=bc.max_seq_len,
+                            scale=bc.scale, partition_size=P, out_dtype=torch.float32,
+                            v1_max_seq_len=1)                     # pa_decode's choice: V2
+    assert pa.decode_launches(params) == 1
+    ws = torch.empty(pa.workspace_size(params), dtype=torch.uint8, device="cuda")
+    ws.view(torch.float32).fill_(float("nan"))
+    pa.workspace_init(ws)
+    out = torch.full(tuple(bc.q.shape), float("nan"), device="cuda")
+    kw = dict(max_seq_len=bc.max_seq_len, scale=bc.scale, partition_size=P)
+    g = torch.Generator().manual_seed(90 + case)
+    launches = [0]
+
+    def new_inputs(cut):
+        q = torch.randn(tuple(bc.q.shape), generator=g).to(bc.q.dtype)
+        lens = torch.where(bc.seq_lens > cut, bc.seq_lens - cut, bc.seq_lens)
+        bg.q.copy_(q)
+        bg.seq_lens.copy_(lens)
+        return q, lens
+
+    def check(q, lens, what):
+        launches[0] += 1
+        ref = oracle.decode(q, bc.k_cache, bc.v_cache, bc.block_tables, lens, bc.scale)
+        assert_close(out.double().cpu().numpy(), ref, TOL[w.dtype], what)
+        assert pa.read_device_status(ws, clear=False) == pa.PA_OK
+        marker, epoch, started, _, _ = control_words(ws)
+        assert (marker, epoch, started) == (MARKER, launches[0], 0), (what, epoch, started)
+
+    for step, cut in enumerate((0, 333)):
+        q, lens = new_inputs(cut)
+        pa.decode_v2(bg.q, bg.k_cache, bg.v_cache, bg.block_tables, bg.seq_lens, out, ws, **kw)
+        torch.cuda.synchronize()
+        check(q, lens, f"step {step}")
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        pa.decode_v2(bg.q, bg.k_cache, bg.v_cache, bg.block_tables, bg.seq_lens, out, ws, **kw)
+    for rep, cut in enumerate((1000, 7)):
+        q, lens = new_inputs(cut)
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        check(q, lens, f"replay {rep}")
+
+
+def test_one_launch_matches_two_launches_closely():
+    """The one-launch step and the two-kernel form (pa_decode_v2_partitions,
+    pa_decode_v2_reduce) compute the same log-sum-exp identity in different
+    orders: they agree far inside the tolerance, and each is bit-identical
+    from run to run."""
+    bg = wl.make(wl.scaled(wl.WORKLOADS["long_100k"], seq_len=50000), poison=True).to("cuda")
+    params = pa.make_params(bg.q, bg.k_cache, bg.block_tables, max_seq_len=bg.max_seq_len,
+                            scale=bg.scale, partition_size=256, out_dtype=torch.float32)
+    assert pa.decode_launches(params) == 1
+    one = run(bg, path="v2", partition_size=256)           # 196 partitions
+    two, _ = _partitions_then_reduce(bg, 256, False)
+    assert max_err(one, two) <= 1e-5
+    assert np.array_equal(run(bg, path="v2", partition_size=256), one)
+
+
+def test_uninitialised_workspace_is_reported_not_reduced():
+    """A workspace that pa_workspace_init never initialised (NaN everywhere,
+    control block included): the one-launch step reduces nothing, the status
+    word reads PA_ERR_WORKSPACE_NOT_INIT, the rows it would have reduced
+    (split sequences, and the empty one) are NaN, and the sequence that pass
+    1 finished itself is still right."""
+    lens = [3000, 100, 0, 5000]
+    w = dataclasses.replace(
+        wl.WORKLOADS["mixed_32"], name="uninit", num_seqs=len(lens), num_heads=8,
+        num_kv_heads=2, head_dim=128, block_size=16, pool_blocks=None,
+        seq_lens=lambda g: torch.tensor(lens, dtype=torch.int32))
+    bc = wl.make(w, poison=True)
+    ref = _ref(bc)
+    bg = bc.to("cuda")
+    params = pa.make_params(bc.q, bc.k_cache, bc.block_tables, max_seq_len=bc.max_seq_len,
+                            scale=bc.scale, partition_size=128, out_dtype=torch.float32,
+                            v1_max_seq_len=1)                     # pa_decode's choice: V2
+    assert pa.decode_launches(params) == 1
+    ws = torch.empty(pa.workspace_size(params), dtype=torch.uint8, device="cuda")
+    ws.view(torch.float32).fill_(float("nan"))
+    got = run(bg, path="v2", partition_size=128, workspace=ws, check_status=False)
+    assert pa.read_device_status(ws) == pa.PA_ERR_WORKSPACE_NOT_INIT
+    for b, L in enumerate(lens):
+        if L > 128 or L == 0:
+            assert np.all(np.isnan(got[b])), b
+        else:
+            assert_close(got[b], ref[b], 2e-3, f"sequence {b} (L={L})")
+    # once initialised, the same workspace gives the right answer
+    pa.workspace_init(ws)
+    assert_close(run(bg, path="v2", partition_size=128, workspace=ws), ref, 2e-3, "after init")
+
+
+def test_two_launches_for_many_rows():
+    """A batch with more reduce units (query rows x head_dim / 32) than the
+    persistent grid has CTAs -- 2048 sequences x 8 heads -- runs as pass 1
+    plus the dependent reduce kernel; every row against the oracle."""
+    n = 2048
+    w = dataclasses.replace(
+        wl.WORKLOADS["mixed_32"], name="many_heads", num_seqs=n, num_heads=8, num_kv_heads=8,
+        head_dim=128, block_size=16, pool_blocks=None,
+        seq_lens=lambda g: torch.randint(1, 301, (n,), generator=g,
+                                         dtype=torch.int64).to(torch.int32))
+    bc = wl.make(w, poison=True)
+    params = pa.make_params(bc.q, bc.k_cache, bc.block_tables, max_seq_len=bc.max_seq_len,
+                            scale=bc.scale, partition_size=16, out_dtype=torch.float32,
+                            v1_max_seq_len=1)                     # pa_decode's choice: V2
+    assert pa.decode_launches(params) == 2
+    assert_close(run(bc.to("cuda"), path="v2", partition_size=16), _ref(bc), 2e-3, "two launches")
