@@ -82,8 +82,8 @@ inline bool one_launch_plan(int64_t num_seqs, int64_t num_heads, int64_t num_kv_
   const int64_t items = num_seqs * num_kv_heads * np;
   const bool compact = num_seqs > 1 && num_seqs <= 1024;  // the kernel's compact work list
   const int64_t grid = tc_persistent_grid(items, compact, num_sms);
-  // a unit holds the statistics of up to 4096 partitions
-  return grid > 0 && np <= 4096 && num_seqs * num_heads * (head_dim / 32) <= grid;
+  // a unit holds the statistics of up to 1024 partitions
+  return grid > 0 && np <= 1024 && num_seqs * num_heads * (head_dim / 32) <= grid;
 }
 
 // Everything the prefill kernel needs besides its tensor maps (pa_prefill.cuh).

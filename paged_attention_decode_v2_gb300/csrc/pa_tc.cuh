@@ -692,6 +692,16 @@ __global__ void __launch_bounds__(tc::kThreads, CPS)
         }
       }
     };
+    // One-launch V2: run the end-of-kernel reduce once now, dry (no side
+    // effects, scratch in the still unused P^T buffer), while the first keys
+    // land, so its code is in the instruction cache when the reduce runs.
+    static_assert(gridred::kDryBytes <= (kChunk / 16) * 512, "dry run within the P^T buffer");
+    if (kV2 && !kClusters && a.fused && c.ws_ok) {
+      uint32_t dry_phase = 0;
+      gridred::reduce_unit<D>(a, &pmap, &c.red_bar, dry_phase, 0, 0,
+                              *reinterpret_cast<gridred::UnitScratch*>(pt), tid, false, budget,
+                              true);
+    }
     uint32_t cc = 0, ic = 0;  // chunks / cluster combines so far
     for (int64_t k = cid; k < total_items; k += stride) {
       const Item it = item_at(a, prefix, k, kV2, rank, cs);
@@ -867,7 +877,8 @@ __global__ void __launch_bounds__(tc::kThreads, CPS)
   // one-launch V2 (persistent shape only): pass 2 by this grid, once every
   // CTA has stored its partials; the ring is free scratch now
   static_assert(sizeof(gridred::UnitScratch) <= NST * kStageBytes, "reduce scratch in the ring");
-  if (kV2 && !kClusters && a.fused)
+  static_assert(alignof(gridred::UnitScratch) <= 1024, "the ring starts 1024-byte aligned");
+  if (kV2 && !kClusters && a.fused && warp < 4)
     gridred::grid_reduce<D>(a, c.ws_ok != 0, started, c.red_word,
                             *reinterpret_cast<gridred::UnitScratch*>(ring), &pmap, &c.red_bar, tid,
                             budget);
