@@ -27,6 +27,7 @@ all ranks' bytes over that time.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import glob
 import json
@@ -213,9 +214,20 @@ def run_ours(args, rank, world, device):
     w = wl.WORKLOADS[args.workload]
     P = args.partition_size or w.partition_sizes[0]
     batch = wl.make(w, device=device)
+    sx = {}
+    if args.split_x:
+        # the caches rewritten (on the device, before timing) into the pages'
+        # V1 layout: keys [blocks, kv_heads, head_dim / 8, block_size, 8],
+        # values [blocks, kv_heads, head_dim, block_size]
+        nb, hkv, bsz, dh = batch.k_cache.shape
+        xg = 16 // batch.k_cache.element_size()
+        k5 = batch.k_cache.view(nb, hkv, bsz, dh // xg, xg).permute(0, 1, 3, 2, 4).contiguous()
+        v4 = batch.v_cache.permute(0, 1, 3, 2).contiguous()
+        batch = dataclasses.replace(batch, k_cache=k5, v_cache=v4)
+        sx = dict(split_x=True)
     params = pa.make_params(batch.q, batch.k_cache, batch.block_tables,
                             max_seq_len=batch.max_seq_len, scale=batch.scale, partition_size=P,
-                            out_dtype=torch.float32)
+                            out_dtype=torch.float32, **sx)
     path = pa.decode_path(params) if args.path == "decode" else (1 if args.path == "v1" else 2)
     family = pa.decode_kernel(params)
     # kernel launches of the step on this path (V2: one when pass 1 merges its
@@ -223,9 +235,10 @@ def run_ours(args, rank, world, device):
     launches_per_step = pa.decode_launches(pa.make_params(
         batch.q, batch.k_cache, batch.block_tables, max_seq_len=batch.max_seq_len,
         scale=batch.scale, partition_size=P, out_dtype=torch.float32,
-        v1_max_seq_len=max(batch.max_seq_len, 1) if path == 1 else 1))
+        v1_max_seq_len=max(batch.max_seq_len, 1) if path == 1 else 1, **sx))
     one_launch_v2 = path == 2 and launches_per_step == 1
-    kname = ("pa_tc_kernel" if family == 2 else "pa_generic_kernel") + \
+    kname = ("pa_sx_kernel" if family == 2 and args.split_x else
+             "pa_tc_kernel" if family == 2 else "pa_generic_kernel") + \
         (" (V2 in one launch: pass 1 + merge)" if one_launch_v2 else
          " (V2 pass 1)" if path == 2 else " (V1)")
     ws = pa.alloc_workspace(params, device=device)
@@ -244,7 +257,7 @@ def run_ours(args, rank, world, device):
 
     flush = _Flush()
     stream = torch.cuda.current_stream(device)
-    kw = dict(max_seq_len=batch.max_seq_len, scale=batch.scale, partition_size=P)
+    kw = dict(max_seq_len=batch.max_seq_len, scale=batch.scale, partition_size=P, **sx)
 
     def step():
         if args.path == "decode":
@@ -252,7 +265,8 @@ def run_ours(args, rank, world, device):
                       out, ws, **kw)
         elif args.path == "v1":
             pa.decode_v1(batch.q, batch.k_cache, batch.v_cache, batch.block_tables,
-                         batch.seq_lens, out, max_seq_len=batch.max_seq_len, scale=batch.scale)
+                         batch.seq_lens, out, max_seq_len=batch.max_seq_len, scale=batch.scale,
+                         **sx)
         else:
             pa.decode_v2(batch.q, batch.k_cache, batch.v_cache, batch.block_tables,
                          batch.seq_lens, out, ws, **kw)
@@ -348,7 +362,7 @@ def run_ours(args, rank, world, device):
     v1max = {"v1": max(batch.max_seq_len, 1), "v2": 1}.get(args.path, pa.DEFAULT_V1_MAX_SEQ_LEN)
     hparams = pa.make_params(batch.q, batch.k_cache, batch.block_tables,
                              max_seq_len=batch.max_seq_len, scale=batch.scale, partition_size=P,
-                             out_dtype=out.dtype, v1_max_seq_len=v1max)
+                             out_dtype=out.dtype, v1_max_seq_len=v1max, **sx)
     # the host inputs live in a pinned mirror of the staging layout, so the
     # call moves them in one copy
     mbuf, q_h, bt_h, sl_h = pa.alloc_host_mirror(hparams, batch.q.dtype, *batch.q.shape,
@@ -397,7 +411,7 @@ def run_ours(args, rank, world, device):
         e[1].record(stream)
         pa.decode(q_d, batch.k_cache, batch.v_cache, bt_d, sl_d, out_d, ws_host,
                   max_seq_len=batch.max_seq_len, scale=batch.scale, partition_size=P,
-                  v1_max_seq_len=v1max)
+                  v1_max_seq_len=v1max, **sx)
         e[2].record(stream)
         out_h.copy_(out_d, non_blocking=True)
         e[3].record(stream)
@@ -441,6 +455,9 @@ def run_ours(args, rank, world, device):
                         f"{w.num_heads} q / {w.num_kv_heads} kv heads, head_dim {w.head_dim}, "
                         f"{str(w.dtype).replace('torch.', '')} KV, block {w.block_size}",
             "partition_size": P,
+            "cache_layout": ("split-x (keys [blocks, kv_heads, head_dim/8, block, 8], values "
+                             "[blocks, kv_heads, head_dim, block])" if args.split_x else
+                             "[blocks, kv_heads, block, head_dim]"),
             "path": ("V2 in one launch (partition kernel merging its own partials)"
                      if one_launch_v2 else
                      "V2 (partition kernel + LSE reduce)" if path == 2 else "V1 single pass") +
@@ -804,6 +821,8 @@ def main():
     ap.add_argument("--workload", default="long_100k",
                     choices=sorted(wl.WORKLOADS) + sorted(wl.PREFILL_WORKLOADS))
     ap.add_argument("--partition-size", type=int, default=0)
+    ap.add_argument("--split-x", action="store_true",
+                    help="caches in the pages' V1 split-x layout (read directly)")
     ap.add_argument("--path", choices=("decode", "v1", "v2"), default="decode",
                     help="pa_decode (threshold dispatch), or force V1 / V2")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,

@@ -97,9 +97,11 @@ typedef enum pa_dtype { PA_F32 = 0, PA_BF16 = 1, PA_F16 = 2 } pa_dtype_t;
                                          head_dim, block_size]
                               with x = 16 / element bytes (8 for bf16 / f16,
                               4 for f32).  Read directly, with no conversion
-                              copy, by the CUDA-core kernels (the tensor-core
-                              kernels need the [.., block_size, head_dim]
-                              layout); every call accepts it. */
+                              copy: for bf16 / f16 caches with block_size 16
+                              or 32 and at most 8 query heads per KV head by
+                              a tensor-core kernel (warp-level MMA fed by
+                              ldmatrix from whole-block bulk copies), else by
+                              the CUDA-core kernels; every call accepts it. */
 
 typedef struct pa_params {
   int32_t num_seqs;           /* B >= 0                                      */
@@ -312,11 +314,13 @@ PA_API int pa_decode_path(const pa_params_t* params);
 PA_API int pa_decode_launches(const pa_params_t* params);
 
 /* Which kernels the decode calls use for these parameters on the current
- * device: 2 = tensor-core kernels (TMA + tcgen05; bf16 / f16 caches, at most
- * 8 query heads per KV head, head_dim 128 or 256 with block_size 16 or 32,
- * or head_dim 128 with block_size 64), 1 = CUDA-core kernels (every other
- * valid case, or PA_FLAG_PORTABLE), 0 = invalid parameters.  Host function;
- * it queries the current device's compute capability. */
+ * device: 2 = tensor-core kernels (bf16 / f16 caches, at most 8 query heads
+ * per KV head; standard layout: TMA + tcgen05, head_dim 128 or 256 with
+ * block_size 16 or 32, or head_dim 128 with block_size 64; PA_FLAG_SPLIT_X:
+ * bulk copies + warp-level MMA, head_dim 64, 128 or 256 with block_size 16
+ * or 32), 1 = CUDA-core kernels (every other valid case, or
+ * PA_FLAG_PORTABLE), 0 = invalid parameters.  Host function; it queries the
+ * current device's compute capability. */
 PA_API int pa_decode_kernel(const pa_params_t* params);
 
 /* Static description of a status code (never NULL). */

@@ -281,10 +281,12 @@ def decode_v2(q, k_cache, v_cache, block_tables, seq_lens, out, workspace, *, ma
 
 def decode_v2_partitions(q, k_cache, v_cache, block_tables, seq_lens, workspace, *,
                          max_seq_len: int, scale: float, partition_size: int = 512,
-                         out_dtype=None, portable: bool = False, stream=None):
+                         out_dtype=None, portable: bool = False, split_x: bool = False,
+                         stream=None):
     """``pa_decode_v2_partitions``: V2 pass 1 only (fills the workspace)."""
     p = make_params(q, k_cache, block_tables, max_seq_len=max_seq_len, scale=scale,
-                    partition_size=partition_size, out_dtype=out_dtype, portable=portable)
+                    partition_size=partition_size, out_dtype=out_dtype, portable=portable,
+                    split_x=split_x)
     st = lib().pa_decode_v2_partitions(ctypes.byref(p), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                        _ptr(block_tables), _ptr(seq_lens), _ptr(workspace),
                                        workspace.numel() * workspace.element_size(),

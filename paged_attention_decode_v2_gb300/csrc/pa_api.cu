@@ -97,6 +97,8 @@ KernelArgs make_args(const pa_params_t* p, const void* q, const void* k, const v
 
 cudaError_t launch_pass(const pa_params_t* p, const KernelArgs& a, bool v2, cudaStream_t s) {
   if (tc_applicable(p)) return launch_tc(a, p->kv_dtype, v2, s);
+  if (sx_applicable(p))
+    return p->kv_dtype == PA_BF16 ? launch_sx_bf16(a, v2, s) : launch_sx_f16(a, v2, s);
   switch (p->kv_dtype) {
     case PA_F32: return launch_generic_f32(a, v2, s);
     case PA_BF16: return launch_generic_bf16(a, v2, s);
@@ -261,7 +263,7 @@ int pa_decode_launches(const pa_params_t* p) {
 
 int pa_decode_kernel(const pa_params_t* p) {
   if (check_params(p, false) != PA_OK) return 0;
-  return tc_applicable(p) ? 2 : 1;
+  return tc_applicable(p) || sx_applicable(p) ? 2 : 1;
 }
 
 const char* pa_status_string(pa_status_t s) {

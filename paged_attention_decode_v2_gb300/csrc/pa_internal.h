@@ -122,6 +122,11 @@ pa_status_t check_params(const pa_params_t* p, bool v2);
 // the current device, and its launch (pass 1 for V2, the whole pass for V1).
 bool tc_applicable(const pa_params_t* p);
 cudaError_t launch_tc(const KernelArgs& a, pa_dtype_t kv, bool v2, cudaStream_t s);
+// Tensor-core path for caches in the split-x layout (pa_sx.cuh): whether it
+// serves these parameters on the current device, and its launches.
+bool sx_applicable(const pa_params_t* p);
+cudaError_t launch_sx_bf16(const KernelArgs& a, bool v2, cudaStream_t s);
+cudaError_t launch_sx_f16(const KernelArgs& a, bool v2, cudaStream_t s);
 
 // TMA tiled tensor map (pa_tc_host.cu) with the 128-byte swizzle the MMA
 // descriptors expect: `rank` dims (innermost first), the byte strides of

@@ -1,0 +1,394 @@
+// pa_sx.cuh -- tensor-core decode kernel for caches in the split-x layout.
+//
+// The layout commit 4eb83a7e "qwen3_6_scripts", paragraph "Hardware testing
+// confirmed", gives for its V1 kernel:
+//   keys   [blocks, kv_heads, head_dim / x, block_size, x]  (x = 8 for 16-bit)
+//   values [blocks, kv_heads, head_dim, block_size]
+// One (block, KV head) of either cache is one contiguous region of
+// block_size * head_dim elements, so a block comes in by two bulk copies
+// (cp.async.bulk, 8 KB each for 16 tokens of head_dim 256).  The shared-memory
+// descriptors of tcgen05.mma need 8-row groups at one uniform stride, which
+// blocks scattered over the pool do not give; the warp-level MMA
+// (mma.sync.m16n8k16) takes its operands from registers, loaded with ldmatrix
+// from any eight 16-byte rows, and a split-x key group is exactly such a set
+// of rows (8 consecutive head_dim elements of one token per row), as is a
+// transposed value row (8 consecutive tokens of one head_dim element).  The
+// kernel is bound by HBM, not by the tensor pipe.
+//
+// Work item: one (sequence, KV head, token range), the range a V2 partition
+// or the whole sequence (V1); the G <= 8 query heads of the KV head are
+// served together.  One CTA per item: warp 4 streams the range's blocks into
+// a ring of whole blocks (keys and values), warps 0-3 consume it in chunks
+// of 32 tokens:
+//   QK^T   warp w: S[h, t] for the chunk's 8 tokens 8w .. 8w + 7, over all of
+//          head_dim (A = q, rows 0..7 = the query heads; B = keys);
+//   softmax the chunk's max per head across the four warps (shared memory),
+//          p = exp2(l - m), the running max / sum / rescale across chunks;
+//   P.V    warp w: head_dim slice w of O[h, d] over the chunk's 32 tokens;
+//          A = P with rows 0..7 its 16-bit hi part and rows 8..15 the
+//          rounded remainder, so one MMA carries ~16 significant bits of p
+//          and O = (rows 0..7) + (rows 8..15) at the end.
+// Logits are f32 sums of exact 16-bit products, scaled into base 2 after.
+//
+// This is Phase 1 of the V2 scheme of commit 4eb83a7e "qwen3_6_scripts",
+// paragraph "Implementation (paged_attention_v2_pytorch.py)", or V1 when the
+// range is the whole sequence.  Every wait is bounded; a wait that gives up
+// sets PA_ERR_DEVICE_TIMEOUT and the item's outputs become NaN.
+#pragma once
+
+#include <type_traits>
+
+#include "pa_device.cuh"
+#include "pa_sm100.cuh"
+
+namespace pa {
+namespace sx {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
+constexpr int kChunk = 32;                           // tokens per chunk
+constexpr int kRingBytes = 96 * 1024;                // two CTAs per SM
+constexpr int kMaxStages = 24;
+constexpr long long kWaitBudget = 4000000000LL;      // cycles (about 2 s)
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t (&r)[2], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];"
+               : "=r"(r[0]), "=r"(r[1])
+               : "r"(addr));
+}
+
+// D (16 x 8, f32) += A (16 x 16) * B (16 x 8), 16-bit inputs.
+template <typename T>
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4],
+                                         const uint32_t (&b)[2]) {
+  if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+  }
+}
+
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// from global to shared memory, counted on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                         uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], %4;" ::"r"(sm100::smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(sm100::smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Two 16-bit values in one register (low half: the first).
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(T lo, T hi) {
+  return static_cast<uint32_t>(bits16(lo)) | (static_cast<uint32_t>(bits16(hi)) << 16);
+}
+
+template <int D, int BS>
+struct Layout {
+  static constexpr int kBlockBytes = BS * D * 2;            // one block of one cache
+  static constexpr int kStageBytes = 2 * kBlockBytes;       // keys + values
+  static constexpr int kStages =
+      kRingBytes / kStageBytes < kMaxStages ? kRingBytes / kStageBytes : kMaxStages;
+  static constexpr int kChunkBlocks = kChunk / BS > 0 ? kChunk / BS : 1;
+  static constexpr int kQStride = D + 8;                     // q tile row (elements), padded
+  static constexpr int kPStride = kChunk + 8;                // P tile row (elements), padded
+  static constexpr int kQOff = kStages * kStageBytes;
+  static constexpr int kPOff = kQOff + 16 * kQStride * 2;
+  static constexpr int kRedOff = kPOff + 16 * kPStride * 2;  // [4 warps][8 heads] max, sum
+  static constexpr int kBarOff = kRedOff + 2 * kConsumerWarps * 8 * 4;
+  static constexpr int kSmem = kBarOff + (2 * kMaxStages + 2) * 8 + 64;
+  static_assert(kStages >= 2 * kChunkBlocks, "two chunks in flight");
+  static_assert(kSmem <= 113 * 1024, "two CTAs per SM");
+};
+
+}  // namespace sx
+
+template <typename T, int D, int BS, bool kV2>
+__global__ void __launch_bounds__(sx::kThreads, 2) pa_sx_kernel(const KernelArgs a) {
+  using namespace sx;
+  using Lay = Layout<D, BS>;
+  static_assert(BS == 16 || BS == 32, "block size");
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* ring = smem;
+  T* qs = reinterpret_cast<T*>(smem + Lay::kQOff);
+  T* ps = reinterpret_cast<T*>(smem + Lay::kPOff);
+  float* red_max = reinterpret_cast<float*>(smem + Lay::kRedOff);
+  float* red_sum = red_max + kConsumerWarps * 8;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lay::kBarOff);
+  uint64_t* empty = full + kMaxStages;
+  int* flags = reinterpret_cast<int*>(empty + kMaxStages);  // [0] abort, [1] bad block
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int b = blockIdx.z, kvh = blockIdx.y, part = blockIdx.x;
+  const int G = a.group, Hq = a.num_heads;
+  const int32_t L = __ldg(a.seq_lens + b);
+  const int64_t row0 = static_cast<int64_t>(b) * Hq + kvh * G;
+
+  if (!seq_len_ok(a, L)) {
+    if (tid == 0 && part == 0) set_status(a.status, PA_ERR_BAD_SEQ_LEN);
+    if (!kV2)  // V1 writes the NaN rows; for V2 the reduce does
+      for (int i = tid; i < G * D; i += kThreads) store_out(a.out, row0 * D + i, a.out_dtype, qnan());
+    return;
+  }
+  const int32_t t0 = kV2 ? part * a.partition_size : 0;
+  if (kV2 && t0 >= L) return;  // this sequence has no such partition
+  const int32_t t1 = kV2 ? min(L, t0 + a.partition_size) : L;
+  const bool direct = kV2 && a.single_direct && L <= a.partition_size;
+  if (t0 >= t1) {  // V1 row of an empty sequence
+    for (int i = tid; i < G * D; i += kThreads) store_out(a.out, row0 * D + i, a.out_dtype, 0.f);
+    return;
+  }
+  const int nblk = (t1 - 1) / BS - t0 / BS + 1;  // t0 is a multiple of BS
+
+  // ---- set-up ---------------------------------------------------------------------
+  if (tid == 0) {
+    for (int s = 0; s < Lay::kStages; ++s) {
+      sm100::mbar_init(&full[s], 1);
+      sm100::mbar_init(&empty[s], kConsumerWarps);
+    }
+    flags[0] = 0;
+    flags[1] = 0;
+  }
+  // q tile: rows 0..G-1 the query heads, rows G..15 zero
+  for (int i = tid; i < 16 * D; i += kThreads) {
+    const int r = i / D, d = i % D;
+    const T v = r < G ? static_cast<const T*>(a.q)[(row0 + r) * D + d] : round16(0.f, static_cast<T*>(nullptr));
+    qs[r * Lay::kQStride + d] = v;
+  }
+  __syncthreads();
+  volatile int* abort_flag = &flags[0];
+
+  if (warp == kConsumerWarps) {
+    // ========================= producer =======================================
+    const uint64_t policy = sm100::l2_evict_first_policy();
+    const int32_t* bt = a.block_tables + static_cast<int64_t>(b) * a.max_blocks_per_seq + t0 / BS;
+    const char* kc = static_cast<const char*>(a.k_cache);
+    const char* vc = static_cast<const char*>(a.v_cache);
+    bool ok = true;
+    int issued = 0;
+    for (int j0 = 0; j0 < nblk && ok; j0 += 32) {
+      const int32_t id_l = j0 + lane < nblk ? __ldg(bt + j0 + lane) : 0;
+      const int n32 = min(32, nblk - j0);
+      for (int jj = 0; jj < n32 && ok; ++jj) {
+        const int j = j0 + jj;
+        const int slot = j % Lay::kStages;
+        ok = sm100::mbar_wait(&empty[slot], ((j / Lay::kStages) & 1) ^ 1, kWaitBudget, abort_flag);
+        if (!ok) break;
+        const int32_t id = __shfl_sync(0xffffffffu, id_l, jj);
+        if (lane == 0) {
+          if (id < 0 || id >= a.num_blocks) {  // never read: the item becomes NaN
+            flags[1] = 1;
+            set_status(a.status, PA_ERR_BAD_BLOCK_ID);
+            sm100::mbar_arrive(&full[slot]);
+          } else {
+            const int64_t off =
+                (static_cast<int64_t>(id) * a.num_kv_heads + kvh) * Lay::kBlockBytes;
+            uint8_t* st = ring + slot * Lay::kStageBytes;
+            sm100::mbar_arrive_expect_tx(&full[slot], Lay::kStageBytes);
+            bulk_g2s(st, kc + off, Lay::kBlockBytes, &full[slot], policy);
+            bulk_g2s(st + Lay::kBlockBytes, vc + off, Lay::kBlockBytes, &full[slot], policy);
+          }
+        }
+        __syncwarp();
+        issued = j + 1;
+      }
+    }
+    if (!ok) {
+      if (lane == 0) {
+        flags[0] = 1;
+        set_status(a.status, PA_ERR_DEVICE_TIMEOUT);
+      }
+      // copies issued must land before the CTA may exit
+      for (int j = issued > Lay::kStages ? issued - Lay::kStages : 0; j < issued; ++j)
+        sm100::mbar_wait(&full[j % Lay::kStages], (j / Lay::kStages) & 1, kWaitBudget, nullptr);
+    }
+    return;
+  }
+
+  // =========================== consumers (warps 0-3) ================================
+  const int g = lane >> 2, t = lane & 3;  // mma fragment: row group, column pair
+  const float sl2 = a.scale_log2;
+  const uint32_t q_base = sm100::smem_u32(qs);
+  const uint32_t p_base = sm100::smem_u32(ps);
+  const uint32_t ring_base = sm100::smem_u32(ring);
+  constexpr int kDT = D / 4 / 8;  // 8-wide head_dim tiles of this warp's P.V slice
+  float acc[kDT][4];
+#pragma unroll
+  for (int i = 0; i < kDT; ++i)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[i][e] = 0.f;
+  float m_run = -INFINITY, s_run = 0.f;  // for head g (rows g and g + 8)
+  bool poison = false;
+  const int nchunks = (t1 - t0 + kChunk - 1) / kChunk;
+  for (int ci = 0; ci < nchunks; ++ci) {
+    const int c0 = t0 + ci * kChunk;
+    const int n = min(kChunk, t1 - c0);
+    const int jb0 = (c0 - t0) / BS;  // first block of the chunk within the item
+    const int nb = (n + BS - 1) / BS;
+    // every block of the chunk landed
+    for (int jb = jb0; jb < jb0 + nb; ++jb)
+      if (!sm100::mbar_wait(&full[jb % Lay::kStages], (jb / Lay::kStages) & 1, kWaitBudget,
+                            abort_flag)) {
+        poison = true;
+        if (lane == 0) {
+          flags[0] = 1;
+          set_status(a.status, PA_ERR_DEVICE_TIMEOUT);
+        }
+      }
+    // ---- QK^T: this warp's 8 tokens 8w .. 8w + 7 of the chunk --------------------
+    const int tk = warp * 8;  // first token of the n-tile within the chunk
+    const int jb = jb0 + tk / BS, so = tk % BS;
+    const uint32_t kblk = ring_base + (jb % Lay::kStages) * Lay::kStageBytes;
+    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+    if (tk < n) {
+#pragma unroll 4
+      for (int ks = 0; ks < D / 16; ++ks) {
+        uint32_t qa[4], kb[2];
+        // A: rows (lane % 8) + 8 ((lane / 8) % 2), columns 16 ks + 8 (lane / 16)
+        ldsm_x4(qa, q_base + (((lane & 7) + ((lane >> 3) & 1) * 8) * Lay::kQStride + ks * 16 +
+                              (lane >> 4) * 8) * 2);
+        // B: tokens so .. so + 7 of key groups 2 ks and 2 ks + 1 (16 bytes each)
+        ldsm_x2(kb, kblk + (((2 * ks + ((lane >> 3) & 1)) * BS + so + (lane & 7)) * 16));
+        mma16816<T>(sc, qa, kb);
+      }
+    }
+    // logits of head g, tokens tk + 2t, tk + 2t + 1 (c[0], c[1]); c[2], c[3] are padding
+    float l0 = (tk + 2 * t < n) ? sc[0] * sl2 : -INFINITY;
+    float l1 = (tk + 2 * t + 1 < n) ? sc[1] * sl2 : -INFINITY;
+    if (g >= G) l0 = l1 = -INFINITY;
+    float mx = fmaxf(l0, l1);
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    if (t == 0) red_max[warp * 8 + g] = mx;
+    consumer_sync();
+    float mc = red_max[g];
+#pragma unroll
+    for (int w = 1; w < kConsumerWarps; ++w) mc = fmaxf(mc, red_max[w * 8 + g]);
+    const float m_new = fmaxf(m_run, mc);
+    const float p0 = l0 == -INFINITY ? 0.f : exp2f(l0 - m_new);
+    const float p1 = l1 == -INFINITY ? 0.f : exp2f(l1 - m_new);
+    float ssum = p0 + p1;
+    ssum += __shfl_xor_sync(0xffffffffu, ssum, 1);
+    ssum += __shfl_xor_sync(0xffffffffu, ssum, 2);
+    if (t == 0) red_sum[warp * 8 + g] = ssum;
+    // P tile: row g = the hi parts, row g + 8 = the remainders, tokens tk + 2t, +1
+    {
+      const T h0 = round16(p0, static_cast<T*>(nullptr)), h1 = round16(p1, static_cast<T*>(nullptr));
+      const T r0 = round16(p0 - to_float(h0), static_cast<T*>(nullptr));
+      const T r1 = round16(p1 - to_float(h1), static_cast<T*>(nullptr));
+      *reinterpret_cast<uint32_t*>(ps + g * Lay::kPStride + tk + 2 * t) = pack2<T>(h0, h1);
+      *reinterpret_cast<uint32_t*>(ps + (g + 8) * Lay::kPStride + tk + 2 * t) = pack2<T>(r0, r1);
+    }
+    // the tail block: value columns past the range are cleared (P is 0 there,
+    // but 0 * NaN would be NaN)
+    if (n < nb * BS) {
+      const int jt = jb0 + nb - 1;
+      T* vt = reinterpret_cast<T*>(ring + (jt % Lay::kStages) * Lay::kStageBytes + Lay::kBlockBytes);
+      const int valid = n - (nb - 1) * BS;
+      const T zero = round16(0.f, static_cast<T*>(nullptr));
+      for (int i = tid; i < D * (BS - valid); i += 128) {
+        const int d = i / (BS - valid), s = valid + i % (BS - valid);
+        vt[d * BS + s] = zero;
+      }
+    }
+    consumer_sync();
+    float cs = red_sum[g];
+#pragma unroll
+    for (int w = 1; w < kConsumerWarps; ++w) cs += red_sum[w * 8 + g];
+    const float f = m_run == -INFINITY ? 0.f : exp2f(m_run - m_new);
+    s_run = s_run * f + cs;
+    m_run = m_new;
+    // ---- P.V: this warp's head_dim slice over the chunk's tokens ---------------
+#pragma unroll
+    for (int i = 0; i < kDT; ++i)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[i][e] *= f;
+    for (int kk = 0; kk * 16 < n; ++kk) {  // 16 tokens per step
+      uint32_t pa[4];
+      ldsm_x4(pa, p_base + (((lane & 7) + ((lane >> 3) & 1) * 8) * Lay::kPStride + kk * 16 +
+                            (lane >> 4) * 8) * 2);
+      const int jv = jb0 + (kk * 16) / BS, sv = (kk * 16) % BS;
+      const uint32_t vblk =
+          ring_base + (jv % Lay::kStages) * Lay::kStageBytes + Lay::kBlockBytes;
+#pragma unroll
+      for (int i = 0; i < kDT; ++i) {
+        const int d0 = warp * (D / 4) + i * 8;
+        uint32_t vb[2];
+        // B: head_dim rows d0 .. d0 + 7, tokens sv + 8 ((lane / 8) % 2) .. + 7
+        ldsm_x2(vb, vblk + ((d0 + (lane & 7)) * BS + sv + ((lane >> 3) & 1) * 8) * 2);
+        mma16816<T>(acc[i], pa, vb);
+      }
+    }
+    consumer_sync();  // the P tile and the reductions are read before the next chunk
+    if (lane == 0)
+      for (int j = jb0; j < jb0 + nb; ++j) sm100::mbar_arrive(&empty[j % Lay::kStages]);
+  }
+
+  // ---- epilogue: O[g] = (rows g + rows g + 8) / s ----------------------------------
+  poison |= flags[1] != 0 || *abort_flag != 0;
+  if (g < G) {
+    const int64_t row = row0 + g;
+#pragma unroll
+    for (int i = 0; i < kDT; ++i) {
+      const int d = warp * (D / 4) + i * 8 + 2 * t;
+      const float o0 = poison ? qnan() : (acc[i][0] + acc[i][2]) / s_run;
+      const float o1 = poison ? qnan() : (acc[i][1] + acc[i][3]) / s_run;
+      if (kV2 && !direct) {
+        float* dst = a.tmp_out + (row * a.num_partitions + part) * D + d;
+        dst[0] = o0;
+        dst[1] = o1;
+      } else {
+        store_out(a.out, row * D + d, a.out_dtype, o0);
+        store_out(a.out, row * D + d + 1, a.out_dtype, o1);
+      }
+    }
+    if (kV2 && !direct && warp == 0 && t == 0) {
+      const int64_t w = row * a.num_partitions + part;
+      a.max_logits[w] = poison ? qnan() : m_run * kLn2;
+      a.exp_sums[w] = s_run;
+    }
+  }
+}
+
+template <typename T, int D, int BS>
+cudaError_t launch_sx_t(const KernelArgs& a, bool v2, cudaStream_t s) {
+  using Lay = sx::Layout<D, BS>;
+  const dim3 grid(v2 ? a.num_partitions : 1, a.num_kv_heads, a.num_seqs);
+  auto kern = v2 ? pa_sx_kernel<T, D, BS, true> : pa_sx_kernel<T, D, BS, false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, sx::kThreads, Lay::kSmem, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_sx_dtype(const KernelArgs& a, bool v2, cudaStream_t s) {
+  switch (a.head_dim * 100 + a.block_size) {
+    case 25616: return launch_sx_t<T, 256, 16>(a, v2, s);
+    case 25632: return launch_sx_t<T, 256, 32>(a, v2, s);
+    case 12816: return launch_sx_t<T, 128, 16>(a, v2, s);
+    case 12832: return launch_sx_t<T, 128, 32>(a, v2, s);
+    case 6416: return launch_sx_t<T, 64, 16>(a, v2, s);
+    case 6432: return launch_sx_t<T, 64, 32>(a, v2, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace pa

@@ -1,0 +1,11 @@
+// pa_sx_bf16.cu -- instantiates the split-x tensor-core decode kernels for bf16
+// caches (one translation unit per element type, compiled in parallel).
+#include "pa_sx.cuh"
+
+namespace pa {
+
+cudaError_t launch_sx_bf16(const KernelArgs& a, bool v2, cudaStream_t s) {
+  return launch_sx_dtype<__nv_bfloat16>(a, v2, s);
+}
+
+}  // namespace pa

@@ -109,6 +109,15 @@ bool tc_applicable(const pa_params_t* p) {
   return encoder() != nullptr && device_info().state == 1;
 }
 
+bool sx_applicable(const pa_params_t* p) {
+  if ((p->flags & PA_FLAG_SPLIT_X) == 0 || (p->flags & PA_FLAG_PORTABLE)) return false;
+  if (p->kv_dtype != PA_BF16 && p->kv_dtype != PA_F16) return false;
+  if (p->num_heads / p->num_kv_heads > 8) return false;
+  const int D = p->head_dim, BS = p->block_size;
+  if (!(D == 64 || D == 128 || D == 256) || !(BS == 16 || BS == 32)) return false;
+  return device_info().state == 1;
+}
+
 cudaError_t launch_tc(const KernelArgs& a, pa_dtype_t kv, bool v2, cudaStream_t s) {
   auto enc = encoder();
   if (!enc) return cudaErrorNotSupported;

@@ -485,8 +485,8 @@ def test_cuda_graph_capture_and_replay():
 
 
 def _split_x(bc):
-    """The caches of `bc` rewritten (on the host, as test input) into the
-    split-x layout: keys [blocks, kv_heads, head_dim / x, block_size, x],
+    """The caches of `bc` rewritten (as test input, on the batch's device) into
+    the split-x layout: keys [blocks, kv_heads, head_dim / x, block_size, x],
     values [blocks, kv_heads, head_dim, block_size], x = 16 / element bytes."""
     nb, hkv, bs, d = bc.k_cache.shape
     x = 16 // bc.k_cache.element_size()
@@ -496,37 +496,70 @@ def _split_x(bc):
 
 
 @pytest.mark.parametrize("dtype,D,BS", [(torch.bfloat16, 256, 16), (torch.float16, 128, 32),
-                                        (torch.float32, 64, 16), (torch.float32, 256, 32),
-                                        (torch.bfloat16, 64, 8)])
+                                        (torch.bfloat16, 64, 32), (torch.float32, 64, 16),
+                                        (torch.float32, 256, 32), (torch.bfloat16, 64, 8)])
 def test_split_x_layout(dtype, D, BS):
-    """PA_FLAG_SPLIT_X: the caches in the pages' V1 layout, read directly: the
-    same bits as the standard layout on the same (CUDA-core) kernels, and the
-    oracle's result within the tolerance, on V1, V2 and pa_decode."""
+    """PA_FLAG_SPLIT_X: the caches in the pages' V1 layout, read directly, on
+    V1, V2 and pa_decode.  The CUDA-core kernels (PA_FLAG_PORTABLE, and the
+    only kernels for float32 or block size 8) give the same bits as on the
+    standard layout; the split-x tensor-core kernel (bf16 / f16, block 16 or
+    32) matches the oracle and the CUDA-core kernels within the tolerance."""
     lens = (1, BS - 1, 300, 777, 0, 1500)
     bc = problem(dtype=dtype, lens=lens, Hq=12, Hkv=3, D=D, BS=BS, seed=21)
     ref = _ref(bc)
     bg = bc.to("cuda")
     k5, v4 = (t.cuda() for t in _split_x(bc))
     kw = dict(max_seq_len=bc.max_seq_len, scale=bc.scale)
+    tensor_core = dtype != torch.float32 and BS in (16, 32)
+    params = pa.make_params(bc.q, k5, bc.block_tables, partition_size=256,
+                            out_dtype=torch.float32, split_x=True, **kw)
+    assert pa.decode_kernel(params) == (2 if tensor_core else 1)
     for path in ("v1", "v2", "decode"):
         want = run(bg, path=path, partition_size=256, portable=True, v1_max_seq_len=1024)
-        got = torch.full(tuple(bc.q.shape), float("nan"), device="cuda")
-        params = pa.make_params(bc.q, k5, bc.block_tables, partition_size=256,
-                                out_dtype=torch.float32, split_x=True, **kw)
-        ws = pa.alloc_workspace(params)
-        if path == "v1":
-            pa.decode_v1(bg.q, k5, v4, bg.block_tables, bg.seq_lens, got, split_x=True, **kw)
-        elif path == "v2":
-            pa.decode_v2(bg.q, k5, v4, bg.block_tables, bg.seq_lens, got, ws, partition_size=256,
-                         split_x=True, **kw)
-        else:
-            pa.decode(bg.q, k5, v4, bg.block_tables, bg.seq_lens, got, ws, partition_size=256,
-                      v1_max_seq_len=1024, split_x=True, **kw)
-        torch.cuda.synchronize()
-        g = got.double().cpu().numpy()
-        assert np.array_equal(g, want), f"split-x {path} differs from the standard layout"
-        assert_close(g, ref, TOL[dtype], f"split-x {path}")
-        assert pa.read_device_status(ws) == pa.PA_OK
+        for portable in ((False, True) if tensor_core else (True,)):
+            got = torch.full(tuple(bc.q.shape), float("nan"), device="cuda")
+            ws = pa.alloc_workspace(params)
+            kx = dict(split_x=True, portable=portable, **kw)
+            if path == "v1":
+                pa.decode_v1(bg.q, k5, v4, bg.block_tables, bg.seq_lens, got, **kx)
+            elif path == "v2":
+                pa.decode_v2(bg.q, k5, v4, bg.block_tables, bg.seq_lens, got, ws,
+                             partition_size=256, **kx)
+            else:
+                pa.decode(bg.q, k5, v4, bg.block_tables, bg.seq_lens, got, ws, partition_size=256,
+                          v1_max_seq_len=1024, **kx)
+            torch.cuda.synchronize()
+            g = got.double().cpu().numpy()
+            what = f"split-x {path} {'CUDA-core' if portable else 'tensor-core'}"
+            if portable:
+                assert np.array_equal(g, want), f"{what} differs from the standard layout"
+            else:
+                assert max_err(g, want) <= TOL[dtype], what
+            assert_close(g, ref, TOL[dtype], what)
+            assert pa.read_device_status(ws) == pa.PA_OK
+
+
+def test_split_x_full_size_long_context():
+    """The 100K-token long-context workload with its caches rewritten (on the
+    device, as test input) into the split-x layout: pa_decode (V2) on the
+    split-x tensor-core kernel against the oracle on every row, and a block id
+    outside the pool poisons only its sequence's rows."""
+    w = wl.WORKLOADS["long_100k"]
+    bg = wl.make(w, device="cuda", poison=True)
+    bc = bg.to("cpu")
+    ref = oracle.decode(bc.q, bc.k_cache, bc.v_cache, bc.block_tables, bc.seq_lens, bc.scale)
+    k5, v4 = _split_x(bg)
+    params = pa.make_params(bg.q, k5, bg.block_tables, max_seq_len=bg.max_seq_len,
+                            scale=bg.scale, partition_size=512, out_dtype=torch.float32,
+                            split_x=True)
+    assert pa.decode_kernel(params) == 2 and pa.decode_path(params) == 2
+    ws = pa.alloc_workspace(params)
+    out = torch.full(tuple(bg.q.shape), float("nan"), device="cuda")
+    pa.decode(bg.q, k5, v4, bg.block_tables, bg.seq_lens, out, ws, max_seq_len=bg.max_seq_len,
+              scale=bg.scale, partition_size=512, split_x=True)
+    torch.cuda.synchronize()
+    assert_close(out.double().cpu().numpy(), ref, TOL[w.dtype], "split-x long_100k")
+    assert pa.read_device_status(ws) == pa.PA_OK
 
 
 # ---------------------------------------------------------------------------
