@@ -70,9 +70,9 @@ __device__ __forceinline__ Sync* sync_words(const KernelArgs& a) {
   return reinterpret_cast<Sync*>(reinterpret_cast<char*>(a.status) + kSyncOffset);
 }
 
-__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
   uint32_t v;
-  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
 __device__ __forceinline__ unsigned long long ld_relaxed64(const unsigned long long* p) {
@@ -80,8 +80,10 @@ __device__ __forceinline__ unsigned long long ld_relaxed64(const unsigned long l
   asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
-__device__ __forceinline__ void red_add(uint32_t* p, uint32_t v) {
-  asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+// release: this thread's earlier writes, and those ordered before it by a CTA
+// barrier, are visible to whoever acquires the count
+__device__ __forceinline__ void red_add_release(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 __device__ __forceinline__ void red_add64(unsigned long long* p, unsigned long long v) {
   asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
@@ -254,17 +256,20 @@ __device__ __noinline__ void reduce_unit(const KernelArgs& a, const CUtensorMap*
 // pass 2 become NaN, split statically over the CTAs).  `started` is thread
 // 0's count_started() result; `w` three shared ints for broadcasts; `sc` the
 // unit's shared scratch; `pmap` / `bar`: the tile copy of the partials and
-// its mbarrier (initialised, phase 0).
+// its mbarrier (initialised, phase 0).  `dry`: the same code with no effect
+// (counts of 0, one poll, no unit), run at the kernel's start so that the
+// code is in the instruction cache at the end -- hence out of line.
 template <int D>
-__device__ void grid_reduce(const KernelArgs& a, bool ws_ok, unsigned long long started, int* w,
-                            UnitScratch& sc, const CUtensorMap* pmap, uint64_t* bar, int tid,
-                            long long budget) {
+__device__ __noinline__ void grid_reduce(const KernelArgs& a, bool ws_ok,
+                                         unsigned long long started, int* w, UnitScratch& sc,
+                                         const CUtensorMap* pmap, uint64_t* bar, int tid,
+                                         long long budget, bool dry) {
   constexpr int kSlices = D / kSlice;
   const int64_t units = static_cast<int64_t>(a.num_seqs) * a.num_heads * kSlices;
   auto seq_len_of = [&](int64_t u) { return __ldg(a.seq_lens + u / kSlices / a.num_heads); };
   uint32_t phase = 0;
   if (!ws_ok) {
-    for (int64_t u = blockIdx.x; u < units; u += gridDim.x)
+    for (int64_t u = blockIdx.x; u < units && !dry; u += gridDim.x)
       reduce_unit<D>(a, pmap, bar, phase, u, seq_len_of(u), sc, tid, true, budget, false);
     return;
   }
@@ -272,15 +277,15 @@ __device__ void grid_reduce(const KernelArgs& a, bool ws_ok, unsigned long long 
   const uint32_t grid = gridDim.x;
   const uint32_t epoch = static_cast<uint32_t>(started >> 32);
   const int bank = epoch & 1;
+  const uint32_t one = dry ? 0u : 1u;
   if (tid == 0) {
     const uint32_t rank = static_cast<uint32_t>(started);
-    __threadfence();  // release: every thread's partials precede the count
-    red_add(&s->finished[bank], 1u);
-    if (rank == 0) {  // the other bank: used by the last launch, next by the next one
+    red_add_release(&s->finished[bank], one);  // every thread's partials precede the count
+    if (rank == 0 && !dry) {  // the other bank: used by the last launch, next by the next one
       s->finished[bank ^ 1] = 0u;
       s->queue[bank ^ 1] = 0u;
     }
-    if (rank == grid - 1)  // the last CTA to start: the next launch's epoch
+    if (rank == grid - 1 && !dry)  // the last CTA to start: the next launch's epoch
       red_add64(&s->start, (1ull << 32) - grid);
     // every CTA has started when the count is complete or the epoch moved on
     const unsigned long long now = ld_relaxed64(&s->start);
@@ -289,12 +294,14 @@ __device__ void grid_reduce(const KernelArgs& a, bool ws_ok, unsigned long long 
     int unit = static_cast<int>(units);  // none
     int timed_out = 0;
     int32_t L = 0;
-    if (all) {
-      unit = static_cast<int>(atomicAdd(&s->queue[bank], 1u));
-      if (unit < units) {
-        L = seq_len_of(unit);  // an input: read while the others finish
+    if (all || dry) {
+      const int got = static_cast<int>(atomicAdd(&s->queue[bank], one));
+      if (!dry) unit = got;
+      if (unit < units || dry) {
+        L = seq_len_of(dry ? 0 : unit);  // an input: read while the others finish
         const long long t0 = clock64();
-        while (ld_relaxed(&s->finished[bank]) < grid) {  // every CTA's partials stored
+        while (ld_acquire(&s->finished[bank]) < grid) {  // every CTA's partials stored
+          if (dry) break;
           if (clock64() - t0 > budget) {
             set_status(a.status, PA_ERR_DEVICE_TIMEOUT);
             timed_out = 1;  // this CTA's units are written as NaN
@@ -302,7 +309,6 @@ __device__ void grid_reduce(const KernelArgs& a, bool ws_ok, unsigned long long 
           }
           __nanosleep(64);
         }
-        __threadfence();  // acquire
       }
     }
     w[0] = unit;

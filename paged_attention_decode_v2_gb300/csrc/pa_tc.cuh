@@ -698,6 +698,9 @@ __global__ void __launch_bounds__(tc::kThreads, CPS)
     static_assert(gridred::kDryBytes <= (kChunk / 16) * 512, "dry run within the P^T buffer");
     if (kV2 && !kClusters && a.fused && c.ws_ok) {
       uint32_t dry_phase = 0;
+      gridred::grid_reduce<D>(a, true, started, c.red_word,
+                              *reinterpret_cast<gridred::UnitScratch*>(pt), &pmap, &c.red_bar,
+                              tid, budget, true);
       gridred::reduce_unit<D>(a, &pmap, &c.red_bar, dry_phase, 0, 0,
                               *reinterpret_cast<gridred::UnitScratch*>(pt), tid, false, budget,
                               true);
@@ -881,7 +884,7 @@ __global__ void __launch_bounds__(tc::kThreads, CPS)
   if (kV2 && !kClusters && a.fused && warp < 4)
     gridred::grid_reduce<D>(a, c.ws_ok != 0, started, c.red_word,
                             *reinterpret_cast<gridred::UnitScratch*>(ring), &pmap, &c.red_bar, tid,
-                            budget);
+                            budget, false);
   // no CTA leaves while a peer may still read its shared memory
   if (cs > 1) sm100::cluster_sync_all();
 }
