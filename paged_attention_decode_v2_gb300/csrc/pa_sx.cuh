@@ -17,9 +17,13 @@
 //
 // Work item: one (sequence, KV head, token range), the range a V2 partition
 // or the whole sequence (V1); the G <= 8 query heads of the KV head are
-// served together.  One CTA per item: warp 4 streams the range's blocks into
-// a ring of whole blocks (keys and values), warps 0-3 consume it in chunks
-// of 32 tokens:
+// served together.  The grid is persistent (at most two CTAs per SM, the
+// items dealt out in balanced rounds): CTA c takes items c, c + gridDim.x,
+// ...  Warp 4 streams the blocks of all its items, one after the other, into
+// one ring of whole blocks (keys and values), so the next item's blocks are
+// in flight while the current one finishes, and loads each item's q rows by
+// bulk copy into one of two q tiles; warps 0-3 consume the ring in chunks of
+// 32 tokens:
 //   QK^T   warp w: S[h, t] for the chunk's 8 tokens 8w .. 8w + 7, over all of
 //          head_dim (A = q, rows 0..7 = the query heads; B = keys);
 //   softmax the chunk's max per head across the four warps (shared memory),
@@ -100,6 +104,8 @@ __device__ __forceinline__ uint32_t pack2(T lo, T hi) {
   return static_cast<uint32_t>(bits16(lo)) | (static_cast<uint32_t>(bits16(hi)) << 16);
 }
 
+constexpr int kQRows = 8;  // q tile rows: the query heads of one KV head
+
 template <int D, int BS>
 struct Layout {
   static constexpr int kBlockBytes = BS * D * 2;            // one block of one cache
@@ -108,106 +114,152 @@ struct Layout {
       kRingBytes / kStageBytes < kMaxStages ? kRingBytes / kStageBytes : kMaxStages;
   static constexpr int kChunkBlocks = kChunk / BS > 0 ? kChunk / BS : 1;
   static constexpr int kQStride = D + 8;                     // q tile row (elements), padded
+  static constexpr int kQTile = kQRows * kQStride;           // elements of one q tile
   static constexpr int kPStride = kChunk + 8;                // P tile row (elements), padded
-  static constexpr int kQOff = kStages * kStageBytes;
-  static constexpr int kPOff = kQOff + 16 * kQStride * 2;
+  static constexpr int kQOff = kStages * kStageBytes;        // two q tiles
+  static constexpr int kPOff = kQOff + 2 * kQTile * 2;
   static constexpr int kRedOff = kPOff + 16 * kPStride * 2;  // [4 warps][8 heads] max, sum
   static constexpr int kBarOff = kRedOff + 2 * kConsumerWarps * 8 * 4;
-  static constexpr int kSmem = kBarOff + (2 * kMaxStages + 2) * 8 + 64;
+  // full[kMaxStages], empty[kMaxStages], qfull[2], qempty[2]
+  static constexpr int kFlagOff = kBarOff + (2 * kMaxStages + 4) * 8;
+  // [0] abort; [1 + s] ring slot s holds no block (its id was out of range)
+  static constexpr int kSmem = kFlagOff + (1 + kMaxStages) * 4 + 64;
   static_assert(kStages >= 2 * kChunkBlocks, "two chunks in flight");
+  static_assert((kQStride * 2) % 16 == 0 && kQOff % 16 == 0, "bulk copies of q rows");
   static_assert(kSmem <= 113 * 1024, "two CTAs per SM");
 };
+
+// One work item, decoded the same way by the producer and the consumers.
+struct Item {
+  int b, kvh, part;
+  int32_t t0, t1;  // token range (empty when t0 >= t1)
+  bool len_ok;     // 0 <= seq_len <= max_seq_len
+  bool direct;     // V2 with single_direct: the result is the final output
+  int nblk;        // blocks of the range (0 when it is empty)
+};
+
+// Item k of the (partition, sequence, KV head) space, partition-major for V2
+// (ranges past a sequence's end come out empty), (sequence, KV head) for V1.
+template <int BS>
+__device__ __forceinline__ Item item_at(const KernelArgs& a, int64_t k, bool v2) {
+  Item it;
+  const int64_t per_part = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads;
+  it.part = v2 ? static_cast<int>(k / per_part) : 0;
+  const int64_t rem = v2 ? k % per_part : k;
+  it.b = static_cast<int>(rem / a.num_kv_heads);
+  it.kvh = static_cast<int>(rem % a.num_kv_heads);
+  const int32_t L = __ldg(a.seq_lens + it.b);
+  it.len_ok = seq_len_ok(a, L);
+  it.t0 = v2 ? it.part * a.partition_size : 0;  // a multiple of BS
+  it.t1 = !it.len_ok ? it.t0 : (v2 ? min(L, it.t0 + a.partition_size) : L);
+  it.direct = v2 && a.single_direct && it.len_ok && L <= a.partition_size;
+  it.nblk = it.t0 < it.t1 ? (it.t1 - 1) / BS - it.t0 / BS + 1 : 0;
+  return it;
+}
 
 }  // namespace sx
 
 template <typename T, int D, int BS, bool kV2>
-__global__ void __launch_bounds__(sx::kThreads, 2) pa_sx_kernel(const KernelArgs a) {
+__global__ void __launch_bounds__(sx::kThreads, 2)
+    pa_sx_kernel(const KernelArgs a, int64_t total_items) {
   using namespace sx;
   using Lay = Layout<D, BS>;
   static_assert(BS == 16 || BS == 32, "block size");
   extern __shared__ __align__(128) uint8_t smem[];
   uint8_t* ring = smem;
-  T* qs = reinterpret_cast<T*>(smem + Lay::kQOff);
+  T* qs = reinterpret_cast<T*>(smem + Lay::kQOff);  // two tiles of kQRows x kQStride
   T* ps = reinterpret_cast<T*>(smem + Lay::kPOff);
   float* red_max = reinterpret_cast<float*>(smem + Lay::kRedOff);
   float* red_sum = red_max + kConsumerWarps * 8;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Lay::kBarOff);
   uint64_t* empty = full + kMaxStages;
-  int* flags = reinterpret_cast<int*>(empty + kMaxStages);  // [0] abort, [1] bad block
+  uint64_t* qfull = empty + kMaxStages;
+  uint64_t* qempty = qfull + 2;
+  int* flags = reinterpret_cast<int*>(smem + Lay::kFlagOff);
+  volatile int* abort_flag = &flags[0];
+  volatile int* bad = flags + 1;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int b = blockIdx.z, kvh = blockIdx.y, part = blockIdx.x;
   const int G = a.group, Hq = a.num_heads;
-  const int32_t L = __ldg(a.seq_lens + b);
-  const int64_t row0 = static_cast<int64_t>(b) * Hq + kvh * G;
-
-  if (!seq_len_ok(a, L)) {
-    if (tid == 0 && part == 0) set_status(a.status, PA_ERR_BAD_SEQ_LEN);
-    if (!kV2)  // V1 writes the NaN rows; for V2 the reduce does
-      for (int i = tid; i < G * D; i += kThreads) store_out(a.out, row0 * D + i, a.out_dtype, qnan());
-    return;
-  }
-  const int32_t t0 = kV2 ? part * a.partition_size : 0;
-  if (kV2 && t0 >= L) return;  // this sequence has no such partition
-  const int32_t t1 = kV2 ? min(L, t0 + a.partition_size) : L;
-  const bool direct = kV2 && a.single_direct && L <= a.partition_size;
-  if (t0 >= t1) {  // V1 row of an empty sequence
-    for (int i = tid; i < G * D; i += kThreads) store_out(a.out, row0 * D + i, a.out_dtype, 0.f);
-    return;
-  }
-  const int nblk = (t1 - 1) / BS - t0 / BS + 1;  // t0 is a multiple of BS
+  const T zero = round16(0.f, static_cast<T*>(nullptr));
 
   // ---- set-up ---------------------------------------------------------------------
   if (tid == 0) {
     for (int s = 0; s < Lay::kStages; ++s) {
       sm100::mbar_init(&full[s], 1);
       sm100::mbar_init(&empty[s], kConsumerWarps);
+      bad[s] = 0;
+    }
+    for (int i = 0; i < 2; ++i) {
+      sm100::mbar_init(&qfull[i], 1);
+      sm100::mbar_init(&qempty[i], kConsumerWarps);
     }
     flags[0] = 0;
-    flags[1] = 0;
   }
-  // q tile: rows 0..G-1 the query heads, rows G..15 zero
-  for (int i = tid; i < 16 * D; i += kThreads) {
-    const int r = i / D, d = i % D;
-    const T v = r < G ? static_cast<const T*>(a.q)[(row0 + r) * D + d] : round16(0.f, static_cast<T*>(nullptr));
-    qs[r * Lay::kQStride + d] = v;
+  // rows G .. 7 of both q tiles stay zero; the bulk copies fill rows 0 .. G-1
+  for (int i = tid; i < 2 * kQRows * D; i += kThreads) {
+    const int r = (i / D) % kQRows, tile = i / (kQRows * D);
+    if (r >= G) qs[tile * Lay::kQTile + r * Lay::kQStride + i % D] = zero;
   }
   __syncthreads();
-  volatile int* abort_flag = &flags[0];
 
   if (warp == kConsumerWarps) {
     // ========================= producer =======================================
     const uint64_t policy = sm100::l2_evict_first_policy();
-    const int32_t* bt = a.block_tables + static_cast<int64_t>(b) * a.max_blocks_per_seq + t0 / BS;
+    const uint64_t qpolicy = sm100::l2_evict_last_policy();  // q: read once per partition
     const char* kc = static_cast<const char*>(a.k_cache);
     const char* vc = static_cast<const char*>(a.v_cache);
+    const char* qg = static_cast<const char*>(a.q);
     bool ok = true;
-    int issued = 0;
-    for (int j0 = 0; j0 < nblk && ok; j0 += 32) {
-      const int32_t id_l = j0 + lane < nblk ? __ldg(bt + j0 + lane) : 0;
-      const int n32 = min(32, nblk - j0);
-      for (int jj = 0; jj < n32 && ok; ++jj) {
-        const int j = j0 + jj;
-        const int slot = j % Lay::kStages;
-        ok = sm100::mbar_wait(&empty[slot], ((j / Lay::kStages) & 1) ^ 1, kWaitBudget, abort_flag);
-        if (!ok) break;
-        const int32_t id = __shfl_sync(0xffffffffu, id_l, jj);
-        if (lane == 0) {
-          if (id < 0 || id >= a.num_blocks) {  // never read: the item becomes NaN
-            flags[1] = 1;
-            set_status(a.status, PA_ERR_BAD_BLOCK_ID);
-            sm100::mbar_arrive(&full[slot]);
-          } else {
-            const int64_t off =
-                (static_cast<int64_t>(id) * a.num_kv_heads + kvh) * Lay::kBlockBytes;
-            uint8_t* st = ring + slot * Lay::kStageBytes;
-            sm100::mbar_arrive_expect_tx(&full[slot], Lay::kStageBytes);
-            bulk_g2s(st, kc + off, Lay::kBlockBytes, &full[slot], policy);
-            bulk_g2s(st + Lay::kBlockBytes, vc + off, Lay::kBlockBytes, &full[slot], policy);
+    uint32_t jg = 0;  // ring blocks issued, over all items (a CTA streams far
+                      // fewer than 2^32 blocks, so 32 bits keep the slot
+                      // arithmetic short)
+    int nq = 0;      // q tiles issued
+    for (int64_t k = blockIdx.x; k < total_items && ok; k += gridDim.x) {
+      const Item it = item_at<BS>(a, k, kV2);
+      if (it.nblk == 0) continue;
+      const int qb = nq & 1;
+      ok = __all_sync(0xffffffffu, sm100::mbar_wait(&qempty[qb], ((nq >> 1) & 1) ^ 1,
+                                                    kWaitBudget, abort_flag));
+      if (!ok) break;
+      if (lane == 0) {
+        const int64_t row0 = static_cast<int64_t>(it.b) * Hq + static_cast<int64_t>(it.kvh) * G;
+        sm100::mbar_arrive_expect_tx(&qfull[qb], G * D * 2);
+        for (int r = 0; r < G; ++r)
+          bulk_g2s(qs + qb * Lay::kQTile + r * Lay::kQStride, qg + (row0 + r) * D * 2, D * 2,
+                   &qfull[qb], qpolicy);
+      }
+      __syncwarp();
+      ++nq;
+      const int32_t* bt =
+          a.block_tables + static_cast<int64_t>(it.b) * a.max_blocks_per_seq + it.t0 / BS;
+      for (int j0 = 0; j0 < it.nblk && ok; j0 += 32) {
+        const int32_t id_l = j0 + lane < it.nblk ? __ldg(bt + j0 + lane) : 0;
+        const int n32 = min(32, it.nblk - j0);
+        for (int jj = 0; jj < n32; ++jj, ++jg) {
+          const int slot = static_cast<int>(jg % Lay::kStages);
+          const uint32_t par = static_cast<uint32_t>((jg / Lay::kStages) & 1) ^ 1;
+          ok = __all_sync(0xffffffffu,
+                          sm100::mbar_wait(&empty[slot], par, kWaitBudget, abort_flag));
+          if (!ok) break;
+          const int32_t id = __shfl_sync(0xffffffffu, id_l, jj);
+          if (lane == 0) {
+            if (id < 0 || id >= a.num_blocks) {  // never read: the item becomes NaN
+              bad[slot] = 1;
+              set_status(a.status, PA_ERR_BAD_BLOCK_ID);
+              sm100::mbar_arrive(&full[slot]);
+            } else {
+              bad[slot] = 0;
+              const int64_t off =
+                  (static_cast<int64_t>(id) * a.num_kv_heads + it.kvh) * Lay::kBlockBytes;
+              uint8_t* st = ring + slot * Lay::kStageBytes;
+              sm100::mbar_arrive_expect_tx(&full[slot], Lay::kStageBytes);
+              bulk_g2s(st, kc + off, Lay::kBlockBytes, &full[slot], policy);
+              bulk_g2s(st + Lay::kBlockBytes, vc + off, Lay::kBlockBytes, &full[slot], policy);
+            }
           }
+          __syncwarp();
         }
-        __syncwarp();
-        issued = j + 1;
       }
     }
     if (!ok) {
@@ -216,8 +268,11 @@ __global__ void __launch_bounds__(sx::kThreads, 2) pa_sx_kernel(const KernelArgs
         set_status(a.status, PA_ERR_DEVICE_TIMEOUT);
       }
       // copies issued must land before the CTA may exit
-      for (int j = issued > Lay::kStages ? issued - Lay::kStages : 0; j < issued; ++j)
-        sm100::mbar_wait(&full[j % Lay::kStages], (j / Lay::kStages) & 1, kWaitBudget, nullptr);
+      for (uint32_t j = jg > Lay::kStages ? jg - Lay::kStages : 0; j < jg; ++j)
+        sm100::mbar_wait(&full[j % Lay::kStages], static_cast<uint32_t>((j / Lay::kStages) & 1),
+                         kWaitBudget, nullptr);
+      for (int i = nq > 2 ? nq - 2 : 0; i < nq; ++i)
+        sm100::mbar_wait(&qfull[i & 1], (i >> 1) & 1, kWaitBudget, nullptr);
     }
     return;
   }
@@ -225,144 +280,176 @@ __global__ void __launch_bounds__(sx::kThreads, 2) pa_sx_kernel(const KernelArgs
   // =========================== consumers (warps 0-3) ================================
   const int g = lane >> 2, t = lane & 3;  // mma fragment: row group, column pair
   const float sl2 = a.scale_log2;
-  const uint32_t q_base = sm100::smem_u32(qs);
   const uint32_t p_base = sm100::smem_u32(ps);
   const uint32_t ring_base = sm100::smem_u32(ring);
   constexpr int kDT = D / 4 / 8;  // 8-wide head_dim tiles of this warp's P.V slice
-  float acc[kDT][4];
-#pragma unroll
-  for (int i = 0; i < kDT; ++i)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) acc[i][e] = 0.f;
-  float m_run = -INFINITY, s_run = 0.f;  // for head g (rows g and g + 8)
-  bool poison = false;
-  const int nchunks = (t1 - t0 + kChunk - 1) / kChunk;
-  for (int ci = 0; ci < nchunks; ++ci) {
-    const int c0 = t0 + ci * kChunk;
-    const int n = min(kChunk, t1 - c0);
-    const int jb0 = (c0 - t0) / BS;  // first block of the chunk within the item
-    const int nb = (n + BS - 1) / BS;
-    // every block of the chunk landed
-    for (int jb = jb0; jb < jb0 + nb; ++jb)
-      if (!sm100::mbar_wait(&full[jb % Lay::kStages], (jb / Lay::kStages) & 1, kWaitBudget,
-                            abort_flag)) {
-        poison = true;
-        if (lane == 0) {
-          flags[0] = 1;
-          set_status(a.status, PA_ERR_DEVICE_TIMEOUT);
-        }
+  uint32_t jg = 0;                // ring blocks consumed, over all items
+  int nq = 0;                     // q tiles consumed
+  for (int64_t k = blockIdx.x; k < total_items; k += gridDim.x) {
+    const Item it = item_at<BS>(a, k, kV2);
+    const int64_t row0 = static_cast<int64_t>(it.b) * Hq + static_cast<int64_t>(it.kvh) * G;
+    if (it.nblk == 0) {
+      if (!it.len_ok && tid == 0 && it.part == 0) set_status(a.status, PA_ERR_BAD_SEQ_LEN);
+      if (!kV2) {  // V1: NaN rows for a bad length, zero rows for an empty sequence
+        const float v = it.len_ok ? 0.f : qnan();
+        for (int i = tid; i < G * D; i += kConsumerWarps * 32)
+          store_out(a.out, row0 * D + i, a.out_dtype, v);
       }
-    // ---- QK^T: this warp's 8 tokens 8w .. 8w + 7 of the chunk --------------------
-    const int tk = warp * 8;  // first token of the n-tile within the chunk
-    const int jb = jb0 + tk / BS, so = tk % BS;
-    const uint32_t kblk = ring_base + (jb % Lay::kStages) * Lay::kStageBytes;
-    float sc[4] = {0.f, 0.f, 0.f, 0.f};
-    if (tk < n) {
-#pragma unroll 4
-      for (int ks = 0; ks < D / 16; ++ks) {
-        uint32_t qa[4], kb[2];
-        // A: rows (lane % 8) + 8 ((lane / 8) % 2), columns 16 ks + 8 (lane / 16)
-        ldsm_x4(qa, q_base + (((lane & 7) + ((lane >> 3) & 1) * 8) * Lay::kQStride + ks * 16 +
-                              (lane >> 4) * 8) * 2);
-        // B: tokens so .. so + 7 of key groups 2 ks and 2 ks + 1 (16 bytes each)
-        ldsm_x2(kb, kblk + (((2 * ks + ((lane >> 3) & 1)) * BS + so + (lane & 7)) * 16));
-        mma16816<T>(sc, qa, kb);
+      continue;  // V2: the reduce writes those rows
+    }
+    const int qb = nq & 1;
+    bool poison = false;
+    if (!sm100::mbar_wait(&qfull[qb], (nq >> 1) & 1, kWaitBudget, abort_flag)) {
+      poison = true;
+      if (lane == 0) {
+        flags[0] = 1;
+        set_status(a.status, PA_ERR_DEVICE_TIMEOUT);
       }
     }
-    // logits of head g, tokens tk + 2t, tk + 2t + 1 (c[0], c[1]); c[2], c[3] are padding
-    float l0 = (tk + 2 * t < n) ? sc[0] * sl2 : -INFINITY;
-    float l1 = (tk + 2 * t + 1 < n) ? sc[1] * sl2 : -INFINITY;
-    if (g >= G) l0 = l1 = -INFINITY;
-    float mx = fmaxf(l0, l1);
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    if (t == 0) red_max[warp * 8 + g] = mx;
-    consumer_sync();
-    float mc = red_max[g];
-#pragma unroll
-    for (int w = 1; w < kConsumerWarps; ++w) mc = fmaxf(mc, red_max[w * 8 + g]);
-    const float m_new = fmaxf(m_run, mc);
-    const float p0 = l0 == -INFINITY ? 0.f : exp2f(l0 - m_new);
-    const float p1 = l1 == -INFINITY ? 0.f : exp2f(l1 - m_new);
-    float ssum = p0 + p1;
-    ssum += __shfl_xor_sync(0xffffffffu, ssum, 1);
-    ssum += __shfl_xor_sync(0xffffffffu, ssum, 2);
-    if (t == 0) red_sum[warp * 8 + g] = ssum;
-    // P tile: row g = the hi parts, row g + 8 = the remainders, tokens tk + 2t, +1
-    {
-      const T h0 = round16(p0, static_cast<T*>(nullptr)), h1 = round16(p1, static_cast<T*>(nullptr));
-      const T r0 = round16(p0 - to_float(h0), static_cast<T*>(nullptr));
-      const T r1 = round16(p1 - to_float(h1), static_cast<T*>(nullptr));
-      *reinterpret_cast<uint32_t*>(ps + g * Lay::kPStride + tk + 2 * t) = pack2<T>(h0, h1);
-      *reinterpret_cast<uint32_t*>(ps + (g + 8) * Lay::kPStride + tk + 2 * t) = pack2<T>(r0, r1);
-    }
-    // the tail block: value columns past the range are cleared (P is 0 there,
-    // but 0 * NaN would be NaN)
-    if (n < nb * BS) {
-      const int jt = jb0 + nb - 1;
-      T* vt = reinterpret_cast<T*>(ring + (jt % Lay::kStages) * Lay::kStageBytes + Lay::kBlockBytes);
-      const int valid = n - (nb - 1) * BS;
-      const T zero = round16(0.f, static_cast<T*>(nullptr));
-      for (int i = tid; i < D * (BS - valid); i += 128) {
-        const int d = i / (BS - valid), s = valid + i % (BS - valid);
-        vt[d * BS + s] = zero;
-      }
-    }
-    consumer_sync();
-    float cs = red_sum[g];
-#pragma unroll
-    for (int w = 1; w < kConsumerWarps; ++w) cs += red_sum[w * 8 + g];
-    const float f = m_run == -INFINITY ? 0.f : exp2f(m_run - m_new);
-    s_run = s_run * f + cs;
-    m_run = m_new;
-    // ---- P.V: this warp's head_dim slice over the chunk's tokens ---------------
+    const uint32_t q_base = sm100::smem_u32(qs + qb * Lay::kQTile);
+    float acc[kDT][4];
 #pragma unroll
     for (int i = 0; i < kDT; ++i)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) acc[i][e] *= f;
-    for (int kk = 0; kk * 16 < n; ++kk) {  // 16 tokens per step
-      uint32_t pa[4];
-      ldsm_x4(pa, p_base + (((lane & 7) + ((lane >> 3) & 1) * 8) * Lay::kPStride + kk * 16 +
-                            (lane >> 4) * 8) * 2);
-      const int jv = jb0 + (kk * 16) / BS, sv = (kk * 16) % BS;
-      const uint32_t vblk =
-          ring_base + (jv % Lay::kStages) * Lay::kStageBytes + Lay::kBlockBytes;
+      for (int e = 0; e < 4; ++e) acc[i][e] = 0.f;
+    float m_run = -INFINITY, s_run = 0.f;  // for head g (rows g and g + 8)
+    const int nchunks = (it.t1 - it.t0 + kChunk - 1) / kChunk;
+    for (int ci = 0; ci < nchunks; ++ci) {
+      const int c0 = it.t0 + ci * kChunk;
+      const int n = min(kChunk, it.t1 - c0);
+      const uint32_t jb0 = jg + (c0 - it.t0) / BS;  // ring index of the chunk's first block
+      const int nb = (n + BS - 1) / BS;
+      // every block of the chunk landed
+      for (uint32_t jb = jb0; jb < jb0 + nb; ++jb) {
+        const int slot = static_cast<int>(jb % Lay::kStages);
+        if (!sm100::mbar_wait(&full[slot], static_cast<uint32_t>((jb / Lay::kStages) & 1),
+                              kWaitBudget, abort_flag)) {
+          poison = true;
+          if (lane == 0) {
+            flags[0] = 1;
+            set_status(a.status, PA_ERR_DEVICE_TIMEOUT);
+          }
+        }
+        poison |= bad[slot] != 0;
+      }
+      // ---- QK^T: this warp's 8 tokens 8w .. 8w + 7 of the chunk --------------------
+      const int tk = warp * 8;  // first token of the n-tile within the chunk
+      const int so = tk % BS;
+      const uint32_t kblk =
+          ring_base + static_cast<int>((jb0 + tk / BS) % Lay::kStages) * Lay::kStageBytes;
+      float sc[4] = {0.f, 0.f, 0.f, 0.f};
+      if (tk < n) {
+#pragma unroll 4
+        for (int ks = 0; ks < D / 16; ++ks) {
+          uint32_t qx[2], kb[2];
+          // A rows 0..7 (the query heads), columns 16 ks + 8 ((lane / 8) % 2); rows 8..15 are 0
+          ldsm_x2(qx, q_base + ((lane & 7) * Lay::kQStride + ks * 16 + ((lane >> 3) & 1) * 8) * 2);
+          const uint32_t qa[4] = {qx[0], 0u, qx[1], 0u};
+          // B: tokens so .. so + 7 of key groups 2 ks and 2 ks + 1 (16 bytes each)
+          ldsm_x2(kb, kblk + (((2 * ks + ((lane >> 3) & 1)) * BS + so + (lane & 7)) * 16));
+          mma16816<T>(sc, qa, kb);
+        }
+      }
+      // logits of head g, tokens tk + 2t, tk + 2t + 1 (c[0], c[1]); c[2], c[3] are padding
+      float l0 = (tk + 2 * t < n) ? sc[0] * sl2 : -INFINITY;
+      float l1 = (tk + 2 * t + 1 < n) ? sc[1] * sl2 : -INFINITY;
+      if (g >= G) l0 = l1 = -INFINITY;
+      float mx = fmaxf(l0, l1);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      if (t == 0) red_max[warp * 8 + g] = mx;
+      consumer_sync();
+      float mc = red_max[g];
+#pragma unroll
+      for (int w = 1; w < kConsumerWarps; ++w) mc = fmaxf(mc, red_max[w * 8 + g]);
+      const float m_new = fmaxf(m_run, mc);
+      const float p0 = l0 == -INFINITY ? 0.f : exp2f(l0 - m_new);
+      const float p1 = l1 == -INFINITY ? 0.f : exp2f(l1 - m_new);
+      float ssum = p0 + p1;
+      ssum += __shfl_xor_sync(0xffffffffu, ssum, 1);
+      ssum += __shfl_xor_sync(0xffffffffu, ssum, 2);
+      if (t == 0) red_sum[warp * 8 + g] = ssum;
+      // P tile: row g = the hi parts, row g + 8 = the remainders, tokens tk + 2t, +1
+      {
+        const T h0 = round16(p0, static_cast<T*>(nullptr)), h1 = round16(p1, static_cast<T*>(nullptr));
+        const T r0 = round16(p0 - to_float(h0), static_cast<T*>(nullptr));
+        const T r1 = round16(p1 - to_float(h1), static_cast<T*>(nullptr));
+        *reinterpret_cast<uint32_t*>(ps + g * Lay::kPStride + tk + 2 * t) = pack2<T>(h0, h1);
+        *reinterpret_cast<uint32_t*>(ps + (g + 8) * Lay::kPStride + tk + 2 * t) = pack2<T>(r0, r1);
+      }
+      // the tail block: value columns past the range are cleared (P is 0 there,
+      // but 0 * NaN would be NaN); the slot is refilled by bulk copy later
+      if (n < nb * BS) {
+        const uint32_t jt = jb0 + nb - 1;
+        T* vt = reinterpret_cast<T*>(ring + static_cast<int>(jt % Lay::kStages) * Lay::kStageBytes +
+                                     Lay::kBlockBytes);
+        const int valid = n - (nb - 1) * BS;
+        for (int i = tid; i < D * (BS - valid); i += kConsumerWarps * 32) {
+          const int d = i / (BS - valid), s = valid + i % (BS - valid);
+          vt[d * BS + s] = zero;
+        }
+        sm100::fence_proxy_async_smem();
+      }
+      consumer_sync();
+      float cs = red_sum[g];
+#pragma unroll
+      for (int w = 1; w < kConsumerWarps; ++w) cs += red_sum[w * 8 + g];
+      const float f = m_run == -INFINITY ? 0.f : exp2f(m_run - m_new);
+      s_run = s_run * f + cs;
+      m_run = m_new;
+      // ---- P.V: this warp's head_dim slice over the chunk's tokens ---------------
+#pragma unroll
+      for (int i = 0; i < kDT; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[i][e] *= f;
+      for (int kk = 0; kk * 16 < n; ++kk) {  // 16 tokens per step
+        uint32_t pa[4];
+        ldsm_x4(pa, p_base + (((lane & 7) + ((lane >> 3) & 1) * 8) * Lay::kPStride + kk * 16 +
+                              (lane >> 4) * 8) * 2);
+        const uint32_t jv = jb0 + (kk * 16) / BS;
+        const int sv = (kk * 16) % BS;
+        const uint32_t vblk = ring_base +
+                              static_cast<int>(jv % Lay::kStages) * Lay::kStageBytes + Lay::kBlockBytes;
+#pragma unroll
+        for (int i = 0; i < kDT; ++i) {
+          const int d0 = warp * (D / 4) + i * 8;
+          uint32_t vb[2];
+          // B: head_dim rows d0 .. d0 + 7, tokens sv + 8 ((lane / 8) % 2) .. + 7
+          ldsm_x2(vb, vblk + ((d0 + (lane & 7)) * BS + sv + ((lane >> 3) & 1) * 8) * 2);
+          mma16816<T>(acc[i], pa, vb);
+        }
+      }
+      consumer_sync();  // the P tile and the reductions are read before the next chunk
+      if (lane == 0)
+        for (uint32_t j = jb0; j < jb0 + nb; ++j) sm100::mbar_arrive(&empty[j % Lay::kStages]);
+    }
+    jg += it.nblk;
+    ++nq;
+    if (lane == 0) sm100::mbar_arrive(&qempty[qb]);  // this item's QK^T is done with q
+
+    // ---- epilogue: O[g] = (rows g + rows g + 8) / s --------------------------------
+    poison |= *abort_flag != 0;
+    if (g < G) {
+      const int64_t row = row0 + g;
 #pragma unroll
       for (int i = 0; i < kDT; ++i) {
-        const int d0 = warp * (D / 4) + i * 8;
-        uint32_t vb[2];
-        // B: head_dim rows d0 .. d0 + 7, tokens sv + 8 ((lane / 8) % 2) .. + 7
-        ldsm_x2(vb, vblk + ((d0 + (lane & 7)) * BS + sv + ((lane >> 3) & 1) * 8) * 2);
-        mma16816<T>(acc[i], pa, vb);
+        const int d = warp * (D / 4) + i * 8 + 2 * t;
+        const float o0 = poison ? qnan() : (acc[i][0] + acc[i][2]) / s_run;
+        const float o1 = poison ? qnan() : (acc[i][1] + acc[i][3]) / s_run;
+        if (kV2 && !it.direct) {
+          float* dst = a.tmp_out + (row * a.num_partitions + it.part) * D + d;
+          dst[0] = o0;
+          dst[1] = o1;
+        } else {
+          store_out(a.out, row * D + d, a.out_dtype, o0);
+          store_out(a.out, row * D + d + 1, a.out_dtype, o1);
+        }
       }
-    }
-    consumer_sync();  // the P tile and the reductions are read before the next chunk
-    if (lane == 0)
-      for (int j = jb0; j < jb0 + nb; ++j) sm100::mbar_arrive(&empty[j % Lay::kStages]);
-  }
-
-  // ---- epilogue: O[g] = (rows g + rows g + 8) / s ----------------------------------
-  poison |= flags[1] != 0 || *abort_flag != 0;
-  if (g < G) {
-    const int64_t row = row0 + g;
-#pragma unroll
-    for (int i = 0; i < kDT; ++i) {
-      const int d = warp * (D / 4) + i * 8 + 2 * t;
-      const float o0 = poison ? qnan() : (acc[i][0] + acc[i][2]) / s_run;
-      const float o1 = poison ? qnan() : (acc[i][1] + acc[i][3]) / s_run;
-      if (kV2 && !direct) {
-        float* dst = a.tmp_out + (row * a.num_partitions + part) * D + d;
-        dst[0] = o0;
-        dst[1] = o1;
-      } else {
-        store_out(a.out, row * D + d, a.out_dtype, o0);
-        store_out(a.out, row * D + d + 1, a.out_dtype, o1);
+      if (kV2 && !it.direct && warp == 0 && t == 0) {
+        const int64_t w = row * a.num_partitions + it.part;
+        a.max_logits[w] = poison ? qnan() : m_run * kLn2;
+        a.exp_sums[w] = s_run;
       }
-    }
-    if (kV2 && !direct && warp == 0 && t == 0) {
-      const int64_t w = row * a.num_partitions + part;
-      a.max_logits[w] = poison ? qnan() : m_run * kLn2;
-      a.exp_sums[w] = s_run;
     }
   }
 }
@@ -370,11 +457,18 @@ __global__ void __launch_bounds__(sx::kThreads, 2) pa_sx_kernel(const KernelArgs
 template <typename T, int D, int BS>
 cudaError_t launch_sx_t(const KernelArgs& a, bool v2, cudaStream_t s) {
   using Lay = sx::Layout<D, BS>;
-  const dim3 grid(v2 ? a.num_partitions : 1, a.num_kv_heads, a.num_seqs);
+  const int64_t items =
+      static_cast<int64_t>(a.num_seqs) * a.num_kv_heads * (v2 ? a.num_partitions : 1);
+  if (items == 0) return cudaSuccess;
+  // persistent: at most two CTAs per SM; one CTA per item below one item per SM
+  const int sms = sm100_num_sms();
+  const int64_t persistent = sms > 0 ? tc_persistent_grid(items, false, sms) : 0;
+  const int64_t grid = persistent > 0 ? persistent : items;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
   auto kern = v2 ? pa_sx_kernel<T, D, BS, true> : pa_sx_kernel<T, D, BS, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, sx::kThreads, Lay::kSmem, s>>>(a);
+  kern<<<static_cast<unsigned>(grid), sx::kThreads, Lay::kSmem, s>>>(a, items);
   return cudaGetLastError();
 }
 

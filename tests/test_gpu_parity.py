@@ -539,11 +539,49 @@ def test_split_x_layout(dtype, D, BS):
             assert pa.read_device_status(ws) == pa.PA_OK
 
 
+@pytest.mark.parametrize("dtype,D,BS", [(torch.bfloat16, 128, 16), (torch.float16, 64, 32)])
+def test_split_x_persistent_walk(dtype, D, BS):
+    """More split-x work items than two per SM, so each CTA of the persistent
+    grid walks several items (its ring streams from one item into the next,
+    its two q tiles alternate): V1 and V2 on every row against the oracle,
+    and a block id outside the pool, planted in one sequence, poisons that
+    sequence's rows only (the CTAs that meet it go on to correct items)."""
+    gen = torch.Generator().manual_seed(5)
+    lens = torch.randint(0, 2000, (96,), generator=gen).tolist()
+    lens[:11] = [0, 1, BS - 1, BS, BS + 1, 256, 257, 1999, 1024, 700, 1500]
+    bad_seq = 10
+    kw = dict(dtype=dtype, lens=lens, Hq=16, Hkv=4, D=D, BS=BS, seed=31)
+    ref = _ref(problem(**kw))
+    bc = problem(**kw)
+    bc.block_tables[bad_seq, 3] = bc.k_cache.shape[0] + 1     # outside the pool
+    bg = bc.to("cuda")
+    k5, v4 = (t.cuda() for t in _split_x(bc))
+    kx = dict(max_seq_len=bc.max_seq_len, scale=bc.scale, split_x=True)
+    params = pa.make_params(bc.q, k5, bc.block_tables, partition_size=256,
+                            out_dtype=torch.float32, **kx)
+    assert pa.decode_kernel(params) == 2
+    keep = [b for b in range(len(lens)) if b != bad_seq]
+    for path in ("v1", "v2"):
+        got = torch.full(tuple(bc.q.shape), float("nan"), device="cuda")
+        ws = pa.alloc_workspace(params)
+        if path == "v1":
+            pa.decode_v1(bg.q, k5, v4, bg.block_tables, bg.seq_lens, got, **kx)
+        else:
+            pa.decode_v2(bg.q, k5, v4, bg.block_tables, bg.seq_lens, got, ws,
+                         partition_size=256, **kx)
+        torch.cuda.synchronize()
+        g = got.double().cpu().numpy()
+        assert np.all(np.isnan(g[bad_seq])), path
+        assert_close(g[keep], ref[keep], TOL[dtype], f"split-x persistent {path}")
+        if path == "v2":
+            assert pa.read_device_status(ws) == pa.PA_ERR_BAD_BLOCK_ID
+
+
 def test_split_x_full_size_long_context():
     """The 100K-token long-context workload with its caches rewritten (on the
     device, as test input) into the split-x layout: pa_decode (V2) on the
-    split-x tensor-core kernel against the oracle on every row, and a block id
-    outside the pool poisons only its sequence's rows."""
+    split-x tensor-core kernel against the oracle on every row, in the launch
+    configuration the bench times (784 items on the persistent grid)."""
     w = wl.WORKLOADS["long_100k"]
     bg = wl.make(w, device="cuda", poison=True)
     bc = bg.to("cpu")
