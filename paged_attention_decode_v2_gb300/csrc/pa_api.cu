@@ -98,7 +98,7 @@ KernelArgs make_args(const pa_params_t* p, const void* q, const void* k, const v
 cudaError_t launch_pass(const pa_params_t* p, const KernelArgs& a, bool v2, cudaStream_t s) {
   if (tc_applicable(p)) return launch_tc(a, p->kv_dtype, v2, s);
   if (sx_applicable(p))
-    return p->kv_dtype == PA_BF16 ? launch_sx_bf16(a, v2, s) : launch_sx_f16(a, v2, s);
+    return launch_sx(a, p->kv_dtype, v2, s);
   switch (p->kv_dtype) {
     case PA_F32: return launch_generic_f32(a, v2, s);
     case PA_BF16: return launch_generic_bf16(a, v2, s);
@@ -189,9 +189,10 @@ pa_status_t prepare_v2(const pa_params_t* p, const void* q, const void* k, const
 // itself): the tensor-core kernel serves these parameters as a persistent
 // grid with at least one CTA per reduce unit (pa_internal.h).
 bool one_launch_v2(const pa_params_t* p, int64_t np) {
-  if (!tc_applicable(p)) return false;
+  const bool tc = tc_applicable(p);
+  if (!tc && !sx_applicable(p)) return false;
   return one_launch_plan(p->num_seqs, p->num_heads, p->num_kv_heads, p->head_dim, np,
-                         sm100_num_sms());
+                         sm100_num_sms(), tc);
 }
 
 }  // namespace

@@ -77,10 +77,13 @@ inline int64_t tc_persistent_grid(int64_t items, bool compact, int num_sms) {
 // takes at most one reduce unit (query row x 32 elements of head_dim) per
 // CTA, so its own CTAs run pass 2 in one round after their streaming; other
 // batches use the dependent reduce kernel, which has more CTAs in flight.
+// `compact_list`: the kernel walks a compact work list for batches of 2 to
+// 1024 sequences (the standard-layout kernel; the split-x kernel walks the
+// full space).
 inline bool one_launch_plan(int64_t num_seqs, int64_t num_heads, int64_t num_kv_heads,
-                            int64_t head_dim, int64_t np, int num_sms) {
+                            int64_t head_dim, int64_t np, int num_sms, bool compact_list) {
   const int64_t items = num_seqs * num_kv_heads * np;
-  const bool compact = num_seqs > 1 && num_seqs <= 1024;  // the kernel's compact work list
+  const bool compact = compact_list && num_seqs > 1 && num_seqs <= 1024;
   const int64_t grid = tc_persistent_grid(items, compact, num_sms);
   // a unit holds the statistics of up to 1024 partitions
   return grid > 0 && np <= 1024 && num_seqs * num_heads * (head_dim / 32) <= grid;
@@ -122,11 +125,12 @@ pa_status_t check_params(const pa_params_t* p, bool v2);
 // the current device, and its launch (pass 1 for V2, the whole pass for V1).
 bool tc_applicable(const pa_params_t* p);
 cudaError_t launch_tc(const KernelArgs& a, pa_dtype_t kv, bool v2, cudaStream_t s);
-// Tensor-core path for caches in the split-x layout (pa_sx.cuh): whether it
-// serves these parameters on the current device, and its launches.
+// Tensor-core path for caches in the split-x layout (pa_sx.cuh, launched
+// from pa_tc_host.cu): whether it serves these parameters on the current
+// device, and its launch (pass 1 for V2, or the whole V2 step when
+// a.fused; the whole pass for V1).
 bool sx_applicable(const pa_params_t* p);
-cudaError_t launch_sx_bf16(const KernelArgs& a, bool v2, cudaStream_t s);
-cudaError_t launch_sx_f16(const KernelArgs& a, bool v2, cudaStream_t s);
+cudaError_t launch_sx(const KernelArgs& a, pa_dtype_t kv, bool v2, cudaStream_t s);
 
 // TMA tiled tensor map (pa_tc_host.cu) with the 128-byte swizzle the MMA
 // descriptors expect: `rank` dims (innermost first), the byte strides of

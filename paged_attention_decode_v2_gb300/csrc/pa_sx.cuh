@@ -36,13 +36,19 @@
 //
 // This is Phase 1 of the V2 scheme of commit 4eb83a7e "qwen3_6_scripts",
 // paragraph "Implementation (paged_attention_v2_pytorch.py)", or V1 when the
-// range is the whole sequence.  Every wait is bounded; a wait that gives up
-// sets PA_ERR_DEVICE_TIMEOUT and the item's outputs become NaN.
+// range is the whole sequence.  With a.fused the same grid then runs Phase 2
+// (the grid-end reduce of pa_grid_reduce.cuh, by the four consumer warps,
+// scratch in the ring), so the V2 step is one launch.  Every wait is
+// bounded; a wait that gives up sets PA_ERR_DEVICE_TIMEOUT and the item's
+// outputs become NaN.
 #pragma once
 
 #include <type_traits>
 
+#include <cuda.h>
+
 #include "pa_device.cuh"
+#include "pa_grid_reduce.cuh"
 #include "pa_sm100.cuh"
 
 namespace pa {
@@ -120,10 +126,23 @@ struct Layout {
   static constexpr int kPOff = kQOff + 2 * kQTile * 2;
   static constexpr int kRedOff = kPOff + 16 * kPStride * 2;  // [4 warps][8 heads] max, sum
   static constexpr int kBarOff = kRedOff + 2 * kConsumerWarps * 8 * 4;
-  // full[kMaxStages], empty[kMaxStages], qfull[2], qempty[2]
-  static constexpr int kFlagOff = kBarOff + (2 * kMaxStages + 4) * 8;
-  // [0] abort; [1 + s] ring slot s holds no block (its id was out of range)
-  static constexpr int kSmem = kFlagOff + (1 + kMaxStages) * 4 + 64;
+  // full[kMaxStages], empty[kMaxStages], qfull[2], qempty[2], and for the
+  // one-launch V2 grid: red_bar (a reduce unit's tile copy), dry_done
+  static constexpr int kFlagOff = kBarOff + (2 * kMaxStages + 6) * 8;
+  // [0] abort; [1 + s] ring slot s holds no block (its id was out of range);
+  // [kWsOk] the workspace carries the init marker; [kRedWord ..] three ints
+  // for the reduce's broadcasts
+  static constexpr int kWsOk = 1 + kMaxStages;
+  static constexpr int kRedWord = kWsOk + 1;
+  static constexpr int kSmem = kFlagOff + (kRedWord + 3) * 4 + 64;
+  // One-launch V2: the reduce's scratch is the ring once streaming is done;
+  // its dry run at the start takes the ring's last kDrySlots slots, which the
+  // producer fills for the first time only after that run.
+  static constexpr int kRingEnd = kStages * kStageBytes;
+  static constexpr int kDryOff = kRingEnd - static_cast<int>((gridred::kDryBytes + 127) / 128 * 128);
+  static constexpr int kDrySlots = (kRingEnd - kDryOff + kStageBytes - 1) / kStageBytes;
+  static_assert(sizeof(gridred::UnitScratch) <= kRingEnd, "reduce scratch in the ring");
+  static_assert(kDrySlots < kStages, "dry run beside the first stages");
   static_assert(kStages >= 2 * kChunkBlocks, "two chunks in flight");
   static_assert((kQStride * 2) % 16 == 0 && kQOff % 16 == 0, "bulk copies of q rows");
   static_assert(kSmem <= 113 * 1024, "two CTAs per SM");
@@ -161,7 +180,7 @@ __device__ __forceinline__ Item item_at(const KernelArgs& a, int64_t k, bool v2)
 
 template <typename T, int D, int BS, bool kV2>
 __global__ void __launch_bounds__(sx::kThreads, 2)
-    pa_sx_kernel(const KernelArgs a, int64_t total_items) {
+    pa_sx_kernel(const KernelArgs a, const __grid_constant__ CUtensorMap pmap, int64_t total_items) {
   using namespace sx;
   using Lay = Layout<D, BS>;
   static_assert(BS == 16 || BS == 32, "block size");
@@ -175,6 +194,8 @@ __global__ void __launch_bounds__(sx::kThreads, 2)
   uint64_t* empty = full + kMaxStages;
   uint64_t* qfull = empty + kMaxStages;
   uint64_t* qempty = qfull + 2;
+  uint64_t* red_bar = qempty + 2;
+  uint64_t* dry_done = red_bar + 1;
   int* flags = reinterpret_cast<int*>(smem + Lay::kFlagOff);
   volatile int* abort_flag = &flags[0];
   volatile int* bad = flags + 1;
@@ -184,6 +205,8 @@ __global__ void __launch_bounds__(sx::kThreads, 2)
   const T zero = round16(0.f, static_cast<T*>(nullptr));
 
   // ---- set-up ---------------------------------------------------------------------
+  const bool fused = kV2 && a.fused;  // one-launch V2: pass 2 by this grid at the end
+  unsigned long long started = 0;     // thread 0, one-launch V2: the start word as it was
   if (tid == 0) {
     for (int s = 0; s < Lay::kStages; ++s) {
       sm100::mbar_init(&full[s], 1);
@@ -195,6 +218,19 @@ __global__ void __launch_bounds__(sx::kThreads, 2)
       sm100::mbar_init(&qempty[i], kConsumerWarps);
     }
     flags[0] = 0;
+    // one-launch V2: the counters are usable only in an initialised workspace;
+    // the CTA counts itself started (the result is first used at the end)
+    int ws_ok = 0;
+    if (fused) {
+      sm100::mbar_init(red_bar, 1);
+      sm100::mbar_init(dry_done, kConsumerWarps);
+      ws_ok = __ldcg(a.status + kMarkerOffset / 4) == kMarker;
+      if (ws_ok)
+        started = gridred::count_started(a);
+      else
+        set_status(a.status, PA_ERR_WORKSPACE_NOT_INIT);
+    }
+    flags[Lay::kWsOk] = ws_ok;
   }
   // rows G .. 7 of both q tiles stay zero; the bulk copies fill rows 0 .. G-1
   for (int i = tid; i < 2 * kQRows * D; i += kThreads) {
@@ -202,6 +238,7 @@ __global__ void __launch_bounds__(sx::kThreads, 2)
     if (r >= G) qs[tile * Lay::kQTile + r * Lay::kQStride + i % D] = zero;
   }
   __syncthreads();
+  const bool dry_run = fused && flags[Lay::kWsOk] != 0;
 
   if (warp == kConsumerWarps) {
     // ========================= producer =======================================
@@ -210,6 +247,7 @@ __global__ void __launch_bounds__(sx::kThreads, 2)
     const char* kc = static_cast<const char*>(a.k_cache);
     const char* vc = static_cast<const char*>(a.v_cache);
     const char* qg = static_cast<const char*>(a.q);
+    if (fused && lane == 0) sm100::tma_prefetch_desc(&pmap);
     bool ok = true;
     uint32_t jg = 0;  // ring blocks issued, over all items (a CTA streams far
                       // fewer than 2^32 blocks, so 32 bits keep the slot
@@ -241,6 +279,8 @@ __global__ void __launch_bounds__(sx::kThreads, 2)
           const uint32_t par = static_cast<uint32_t>((jg / Lay::kStages) & 1) ^ 1;
           ok = __all_sync(0xffffffffu,
                           sm100::mbar_wait(&empty[slot], par, kWaitBudget, abort_flag));
+          if (ok && dry_run && jg >= Lay::kStages - Lay::kDrySlots && jg < Lay::kStages)
+            ok = __all_sync(0xffffffffu, sm100::mbar_wait(dry_done, 0, kWaitBudget, abort_flag));
           if (!ok) break;
           const int32_t id = __shfl_sync(0xffffffffu, id_l, jj);
           if (lane == 0) {
@@ -283,8 +323,24 @@ __global__ void __launch_bounds__(sx::kThreads, 2)
   const uint32_t p_base = sm100::smem_u32(ps);
   const uint32_t ring_base = sm100::smem_u32(ring);
   constexpr int kDT = D / 4 / 8;  // 8-wide head_dim tiles of this warp's P.V slice
-  uint32_t jg = 0;                // ring blocks consumed, over all items
+  int hs = 0;                      // ring slot of the next block to consume
+  uint32_t hp = 0;                 // and its phase parity (no division in the hot loop)
+  auto wrap = [](int x) { return x >= Lay::kStages ? x - Lay::kStages : x; };
   int nq = 0;                     // q tiles consumed
+  int* const red_word = flags + Lay::kRedWord;
+  if (dry_run) {
+    // One-launch V2: run the end-of-kernel reduce once now, dry (no side
+    // effects; scratch at the ring's end, which the producer leaves alone
+    // until dry_done), so its code is in the instruction cache at the end.
+    gridred::UnitScratch& dsc = *reinterpret_cast<gridred::UnitScratch*>(ring + Lay::kDryOff);
+    uint32_t dry_phase = 0;
+    gridred::grid_reduce<D>(a, true, started, red_word, dsc, &pmap, red_bar, tid, kWaitBudget,
+                            true);
+    gridred::reduce_unit<D>(a, &pmap, red_bar, dry_phase, 0, 0, dsc, tid, false, kWaitBudget,
+                            true);
+    __syncwarp();
+    if (lane == 0) sm100::mbar_arrive(dry_done);
+  }
   for (int64_t k = blockIdx.x; k < total_items; k += gridDim.x) {
     const Item it = item_at<BS>(a, k, kV2);
     const int64_t row0 = static_cast<int64_t>(it.b) * Hq + static_cast<int64_t>(it.kvh) * G;
@@ -306,7 +362,21 @@ __global__ void __launch_bounds__(sx::kThreads, 2)
         set_status(a.status, PA_ERR_DEVICE_TIMEOUT);
       }
     }
-    const uint32_t q_base = sm100::smem_u32(qs + qb * Lay::kQTile);
+    // q as A fragments for the whole item: rows 0..7 the query heads (rows
+    // 8..15 of the MMA are zero), qf[ks] = columns 16 ks .. 16 ks + 15
+    uint32_t qf[D / 16][2];
+    {
+      const uint32_t q_base = sm100::smem_u32(qs + qb * Lay::kQTile);
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ks += 2) {
+        uint32_t r[4];
+        ldsm_x4(r, q_base + ((lane & 7) * Lay::kQStride + ks * 16 + (lane >> 3) * 8) * 2);
+        qf[ks][0] = r[0];
+        qf[ks][1] = r[1];
+        qf[ks + 1][0] = r[2];
+        qf[ks + 1][1] = r[3];
+      }
+    }
     float acc[kDT][4];
 #pragma unroll
     for (int i = 0; i < kDT; ++i)
@@ -317,13 +387,12 @@ __global__ void __launch_bounds__(sx::kThreads, 2)
     for (int ci = 0; ci < nchunks; ++ci) {
       const int c0 = it.t0 + ci * kChunk;
       const int n = min(kChunk, it.t1 - c0);
-      const uint32_t jb0 = jg + (c0 - it.t0) / BS;  // ring index of the chunk's first block
       const int nb = (n + BS - 1) / BS;
       // every block of the chunk landed
-      for (uint32_t jb = jb0; jb < jb0 + nb; ++jb) {
-        const int slot = static_cast<int>(jb % Lay::kStages);
-        if (!sm100::mbar_wait(&full[slot], static_cast<uint32_t>((jb / Lay::kStages) & 1),
-                              kWaitBudget, abort_flag)) {
+      for (int i = 0; i < nb; ++i) {
+        const int slot = wrap(hs + i);
+        if (!sm100::mbar_wait(&full[slot], hs + i >= Lay::kStages ? hp ^ 1u : hp, kWaitBudget,
+                              abort_flag)) {
           poison = true;
           if (lane == 0) {
             flags[0] = 1;
@@ -336,20 +405,21 @@ __global__ void __launch_bounds__(sx::kThreads, 2)
       const int tk = warp * 8;  // first token of the n-tile within the chunk
       const int so = tk % BS;
       const uint32_t kblk =
-          ring_base + static_cast<int>((jb0 + tk / BS) % Lay::kStages) * Lay::kStageBytes;
-      float sc[4] = {0.f, 0.f, 0.f, 0.f};
+          ring_base + wrap(hs + tk / BS) * Lay::kStageBytes;
+      float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
       if (tk < n) {
-#pragma unroll 4
+#pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          uint32_t qx[2], kb[2];
-          // A rows 0..7 (the query heads), columns 16 ks + 8 ((lane / 8) % 2); rows 8..15 are 0
-          ldsm_x2(qx, q_base + ((lane & 7) * Lay::kQStride + ks * 16 + ((lane >> 3) & 1) * 8) * 2);
-          const uint32_t qa[4] = {qx[0], 0u, qx[1], 0u};
+          uint32_t kb[2];
+          const uint32_t qa[4] = {qf[ks][0], 0u, qf[ks][1], 0u};
           // B: tokens so .. so + 7 of key groups 2 ks and 2 ks + 1 (16 bytes each)
           ldsm_x2(kb, kblk + (((2 * ks + ((lane >> 3) & 1)) * BS + so + (lane & 7)) * 16));
-          mma16816<T>(sc, qa, kb);
+          if (ks & 1) mma16816<T>(sd, qa, kb);  // two chains: half the dependent MMAs
+          else mma16816<T>(sc, qa, kb);
         }
       }
+      sc[0] += sd[0];
+      sc[1] += sd[1];
       // logits of head g, tokens tk + 2t, tk + 2t + 1 (c[0], c[1]); c[2], c[3] are padding
       float l0 = (tk + 2 * t < n) ? sc[0] * sl2 : -INFINITY;
       float l1 = (tk + 2 * t + 1 < n) ? sc[1] * sl2 : -INFINITY;
@@ -380,8 +450,7 @@ __global__ void __launch_bounds__(sx::kThreads, 2)
       // the tail block: value columns past the range are cleared (P is 0 there,
       // but 0 * NaN would be NaN); the slot is refilled by bulk copy later
       if (n < nb * BS) {
-        const uint32_t jt = jb0 + nb - 1;
-        T* vt = reinterpret_cast<T*>(ring + static_cast<int>(jt % Lay::kStages) * Lay::kStageBytes +
+        T* vt = reinterpret_cast<T*>(ring + wrap(hs + nb - 1) * Lay::kStageBytes +
                                      Lay::kBlockBytes);
         const int valid = n - (nb - 1) * BS;
         for (int i = tid; i < D * (BS - valid); i += kConsumerWarps * 32) {
@@ -406,10 +475,9 @@ __global__ void __launch_bounds__(sx::kThreads, 2)
         uint32_t pa[4];
         ldsm_x4(pa, p_base + (((lane & 7) + ((lane >> 3) & 1) * 8) * Lay::kPStride + kk * 16 +
                               (lane >> 4) * 8) * 2);
-        const uint32_t jv = jb0 + (kk * 16) / BS;
         const int sv = (kk * 16) % BS;
         const uint32_t vblk = ring_base +
-                              static_cast<int>(jv % Lay::kStages) * Lay::kStageBytes + Lay::kBlockBytes;
+                              wrap(hs + (kk * 16) / BS) * Lay::kStageBytes + Lay::kBlockBytes;
 #pragma unroll
         for (int i = 0; i < kDT; ++i) {
           const int d0 = warp * (D / 4) + i * 8;
@@ -421,9 +489,13 @@ __global__ void __launch_bounds__(sx::kThreads, 2)
       }
       consumer_sync();  // the P tile and the reductions are read before the next chunk
       if (lane == 0)
-        for (uint32_t j = jb0; j < jb0 + nb; ++j) sm100::mbar_arrive(&empty[j % Lay::kStages]);
+        for (int i = 0; i < nb; ++i) sm100::mbar_arrive(&empty[wrap(hs + i)]);
+      hs += nb;
+      if (hs >= Lay::kStages) {
+        hs -= Lay::kStages;
+        hp ^= 1u;
+      }
     }
-    jg += it.nblk;
     ++nq;
     if (lane == 0) sm100::mbar_arrive(&qempty[qb]);  // this item's QK^T is done with q
 
@@ -452,10 +524,19 @@ __global__ void __launch_bounds__(sx::kThreads, 2)
       }
     }
   }
+  // one-launch V2: pass 2 by this grid, once every CTA has stored its
+  // partials (this CTA's consumer threads meet first: their stores precede
+  // the finished count); every block was consumed, so the ring is free
+  if (fused) {
+    consumer_sync();
+    gridred::grid_reduce<D>(a, flags[Lay::kWsOk] != 0, started, red_word,
+                            *reinterpret_cast<gridred::UnitScratch*>(ring), &pmap, red_bar, tid,
+                            kWaitBudget, false);
+  }
 }
 
 template <typename T, int D, int BS>
-cudaError_t launch_sx_t(const KernelArgs& a, bool v2, cudaStream_t s) {
+cudaError_t launch_sx_t(const KernelArgs& a, const CUtensorMap& pm, bool v2, cudaStream_t s) {
   using Lay = sx::Layout<D, BS>;
   const int64_t items =
       static_cast<int64_t>(a.num_seqs) * a.num_kv_heads * (v2 ? a.num_partitions : 1);
@@ -468,19 +549,19 @@ cudaError_t launch_sx_t(const KernelArgs& a, bool v2, cudaStream_t s) {
   auto kern = v2 ? pa_sx_kernel<T, D, BS, true> : pa_sx_kernel<T, D, BS, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmem);
   if (e != cudaSuccess) return e;
-  kern<<<static_cast<unsigned>(grid), sx::kThreads, Lay::kSmem, s>>>(a, items);
+  kern<<<static_cast<unsigned>(grid), sx::kThreads, Lay::kSmem, s>>>(a, pm, items);
   return cudaGetLastError();
 }
 
 template <typename T>
-cudaError_t launch_sx_dtype(const KernelArgs& a, bool v2, cudaStream_t s) {
+cudaError_t launch_sx_dtype(const KernelArgs& a, const CUtensorMap& pm, bool v2, cudaStream_t s) {
   switch (a.head_dim * 100 + a.block_size) {
-    case 25616: return launch_sx_t<T, 256, 16>(a, v2, s);
-    case 25632: return launch_sx_t<T, 256, 32>(a, v2, s);
-    case 12816: return launch_sx_t<T, 128, 16>(a, v2, s);
-    case 12832: return launch_sx_t<T, 128, 32>(a, v2, s);
-    case 6416: return launch_sx_t<T, 64, 16>(a, v2, s);
-    case 6432: return launch_sx_t<T, 64, 32>(a, v2, s);
+    case 25616: return launch_sx_t<T, 256, 16>(a, pm, v2, s);
+    case 25632: return launch_sx_t<T, 256, 32>(a, pm, v2, s);
+    case 12816: return launch_sx_t<T, 128, 16>(a, pm, v2, s);
+    case 12832: return launch_sx_t<T, 128, 32>(a, pm, v2, s);
+    case 6416: return launch_sx_t<T, 64, 16>(a, pm, v2, s);
+    case 6432: return launch_sx_t<T, 64, 32>(a, pm, v2, s);
     default: return cudaErrorInvalidValue;
   }
 }

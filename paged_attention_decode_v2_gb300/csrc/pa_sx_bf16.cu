@@ -4,8 +4,8 @@
 
 namespace pa {
 
-cudaError_t launch_sx_bf16(const KernelArgs& a, bool v2, cudaStream_t s) {
-  return launch_sx_dtype<__nv_bfloat16>(a, v2, s);
+cudaError_t launch_sx_bf16(const KernelArgs& a, const CUtensorMap& pmap, bool v2, cudaStream_t s) {
+  return launch_sx_dtype<__nv_bfloat16>(a, pmap, v2, s);
 }
 
 }  // namespace pa

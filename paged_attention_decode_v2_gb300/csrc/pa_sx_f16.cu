@@ -4,8 +4,8 @@
 
 namespace pa {
 
-cudaError_t launch_sx_f16(const KernelArgs& a, bool v2, cudaStream_t s) {
-  return launch_sx_dtype<__half>(a, v2, s);
+cudaError_t launch_sx_f16(const KernelArgs& a, const CUtensorMap& pmap, bool v2, cudaStream_t s) {
+  return launch_sx_dtype<__half>(a, pmap, v2, s);
 }
 
 }  // namespace pa

@@ -9,6 +9,7 @@
 // laid out slice-major; q is viewed as (head_dim, num_seqs * num_heads)
 // rows with an 8-row box (one KV head's query rows).  All use the 128-byte
 // swizzle the MMA descriptors expect.
+#include <cstring>
 #include <atomic>
 #include <mutex>
 
@@ -25,6 +26,8 @@ cudaError_t launch_tc_bf16(const KernelArgs& a, const CUtensorMap& kmap, const C
 cudaError_t launch_tc_f16(const KernelArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                           const CUtensorMap& qmap, const CUtensorMap& pmap, bool v2, int num_sms,
                           cudaStream_t s);
+cudaError_t launch_sx_bf16(const KernelArgs& a, const CUtensorMap& pmap, bool v2, cudaStream_t s);
+cudaError_t launch_sx_f16(const KernelArgs& a, const CUtensorMap& pmap, bool v2, cudaStream_t s);
 
 namespace {
 
@@ -118,6 +121,36 @@ bool sx_applicable(const pa_params_t* p) {
   return device_info().state == 1;
 }
 
+// The V2 partials as [rows][NP][head_dim] floats, a box of 32 elements x up
+// to 256 partitions of one row: the tile copies of the one-launch grid's
+// reduce units.
+static bool encode_partials_map(PFN_cuTensorMapEncodeTiled_v12000 enc, const KernelArgs& a,
+                                CUtensorMap* pmap) {
+  const cuuint64_t D = static_cast<cuuint64_t>(a.head_dim);
+  const cuuint64_t np = static_cast<cuuint64_t>(a.num_partitions);
+  const cuuint64_t dims[3] = {D, np, static_cast<cuuint64_t>(a.num_seqs) * a.num_heads};
+  const cuuint64_t strides[2] = {D * 4, np * D * 4};
+  const cuuint32_t box[3] = {32, static_cast<cuuint32_t>(np < 256 ? np : 256), 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return enc(pmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, a.tmp_out, dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The split-x kernel reads the caches by bulk copy (one contiguous run per
+// block and KV head); only the one-launch grid needs a tensor map (the
+// partials).
+cudaError_t launch_sx(const KernelArgs& a, pa_dtype_t kv, bool v2, cudaStream_t s) {
+  CUtensorMap pmap;
+  std::memset(&pmap, 0, sizeof pmap);  // never read unless a.fused
+  if (a.fused) {
+    auto enc = encoder();
+    if (!enc) return cudaErrorNotSupported;
+    if (!encode_partials_map(enc, a, &pmap)) return cudaErrorInvalidValue;
+  }
+  return kv == PA_BF16 ? launch_sx_bf16(a, pmap, v2, s) : launch_sx_f16(a, pmap, v2, s);
+}
+
 cudaError_t launch_tc(const KernelArgs& a, pa_dtype_t kv, bool v2, cudaStream_t s) {
   auto enc = encoder();
   if (!enc) return cudaErrorNotSupported;
@@ -158,21 +191,10 @@ cudaError_t launch_tc(const KernelArgs& a, pa_dtype_t kv, bool v2, cudaStream_t 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  // The partials as [rows][NP][head_dim] floats, a box of 32 elements x up to
-  // 256 partitions of one row: only the one-launch V2 grid reads it (its
-  // reduce units); otherwise a copy of the q map stands in, never used.
+  // only the one-launch V2 grid reads the partials map; otherwise a copy of
+  // the q map stands in, never used
   CUtensorMap pmap = qmap;
-  if (a.fused) {
-    const cuuint64_t np = static_cast<cuuint64_t>(a.num_partitions);
-    const cuuint64_t dims[3] = {D, np, static_cast<cuuint64_t>(a.num_seqs) * a.num_heads};
-    const cuuint64_t strides[2] = {D * 4, np * D * 4};
-    const cuuint32_t box[3] = {32, static_cast<cuuint32_t>(np < 256 ? np : 256), 1};
-    const cuuint32_t es[3] = {1, 1, 1};
-    if (enc(&pmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, a.tmp_out, dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
+  if (a.fused && !encode_partials_map(enc, a, &pmap)) return cudaErrorInvalidValue;
   const int sms = device_info().num_sms;
   return kv == PA_BF16 ? launch_tc_bf16(a, kmap, vmap, qmap, pmap, v2, sms, s)
                        : launch_tc_f16(a, kmap, vmap, qmap, pmap, v2, sms, s);

@@ -32,37 +32,51 @@ def _guards_intact(whole, n_elems, fill):
     return bool((lo == fill).all().item()) and bool((hi == fill).all().item())
 
 
+def split_x_caches(batch):
+    """The caches of ``batch`` rewritten (as test input, on the batch's
+    device) into the split-x layout: keys [blocks, kv_heads, head_dim / x,
+    block_size, x], values [blocks, kv_heads, head_dim, block_size],
+    x = 16 / element bytes."""
+    nb, hkv, bs, d = batch.k_cache.shape
+    x = 16 // batch.k_cache.element_size()
+    k5 = batch.k_cache.view(nb, hkv, bs, d // x, x).permute(0, 1, 3, 2, 4).contiguous()
+    v4 = batch.v_cache.permute(0, 1, 3, 2).contiguous()
+    return k5, v4
+
+
 def run(batch, path="decode", partition_size=512, portable=False, out_dtype=torch.float32,
         v1_max_seq_len=pa.DEFAULT_V1_MAX_SEQ_LEN, workspace=None, return_ws=False,
-        check_status=True):
+        check_status=True, split_x=False):
     """Run one decode step of ``batch`` (already on the GPU); returns out as a
     float64 numpy array (and the workspace tensor when asked).  When a
     workspace was used, its device status word must read OK afterwards
     (unless ``check_status`` is False).  ``out`` and a workspace made here
     sit between canary regions that must be untouched after the call (no
-    write outside the buffers the call was given)."""
+    write outside the buffers the call was given).  ``split_x``: the caches
+    go in rewritten into the split-x layout."""
     b = batch
+    kc, vc = split_x_caches(b) if split_x else (b.k_cache, b.v_cache)
     n_out = int(np.prod(tuple(b.q.shape)))
     out_whole, out_flat = _guarded(n_out, out_dtype, GUARD_F, b.q.device)
     out_flat.fill_(float("nan"))
     out = out_flat.view(tuple(b.q.shape))
-    params = pa.make_params(b.q, b.k_cache, b.block_tables, max_seq_len=b.max_seq_len,
+    params = pa.make_params(b.q, kc, b.block_tables, max_seq_len=b.max_seq_len,
                             scale=b.scale, partition_size=partition_size, out_dtype=out_dtype,
-                            v1_max_seq_len=v1_max_seq_len, portable=portable)
+                            v1_max_seq_len=v1_max_seq_len, portable=portable, split_x=split_x)
     ws_whole = None
     if workspace is None and path in ("v2", "decode"):
         n = pa.workspace_size(params)
         ws_whole, workspace = _guarded(n, torch.uint8, GUARD_B, b.q.device)
         workspace.view(torch.float32).fill_(float("nan"))        # poison everything,
         pa.workspace_init(workspace)                              # then the control block
-    kw = dict(max_seq_len=b.max_seq_len, scale=b.scale, portable=portable)
+    kw = dict(max_seq_len=b.max_seq_len, scale=b.scale, portable=portable, split_x=split_x)
     if path == "v1":
-        pa.decode_v1(b.q, b.k_cache, b.v_cache, b.block_tables, b.seq_lens, out, **kw)
+        pa.decode_v1(b.q, kc, vc, b.block_tables, b.seq_lens, out, **kw)
     elif path == "v2":
-        pa.decode_v2(b.q, b.k_cache, b.v_cache, b.block_tables, b.seq_lens, out, workspace,
+        pa.decode_v2(b.q, kc, vc, b.block_tables, b.seq_lens, out, workspace,
                      partition_size=partition_size, **kw)
     else:
-        pa.decode(b.q, b.k_cache, b.v_cache, b.block_tables, b.seq_lens, out, workspace,
+        pa.decode(b.q, kc, vc, b.block_tables, b.seq_lens, out, workspace,
                   partition_size=partition_size, v1_max_seq_len=v1_max_seq_len, **kw)
     torch.cuda.synchronize()
     assert _guards_intact(out_whole, n_out, GUARD_F), "write outside out"

@@ -17,7 +17,7 @@ import oracle
 import paged_attention_decode_v2_gb300 as pa
 from paged_attention_decode_v2_gb300 import workloads as wl
 from gpu_helpers import (MARKER, TOL, assert_close, bf16_round, control_words, max_err, run,
-                         workspace_views)
+                         split_x_caches, workspace_views)
 from oracle_pins import problem
 
 pytestmark = pytest.mark.gpu
@@ -484,17 +484,6 @@ def test_cuda_graph_capture_and_replay():
             assert pa.read_device_status(ws) == pa.PA_OK
 
 
-def _split_x(bc):
-    """The caches of `bc` rewritten (as test input, on the batch's device) into
-    the split-x layout: keys [blocks, kv_heads, head_dim / x, block_size, x],
-    values [blocks, kv_heads, head_dim, block_size], x = 16 / element bytes."""
-    nb, hkv, bs, d = bc.k_cache.shape
-    x = 16 // bc.k_cache.element_size()
-    k5 = bc.k_cache.view(nb, hkv, bs, d // x, x).permute(0, 1, 3, 2, 4).contiguous()
-    v4 = bc.v_cache.permute(0, 1, 3, 2).contiguous()
-    return k5, v4
-
-
 @pytest.mark.parametrize("dtype,D,BS", [(torch.bfloat16, 256, 16), (torch.float16, 128, 32),
                                         (torch.bfloat16, 64, 32), (torch.float32, 64, 16),
                                         (torch.float32, 256, 32), (torch.bfloat16, 64, 8)])
@@ -508,7 +497,7 @@ def test_split_x_layout(dtype, D, BS):
     bc = problem(dtype=dtype, lens=lens, Hq=12, Hkv=3, D=D, BS=BS, seed=21)
     ref = _ref(bc)
     bg = bc.to("cuda")
-    k5, v4 = (t.cuda() for t in _split_x(bc))
+    k5, v4 = (t.cuda() for t in split_x_caches(bc))
     kw = dict(max_seq_len=bc.max_seq_len, scale=bc.scale)
     tensor_core = dtype != torch.float32 and BS in (16, 32)
     params = pa.make_params(bc.q, k5, bc.block_tables, partition_size=256,
@@ -555,7 +544,7 @@ def test_split_x_persistent_walk(dtype, D, BS):
     bc = problem(**kw)
     bc.block_tables[bad_seq, 3] = bc.k_cache.shape[0] + 1     # outside the pool
     bg = bc.to("cuda")
-    k5, v4 = (t.cuda() for t in _split_x(bc))
+    k5, v4 = (t.cuda() for t in split_x_caches(bc))
     kx = dict(max_seq_len=bc.max_seq_len, scale=bc.scale, split_x=True)
     params = pa.make_params(bc.q, k5, bc.block_tables, partition_size=256,
                             out_dtype=torch.float32, **kx)
@@ -586,7 +575,7 @@ def test_split_x_full_size_long_context():
     bg = wl.make(w, device="cuda", poison=True)
     bc = bg.to("cpu")
     ref = oracle.decode(bc.q, bc.k_cache, bc.v_cache, bc.block_tables, bc.seq_lens, bc.scale)
-    k5, v4 = _split_x(bg)
+    k5, v4 = split_x_caches(bg)
     params = pa.make_params(bg.q, k5, bg.block_tables, max_seq_len=bg.max_seq_len,
                             scale=bg.scale, partition_size=512, out_dtype=torch.float32,
                             split_x=True)
@@ -614,26 +603,30 @@ def _one_launch_cases():
             (wl.scaled(wl.WORKLOADS["long_100k"], seq_len=60000), 1024)]  # two rounds of items
 
 
+@pytest.mark.parametrize("split_x", [False, True], ids=["standard", "split_x"])
 @pytest.mark.parametrize("case", [0, 1, 2], ids=["one_long_sequence", "mixed_lengths",
                                                  "two_rounds"])
-def test_one_launch_back_to_back_then_graph_replay(case):
-    """pa_decode_v2 as one launch: two steps in a row on one NaN-poisoned
-    workspace with different q and lengths, then the step captured in a CUDA
-    graph and replayed twice with new inputs; every step against the oracle,
-    and after each launch the control block ready for the next (marker
-    intact, epoch advanced by one, start count back at zero)."""
+def test_one_launch_back_to_back_then_graph_replay(case, split_x):
+    """pa_decode_v2 as one launch, on the standard and on the split-x cache
+    layout (each its own tensor-core kernel): two steps in a row on one
+    NaN-poisoned workspace with different q and lengths, then the step
+    captured in a CUDA graph and replayed twice with new inputs; every step
+    against the oracle, and after each launch the control block ready for
+    the next (marker intact, epoch advanced by one, start count back at
+    zero)."""
     w, P = _one_launch_cases()[case]
     bc = wl.make(w, poison=True)
     bg = bc.to("cuda")
-    params = pa.make_params(bc.q, bc.k_cache, bc.block_tables, max_seq_len=bc.max_seq_len,
+    kc, vc = split_x_caches(bg) if split_x else (bg.k_cache, bg.v_cache)
+    params = pa.make_params(bc.q, kc, bc.block_tables, max_seq_len=bc.max_seq_len,
                             scale=bc.scale, partition_size=P, out_dtype=torch.float32,
-                            v1_max_seq_len=1)                     # pa_decode's choice: V2
-    assert pa.decode_launches(params) == 1
+                            v1_max_seq_len=1, split_x=split_x)    # pa_decode's choice: V2
+    assert pa.decode_launches(params) == 1 and pa.decode_kernel(params) == 2
     ws = torch.empty(pa.workspace_size(params), dtype=torch.uint8, device="cuda")
     ws.view(torch.float32).fill_(float("nan"))
     pa.workspace_init(ws)
     out = torch.full(tuple(bc.q.shape), float("nan"), device="cuda")
-    kw = dict(max_seq_len=bc.max_seq_len, scale=bc.scale, partition_size=P)
+    kw = dict(max_seq_len=bc.max_seq_len, scale=bc.scale, partition_size=P, split_x=split_x)
     g = torch.Generator().manual_seed(90 + case)
     launches = [0]
 
@@ -654,12 +647,12 @@ def test_one_launch_back_to_back_then_graph_replay(case):
 
     for step, cut in enumerate((0, 333)):
         q, lens = new_inputs(cut)
-        pa.decode_v2(bg.q, bg.k_cache, bg.v_cache, bg.block_tables, bg.seq_lens, out, ws, **kw)
+        pa.decode_v2(bg.q, kc, vc, bg.block_tables, bg.seq_lens, out, ws, **kw)
         torch.cuda.synchronize()
         check(q, lens, f"step {step}")
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
-        pa.decode_v2(bg.q, bg.k_cache, bg.v_cache, bg.block_tables, bg.seq_lens, out, ws, **kw)
+        pa.decode_v2(bg.q, kc, vc, bg.block_tables, bg.seq_lens, out, ws, **kw)
     for rep, cut in enumerate((1000, 7)):
         q, lens = new_inputs(cut)
         out.fill_(float("nan"))
@@ -683,12 +676,13 @@ def test_one_launch_matches_two_launches_closely():
     assert np.array_equal(run(bg, path="v2", partition_size=256), one)
 
 
-def test_uninitialised_workspace_is_reported_not_reduced():
+@pytest.mark.parametrize("split_x", [False, True], ids=["standard", "split_x"])
+def test_uninitialised_workspace_is_reported_not_reduced(split_x):
     """A workspace that pa_workspace_init never initialised (NaN everywhere,
     control block included): the one-launch step reduces nothing, the status
     word reads PA_ERR_WORKSPACE_NOT_INIT, the rows it would have reduced
     (split sequences, and the empty one) are NaN, and the sequence that pass
-    1 finished itself is still right."""
+    1 finished itself is still right (both cache layouts)."""
     lens = [3000, 100, 0, 5000]
     w = dataclasses.replace(
         wl.WORKLOADS["mixed_32"], name="uninit", num_seqs=len(lens), num_heads=8,
@@ -697,13 +691,15 @@ def test_uninitialised_workspace_is_reported_not_reduced():
     bc = wl.make(w, poison=True)
     ref = _ref(bc)
     bg = bc.to("cuda")
-    params = pa.make_params(bc.q, bc.k_cache, bc.block_tables, max_seq_len=bc.max_seq_len,
-                            scale=bc.scale, partition_size=128, out_dtype=torch.float32,
-                            v1_max_seq_len=1)                     # pa_decode's choice: V2
+    params = pa.make_params(bc.q, split_x_caches(bc)[0] if split_x else bc.k_cache,
+                            bc.block_tables, max_seq_len=bc.max_seq_len, scale=bc.scale,
+                            partition_size=128, out_dtype=torch.float32, v1_max_seq_len=1,
+                            split_x=split_x)                      # pa_decode's choice: V2
     assert pa.decode_launches(params) == 1
     ws = torch.empty(pa.workspace_size(params), dtype=torch.uint8, device="cuda")
     ws.view(torch.float32).fill_(float("nan"))
-    got = run(bg, path="v2", partition_size=128, workspace=ws, check_status=False)
+    got = run(bg, path="v2", partition_size=128, workspace=ws, check_status=False,
+              split_x=split_x)
     assert pa.read_device_status(ws) == pa.PA_ERR_WORKSPACE_NOT_INIT
     for b, L in enumerate(lens):
         if L > 128 or L == 0:
@@ -712,7 +708,8 @@ def test_uninitialised_workspace_is_reported_not_reduced():
             assert_close(got[b], ref[b], 2e-3, f"sequence {b} (L={L})")
     # once initialised, the same workspace gives the right answer
     pa.workspace_init(ws)
-    assert_close(run(bg, path="v2", partition_size=128, workspace=ws), ref, 2e-3, "after init")
+    assert_close(run(bg, path="v2", partition_size=128, workspace=ws, split_x=split_x), ref,
+                 2e-3, "after init")
 
 
 def test_two_launches_for_many_rows():
