@@ -62,11 +62,15 @@ KERNEL_SOURCES = {
                           "pa_device.cuh", "pa_internal.h"),
     "pa_prefill_kernel": ("pa_prefill.cuh", "pa_prefill_host.cu", "pa_prefill_bf16.cu",
                           "pa_sm100.cuh", "pa_device.cuh", "pa_internal.h"),
+    "pa_sx_kernel": ("pa_sx.cuh", "pa_tc_host.cu", "pa_sx_bf16.cu", "pa_sm100.cuh",
+                     "pa_device.cuh", "pa_internal.h", "pa_grid_reduce.cuh"),
 }
 NCU_TRAFFIC = {
     # (kernel, source hash, workload, partition size, path): bytes per launch
     # the one-launch V2 kernel (pass 1 and the in-grid reduce)
-    ("pa_tc_kernel", "08d66c05ab0505f9", "long_100k", 512, "v2"): 409_756_416 + 3_763_968,
+    ("pa_tc_kernel", "c0d7a31c112c4204", "long_100k", 512, "v2"): 409_759_232 + 3_862_016,
+    # the split-x kernel in one launch (its own pass 1 and the same in-grid reduce)
+    ("pa_sx_kernel", "19c24b8aafd897b9", "long_100k", 512, "v2"): 409_763_840 + 5_198_336,
     ("pa_prefill_kernel", "686df58de52966ca", "prefill_32k", 0, "prefill"):
         1_354_087_424 + 194_575_616,
 }
