@@ -43,6 +43,8 @@
 // outputs become NaN.
 #pragma once
 
+#include <algorithm>
+#include <atomic>
 #include <type_traits>
 
 #include <cuda.h>
@@ -103,6 +105,17 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 }
 
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// consumer_sync that also returns whether any consumer thread passed true
+__device__ __forceinline__ bool consumer_any(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.or.pred q, 1, 128, p;\n"
+      "selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"(v ? 1u : 0u)
+      : "memory");
+  return r != 0;
+}
 
 // Two 16-bit values in one register (low half: the first).
 template <typename T>
@@ -111,6 +124,9 @@ __device__ __forceinline__ uint32_t pack2(T lo, T hi) {
 }
 
 constexpr int kQRows = 8;  // q tile rows: the query heads of one KV head
+// A cluster share's partial at the start of the ring (floats): per head m
+// and s, a poison flag, then O [8 heads][head_dim] (unnormalised)
+constexpr int kMergeM = 0, kMergeS = 8, kMergePoison = 16, kMergeO = 32;
 
 template <int D, int BS>
 struct Layout {
@@ -154,13 +170,16 @@ struct Item {
   int32_t t0, t1;  // token range (empty when t0 >= t1)
   bool len_ok;     // 0 <= seq_len <= max_seq_len
   bool direct;     // V2 with single_direct: the result is the final output
-  int nblk;        // blocks of the range (0 when it is empty)
+  bool any;        // the item's whole range (over all CTAs of a cluster) has tokens
+  int nblk;        // blocks of this CTA's range (0 when it is empty)
 };
 
 // Item k of the (partition, sequence, KV head) space, partition-major for V2
 // (ranges past a sequence's end come out empty), (sequence, KV head) for V1.
+// With a cluster of cs CTAs sharing the item, CTA `rank` takes a balanced
+// run of its 32-token chunks.
 template <int BS>
-__device__ __forceinline__ Item item_at(const KernelArgs& a, int64_t k, bool v2) {
+__device__ __forceinline__ Item item_at(const KernelArgs& a, int64_t k, bool v2, int rank, int cs) {
   Item it;
   const int64_t per_part = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads;
   it.part = v2 ? static_cast<int>(k / per_part) : 0;
@@ -172,6 +191,13 @@ __device__ __forceinline__ Item item_at(const KernelArgs& a, int64_t k, bool v2)
   it.t0 = v2 ? it.part * a.partition_size : 0;  // a multiple of BS
   it.t1 = !it.len_ok ? it.t0 : (v2 ? min(L, it.t0 + a.partition_size) : L);
   it.direct = v2 && a.single_direct && it.len_ok && L <= a.partition_size;
+  it.any = it.t0 < it.t1;
+  if (cs > 1 && it.any) {
+    const int nch = (it.t1 - it.t0 + kChunk - 1) / kChunk;
+    const int lo = rank * nch / cs, hi = (rank + 1) * nch / cs;
+    it.t1 = min(it.t1, it.t0 + hi * kChunk);
+    it.t0 += lo * kChunk;  // a multiple of kChunk, so of BS; empty when lo == hi
+  }
   it.nblk = it.t0 < it.t1 ? (it.t1 - 1) / BS - it.t0 / BS + 1 : 0;
   return it;
 }
@@ -180,7 +206,8 @@ __device__ __forceinline__ Item item_at(const KernelArgs& a, int64_t k, bool v2)
 
 template <typename T, int D, int BS, bool kV2>
 __global__ void __launch_bounds__(sx::kThreads, 2)
-    pa_sx_kernel(const KernelArgs a, const __grid_constant__ CUtensorMap pmap, int64_t total_items) {
+    pa_sx_kernel(const KernelArgs a, const __grid_constant__ CUtensorMap pmap, int64_t total_items,
+                 int cs) {
   using namespace sx;
   using Lay = Layout<D, BS>;
   static_assert(BS == 16 || BS == 32, "block size");
@@ -203,6 +230,10 @@ __global__ void __launch_bounds__(sx::kThreads, 2)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = a.group, Hq = a.num_heads;
   const T zero = round16(0.f, static_cast<T*>(nullptr));
+  // Clusters of cs CTAs (cs == 1: none) share each work item: the host then
+  // launches one cluster per item, and CTA `rank` streams its share.
+  const int rank = cs > 1 ? static_cast<int>(blockIdx.x % cs) : 0;
+  const int64_t cid = blockIdx.x / cs, cstride = gridDim.x / cs;
 
   // ---- set-up ---------------------------------------------------------------------
   const bool fused = kV2 && a.fused;  // one-launch V2: pass 2 by this grid at the end
@@ -253,8 +284,8 @@ __global__ void __launch_bounds__(sx::kThreads, 2)
                       // fewer than 2^32 blocks, so 32 bits keep the slot
                       // arithmetic short)
     int nq = 0;      // q tiles issued
-    for (int64_t k = blockIdx.x; k < total_items && ok; k += gridDim.x) {
-      const Item it = item_at<BS>(a, k, kV2);
+    for (int64_t k = cid; k < total_items && ok; k += cstride) {
+      const Item it = item_at<BS>(a, k, kV2, rank, cs);
       if (it.nblk == 0) continue;
       const int qb = nq & 1;
       ok = __all_sync(0xffffffffu, sm100::mbar_wait(&qempty[qb], ((nq >> 1) & 1) ^ 1,
@@ -314,15 +345,33 @@ __global__ void __launch_bounds__(sx::kThreads, 2)
       for (int i = nq > 2 ? nq - 2 : 0; i < nq; ++i)
         sm100::mbar_wait(&qfull[i & 1], (i >> 1) & 1, kWaitBudget, nullptr);
     }
-    return;
-  }
-
+    if (cs == 1) return;  // in a cluster the warp meets the merge's barriers below
+  } else {
   // =========================== consumers (warps 0-3) ================================
   const int g = lane >> 2, t = lane & 3;  // mma fragment: row group, column pair
   const float sl2 = a.scale_log2;
   const uint32_t p_base = sm100::smem_u32(ps);
   const uint32_t ring_base = sm100::smem_u32(ring);
   constexpr int kDT = D / 4 / 8;  // 8-wide head_dim tiles of this warp's P.V slice
+  // a cluster share's result, left for the merge at the start of the ring
+  // (every block of the share was consumed: the ring is free)
+  float* const mgp = reinterpret_cast<float*>(ring);
+  auto write_partial = [&](float m, float sv, float (*accp)[kDT][4], bool pois) {
+    const bool any_pois = consumer_any(pois);  // a barrier too: the ring reads are done
+    if (g < G) {
+#pragma unroll
+      for (int i = 0; i < kDT; ++i) {
+        const int d = warp * (D / 4) + i * 8 + 2 * t;
+        mgp[kMergeO + g * D + d] = accp ? (*accp)[i][0] + (*accp)[i][2] : 0.f;
+        mgp[kMergeO + g * D + d + 1] = accp ? (*accp)[i][1] + (*accp)[i][3] : 0.f;
+      }
+      if (warp == 0 && t == 0) {
+        mgp[kMergeM + g] = m;
+        mgp[kMergeS + g] = sv;
+      }
+    }
+    if (tid == 0) mgp[kMergePoison] = any_pois ? 1.f : 0.f;
+  };
   int hs = 0;                      // ring slot of the next block to consume
   uint32_t hp = 0;                 // and its phase parity (no division in the hot loop)
   auto wrap = [](int x) { return x >= Lay::kStages ? x - Lay::kStages : x; };
@@ -341,11 +390,15 @@ __global__ void __launch_bounds__(sx::kThreads, 2)
     __syncwarp();
     if (lane == 0) sm100::mbar_arrive(dry_done);
   }
-  for (int64_t k = blockIdx.x; k < total_items; k += gridDim.x) {
-    const Item it = item_at<BS>(a, k, kV2);
+  for (int64_t k = cid; k < total_items; k += cstride) {
+    const Item it = item_at<BS>(a, k, kV2, rank, cs);
     const int64_t row0 = static_cast<int64_t>(it.b) * Hq + static_cast<int64_t>(it.kvh) * G;
     if (it.nblk == 0) {
-      if (!it.len_ok && tid == 0 && it.part == 0) set_status(a.status, PA_ERR_BAD_SEQ_LEN);
+      if (!it.len_ok && tid == 0 && it.part == 0 && rank == 0) set_status(a.status, PA_ERR_BAD_SEQ_LEN);
+      if (cs > 1) {  // an empty share: the merge sees m = -inf, s = 0, O = 0
+        write_partial(-INFINITY, 0.f, nullptr, false);
+        continue;
+      }
       if (!kV2) {  // V1: NaN rows for a bad length, zero rows for an empty sequence
         const float v = it.len_ok ? 0.f : qnan();
         for (int i = tid; i < G * D; i += kConsumerWarps * 32)
@@ -501,6 +554,10 @@ __global__ void __launch_bounds__(sx::kThreads, 2)
 
     // ---- epilogue: O[g] = (rows g + rows g + 8) / s --------------------------------
     poison |= *abort_flag != 0;
+    if (cs > 1) {  // the cluster merges the CTAs' shares below
+      write_partial(m_run, s_run, &acc, poison);
+      continue;
+    }
     if (g < G) {
       const int64_t row = row0 + g;
 #pragma unroll
@@ -533,24 +590,155 @@ __global__ void __launch_bounds__(sx::kThreads, 2)
                             *reinterpret_cast<gridred::UnitScratch*>(ring), &pmap, red_bar, tid,
                             kWaitBudget, false);
   }
+  }
+
+  // ---- cluster merge (cs > 1: one item per cluster) -------------------------------
+  // Every CTA left its share's (m, s, unnormalised O, poison) at the start of
+  // its ring; after a cluster barrier CTA `rank` merges head_dim columns
+  // rank * D / cs .. for the item's G heads, with the same log-sum-exp
+  // identity as the V2 reduce (weights exp2(m_r - M)), then a second barrier
+  // keeps every CTA's shared memory alive until its peers have read it.
+  if (cs > 1) {
+    sm100::cluster_sync_all();
+    if (warp < kConsumerWarps && cid < total_items) {
+      const Item it = item_at<BS>(a, cid, kV2, rank, cs);
+      const int64_t row0 = static_cast<int64_t>(it.b) * Hq + static_cast<int64_t>(it.kvh) * G;
+      if (it.any) {
+        const int ncol = D / cs;
+        const uint32_t mg = sm100::smem_u32(ring);
+        for (int e = tid; e < G * ncol; e += kConsumerWarps * 32) {
+          const int gh = e / ncol, d = rank * ncol + e % ncol;
+          const int64_t row = row0 + gh;
+          float M = -INFINITY;
+          bool pois = false;
+          for (int p = 0; p < cs; ++p) {
+            const uint32_t pb = sm100::mapa_shared(mg, static_cast<uint32_t>(p));
+            M = fmaxf(M, sm100::ld_shared_cluster_f32(pb + (kMergeM + gh) * 4));
+            pois |= sm100::ld_shared_cluster_f32(pb + kMergePoison * 4) != 0.f;
+          }
+          float S = 0.f, O = 0.f;
+          for (int p = 0; p < cs; ++p) {
+            const uint32_t pb = sm100::mapa_shared(mg, static_cast<uint32_t>(p));
+            const float m = sm100::ld_shared_cluster_f32(pb + (kMergeM + gh) * 4);
+            const float w = m == -INFINITY ? 0.f : exp2f(m - M);
+            S += w * sm100::ld_shared_cluster_f32(pb + (kMergeS + gh) * 4);
+            O += w * sm100::ld_shared_cluster_f32(pb + (kMergeO + gh * D + d) * 4);
+          }
+          const float res = pois ? qnan() : O / S;
+          if (!kV2 || it.direct) {
+            store_out(a.out, row * D + d, a.out_dtype, res);
+          } else {
+            a.tmp_out[(row * a.num_partitions + it.part) * D + d] = res;
+            if (rank == 0 && e % ncol == 0) {
+              const int64_t w = row * a.num_partitions + it.part;
+              a.max_logits[w] = pois ? qnan() : M * kLn2;
+              a.exp_sums[w] = S;
+            }
+          }
+        }
+      } else if (!kV2 && rank == 0) {  // V1: NaN rows for a bad length, zeros for L = 0
+        for (int i = tid; i < G * D; i += kConsumerWarps * 32)
+          store_out(a.out, row0 * D + i, a.out_dtype, it.len_ok ? 0.f : qnan());
+      }
+    }
+    sm100::cluster_sync_all();
+  }
+}
+
+// Kernel attributes, set once per device and instantiation: the dynamic
+// shared memory, and clusters of up to 16 CTAs.
+template <typename T, int D, int BS, bool V2>
+cudaError_t configure_sx(int dev) {
+  static std::atomic<bool> configured[128];
+  if (configured[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  auto kern = pa_sx_kernel<T, D, BS, V2>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       sx::Layout<D, BS>::kSmem);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e == cudaSuccess) configured[dev].store(true, std::memory_order_release);
+  return e;
+}
+
+// Largest cluster size <= want (a power of two) of which at least `need`
+// clusters can be resident at once (queried once per device and size).
+template <typename T, int D, int BS, bool V2>
+int fit_sx_cluster(int dev, int want, int64_t need) {
+  static std::atomic<int> resident[128][5];  // [device][log2 size], 0 = not queried yet
+  int lg = 0;
+  while ((2 << lg) <= want && lg < 4) ++lg;
+  for (; lg >= 1; --lg) {
+    const int cs = 1 << lg;
+    int r = resident[dev][lg].load(std::memory_order_relaxed);
+    if (r == 0) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(static_cast<unsigned>(cs), 1, 1);
+      cfg.blockDim = dim3(sx::kThreads, 1, 1);
+      cfg.dynamicSmemBytes = static_cast<size_t>(sx::Layout<D, BS>::kSmem);
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, pa_sx_kernel<T, D, BS, V2>, &cfg) != cudaSuccess) {
+        cudaGetLastError();  // a refused size is not an error of the decode call
+        n = 0;
+      }
+      r = n > 0 ? n : -1;
+      resident[dev][lg].store(r, std::memory_order_relaxed);
+    }
+    if (r >= need) return cs;
+  }
+  return 1;
+}
+
+template <typename T, int D, int BS, bool V2>
+cudaError_t launch_sx_v(const KernelArgs& a, const CUtensorMap& pm, int64_t items, int sms,
+                        cudaStream_t s) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+  if (cudaError_t e = configure_sx<T, D, BS, V2>(dev)) return e;
+  // persistent: at most two CTAs per SM, items dealt out in balanced rounds
+  const int64_t persistent = sms > 0 ? tc_persistent_grid(items, false, sms) : 0;
+  int cs = 1;
+  if (persistent == 0 && sms > 0) {
+    // Fewer items than SMs: a cluster of cs CTAs (up to 16) shares each item,
+    // splitting its 32-token chunks and merging the shares through
+    // distributed shared memory, while every CTA keeps at least 8 chunks
+    // (256 tokens), below which the merge costs more than the split saves.
+    const int range = V2 ? std::min(a.partition_size, a.max_seq_len) : a.max_seq_len;
+    const int chunks = (range + sx::kChunk - 1) / sx::kChunk;
+    int want = 1;
+    while (want < 16 && items * want * 2 <= 2LL * sms && want * 2 * 8 <= chunks) want *= 2;
+    if (want > 1 && !a.fused) cs = fit_sx_cluster<T, D, BS, V2>(dev, want, items);
+  }
+  const int64_t grid = persistent > 0 ? persistent : items * cs;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(sx::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(sx::Layout<D, BS>::kSmem);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cs);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = cs > 1 ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, pa_sx_kernel<T, D, BS, V2>, a, pm, items, cs);
 }
 
 template <typename T, int D, int BS>
 cudaError_t launch_sx_t(const KernelArgs& a, const CUtensorMap& pm, bool v2, cudaStream_t s) {
-  using Lay = sx::Layout<D, BS>;
   const int64_t items =
       static_cast<int64_t>(a.num_seqs) * a.num_kv_heads * (v2 ? a.num_partitions : 1);
   if (items == 0) return cudaSuccess;
-  // persistent: at most two CTAs per SM; one CTA per item below one item per SM
   const int sms = sm100_num_sms();
-  const int64_t persistent = sms > 0 ? tc_persistent_grid(items, false, sms) : 0;
-  const int64_t grid = persistent > 0 ? persistent : items;
-  if (grid > 0x7fffffffLL) return cudaErrorInvalidValue;
-  auto kern = v2 ? pa_sx_kernel<T, D, BS, true> : pa_sx_kernel<T, D, BS, false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kSmem);
-  if (e != cudaSuccess) return e;
-  kern<<<static_cast<unsigned>(grid), sx::kThreads, Lay::kSmem, s>>>(a, pm, items);
-  return cudaGetLastError();
+  return v2 ? launch_sx_v<T, D, BS, true>(a, pm, items, sms, s)
+            : launch_sx_v<T, D, BS, false>(a, pm, items, sms, s);
 }
 
 template <typename T>

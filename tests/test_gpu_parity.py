@@ -566,6 +566,56 @@ def test_split_x_persistent_walk(dtype, D, BS):
             assert pa.read_device_status(ws) == pa.PA_ERR_BAD_BLOCK_ID
 
 
+def test_split_x_clusters_share_items():
+    """Fewer split-x work items than SMs: a cluster of CTAs shares each item
+    and merges the shares through distributed shared memory.  V1 (clusters
+    of 8 here) on lengths that leave some CTAs of a cluster without tokens
+    (5 and 0 tokens), V2 at P = 4096 (clusters of 4, then the reduce), and
+    the one-sequence 8192-token workload through pa_decode (V1, clusters of
+    16): every row against the oracle, and a block id outside the pool in
+    one CTA's share poisons only its sequence."""
+    lens = (8192, 5, 0, 3001)
+    kw = dict(dtype=torch.bfloat16, lens=lens, Hq=24, Hkv=4, D=256, BS=16, seed=41)
+    ref = _ref(problem(**kw))
+    bc = problem(**kw)
+    bad_seq = 3
+    bc.block_tables[bad_seq, 100] = bc.k_cache.shape[0] + 3   # token 1600: a middle share
+    bg = bc.to("cuda")
+    k5, v4 = (t.cuda() for t in split_x_caches(bc))
+    kx = dict(max_seq_len=bc.max_seq_len, scale=bc.scale, split_x=True)
+    keep = [b for b in range(len(lens)) if b != bad_seq]
+    got = torch.full(tuple(bc.q.shape), float("nan"), device="cuda")
+    pa.decode_v1(bg.q, k5, v4, bg.block_tables, bg.seq_lens, got, **kx)
+    torch.cuda.synchronize()
+    g = got.double().cpu().numpy()
+    assert np.all(np.isnan(g[bad_seq]))
+    assert_close(g[keep], ref[keep], TOL[torch.bfloat16], "split-x V1 in clusters")
+    assert np.all(g[2] == 0.0)                                  # the empty sequence
+    params = pa.make_params(bc.q, k5, bc.block_tables, partition_size=4096,
+                            out_dtype=torch.float32, **kx)
+    ws = pa.alloc_workspace(params)
+    got.fill_(float("nan"))
+    pa.decode_v2(bg.q, k5, v4, bg.block_tables, bg.seq_lens, got, ws, partition_size=4096, **kx)
+    torch.cuda.synchronize()
+    g = got.double().cpu().numpy()
+    assert np.all(np.isnan(g[bad_seq]))
+    assert_close(g[keep], ref[keep], TOL[torch.bfloat16], "split-x V2 in clusters")
+    assert pa.read_device_status(ws) == pa.PA_ERR_BAD_BLOCK_ID
+    # config 2's shape: one 8192-token sequence, pa_decode -> V1
+    w = wl.WORKLOADS["gqa_8k"]
+    bc2 = wl.make(w, poison=True)
+    bg2 = bc2.to("cuda")
+    k5, v4 = split_x_caches(bg2)
+    params = pa.make_params(bg2.q, k5, bg2.block_tables, max_seq_len=bg2.max_seq_len,
+                            scale=bg2.scale, out_dtype=torch.float32, split_x=True)
+    assert pa.decode_path(params) == 1 and pa.decode_kernel(params) == 2
+    got = torch.full(tuple(bg2.q.shape), float("nan"), device="cuda")
+    pa.decode(bg2.q, k5, v4, bg2.block_tables, bg2.seq_lens, got, None,   # V1: no workspace
+              max_seq_len=bg2.max_seq_len, scale=bg2.scale, split_x=True)
+    torch.cuda.synchronize()
+    assert_close(got.double().cpu().numpy(), _ref(bc2), TOL[w.dtype], "split-x gqa_8k V1")
+
+
 def test_split_x_full_size_long_context():
     """The 100K-token long-context workload with its caches rewritten (on the
     device, as test input) into the split-x layout: pa_decode (V2) on the
