@@ -18,9 +18,10 @@
 //
 // The reduce runs once per CTA, at the very end of a long kernel, so its code
 // would be fetched cold (measured: about 2.7 us of a 3.9 us unit on GB300).
-// The softmax warps therefore run the unit once at the kernel's start, in a
-// dry mode with no side effects, while the first keys are still landing, so
-// that the code is in the SM's instruction cache when it is needed.
+// The standard-layout kernel's softmax warps therefore run the unit once at
+// the kernel's start, in a dry mode with no side effects, while the first
+// keys are still landing, so that the code is in the SM's instruction cache
+// when it is needed.
 //
 // Forward progress.  Only CTAs that have started can be waited for: a CTA
 // waits for the others only if the start counter shows that every CTA of the

@@ -143,22 +143,20 @@ struct Layout {
   static constexpr int kRedOff = kPOff + 16 * kPStride * 2;  // [4 warps][8 heads] max, sum
   static constexpr int kBarOff = kRedOff + 2 * kConsumerWarps * 8 * 4;
   // full[kMaxStages], empty[kMaxStages], qfull[2], qempty[2], and for the
-  // one-launch V2 grid: red_bar (a reduce unit's tile copy), dry_done
-  static constexpr int kFlagOff = kBarOff + (2 * kMaxStages + 6) * 8;
+  // one-launch V2 grid red_bar (a reduce unit's tile copy)
+  static constexpr int kFlagOff = kBarOff + (2 * kMaxStages + 5) * 8;
   // [0] abort; [1 + s] ring slot s holds no block (its id was out of range);
   // [kWsOk] the workspace carries the init marker; [kRedWord ..] three ints
   // for the reduce's broadcasts
   static constexpr int kWsOk = 1 + kMaxStages;
   static constexpr int kRedWord = kWsOk + 1;
   static constexpr int kSmem = kFlagOff + (kRedWord + 3) * 4 + 64;
-  // One-launch V2: the reduce's scratch is the ring once streaming is done;
-  // its dry run at the start takes the ring's last kDrySlots slots, which the
-  // producer fills for the first time only after that run.
-  static constexpr int kRingEnd = kStages * kStageBytes;
-  static constexpr int kDryOff = kRingEnd - static_cast<int>((gridred::kDryBytes + 127) / 128 * 128);
-  static constexpr int kDrySlots = (kRingEnd - kDryOff + kStageBytes - 1) / kStageBytes;
-  static_assert(sizeof(gridred::UnitScratch) <= kRingEnd, "reduce scratch in the ring");
-  static_assert(kDrySlots < kStages, "dry run beside the first stages");
+  // One-launch V2: the reduce's scratch is the ring once streaming is done.
+  // (No dry run of the reduce at the start, unlike the standard-layout
+  // kernel: here it would hold back the first fill of the ring slots it
+  // borrows, which measured 2.4 us slower per step than the cold code it
+  // saves at the end.)
+  static_assert(sizeof(gridred::UnitScratch) <= kStages * kStageBytes, "reduce scratch in the ring");
   static_assert(kStages >= 2 * kChunkBlocks, "two chunks in flight");
   static_assert((kQStride * 2) % 16 == 0 && kQOff % 16 == 0, "bulk copies of q rows");
   static_assert(kSmem <= 113 * 1024, "two CTAs per SM");
@@ -222,7 +220,6 @@ __global__ void __launch_bounds__(sx::kThreads, 2)
   uint64_t* qfull = empty + kMaxStages;
   uint64_t* qempty = qfull + 2;
   uint64_t* red_bar = qempty + 2;
-  uint64_t* dry_done = red_bar + 1;
   int* flags = reinterpret_cast<int*>(smem + Lay::kFlagOff);
   volatile int* abort_flag = &flags[0];
   volatile int* bad = flags + 1;
@@ -254,7 +251,6 @@ __global__ void __launch_bounds__(sx::kThreads, 2)
     int ws_ok = 0;
     if (fused) {
       sm100::mbar_init(red_bar, 1);
-      sm100::mbar_init(dry_done, kConsumerWarps);
       ws_ok = __ldcg(a.status + kMarkerOffset / 4) == kMarker;
       if (ws_ok)
         started = gridred::count_started(a);
@@ -269,7 +265,6 @@ __global__ void __launch_bounds__(sx::kThreads, 2)
     if (r >= G) qs[tile * Lay::kQTile + r * Lay::kQStride + i % D] = zero;
   }
   __syncthreads();
-  const bool dry_run = fused && flags[Lay::kWsOk] != 0;
 
   if (warp == kConsumerWarps) {
     // ========================= producer =======================================
@@ -310,8 +305,6 @@ __global__ void __launch_bounds__(sx::kThreads, 2)
           const uint32_t par = static_cast<uint32_t>((jg / Lay::kStages) & 1) ^ 1;
           ok = __all_sync(0xffffffffu,
                           sm100::mbar_wait(&empty[slot], par, kWaitBudget, abort_flag));
-          if (ok && dry_run && jg >= Lay::kStages - Lay::kDrySlots && jg < Lay::kStages)
-            ok = __all_sync(0xffffffffu, sm100::mbar_wait(dry_done, 0, kWaitBudget, abort_flag));
           if (!ok) break;
           const int32_t id = __shfl_sync(0xffffffffu, id_l, jj);
           if (lane == 0) {
@@ -377,19 +370,6 @@ __global__ void __launch_bounds__(sx::kThreads, 2)
   auto wrap = [](int x) { return x >= Lay::kStages ? x - Lay::kStages : x; };
   int nq = 0;                     // q tiles consumed
   int* const red_word = flags + Lay::kRedWord;
-  if (dry_run) {
-    // One-launch V2: run the end-of-kernel reduce once now, dry (no side
-    // effects; scratch at the ring's end, which the producer leaves alone
-    // until dry_done), so its code is in the instruction cache at the end.
-    gridred::UnitScratch& dsc = *reinterpret_cast<gridred::UnitScratch*>(ring + Lay::kDryOff);
-    uint32_t dry_phase = 0;
-    gridred::grid_reduce<D>(a, true, started, red_word, dsc, &pmap, red_bar, tid, kWaitBudget,
-                            true);
-    gridred::reduce_unit<D>(a, &pmap, red_bar, dry_phase, 0, 0, dsc, tid, false, kWaitBudget,
-                            true);
-    __syncwarp();
-    if (lane == 0) sm100::mbar_arrive(dry_done);
-  }
   for (int64_t k = cid; k < total_items; k += cstride) {
     const Item it = item_at<BS>(a, k, kV2, rank, cs);
     const int64_t row0 = static_cast<int64_t>(it.b) * Hq + static_cast<int64_t>(it.kvh) * G;
