@@ -68,11 +68,11 @@ KERNEL_SOURCES = {
 NCU_TRAFFIC = {
     # (kernel, source hash, workload, partition size, path): bytes per launch
     # the one-launch V2 kernel (pass 1 and the in-grid reduce)
-    ("pa_tc_kernel", "c0d7a31c112c4204", "long_100k", 512, "v2"): 409_759_232 + 3_862_016,
+    ("pa_tc_kernel", "7ce83006e435e1ac", "long_100k", 512, "v2"): 409_759_744 + 3_002_880,
     # the split-x kernel in one launch (its own pass 1 and the same in-grid reduce)
-    ("pa_sx_kernel", "19c24b8aafd897b9", "long_100k", 512, "v2"): 409_763_840 + 5_198_336,
-    ("pa_prefill_kernel", "686df58de52966ca", "prefill_32k", 0, "prefill"):
-        1_354_087_424 + 194_575_616,
+    ("pa_sx_kernel", "65c2770a449a512d", "long_100k", 512, "v2"): 409_756_928 + 4_888_320,
+    ("pa_prefill_kernel", "18ddecd480df6262", "prefill_32k", 0, "prefill"):
+        1_355_374_592 + 193_046_528,
 }
 
 
