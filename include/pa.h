@@ -100,8 +100,10 @@ typedef enum pa_dtype { PA_F32 = 0, PA_BF16 = 1, PA_F16 = 2 } pa_dtype_t;
                               copy: for bf16 / f16 caches with block_size 16
                               or 32 and at most 8 query heads per KV head by
                               a tensor-core kernel (warp-level MMA fed by
-                              ldmatrix from whole-block bulk copies), else by
-                              the CUDA-core kernels; every call accepts it. */
+                              ldmatrix from whole-block bulk copies; V2 in one
+                              launch and V1 in clusters as on the standard
+                              layout), else by the CUDA-core kernels; every
+                              call accepts it. */
 
 typedef struct pa_params {
   int32_t num_seqs;           /* B >= 0                                      */
@@ -157,7 +159,10 @@ PA_API size_t pa_workspace_size(const pa_params_t* params);
 
 /*
  * V1: one pass per (sequence, KV head) over the whole sequence, normalised
- * straight into `out`.  No workspace.
+ * straight into `out`.  No workspace: when there are fewer (sequence, KV
+ * head) pairs than SMs, the tensor-core kernels (either cache layout) share
+ * each pair across a thread-block cluster of up to 16 CTAs that merge their
+ * partial results in distributed shared memory.
  * Source: commit 1a4e1005 "paged_attn.py", change 1 (V1 single-CTA
  * iteration); commit 4eb83a7e "qwen3_6_scripts", paragraph "V1
  * paged_attention (decode <= 8192)".
@@ -173,8 +178,8 @@ PA_API pa_status_t pa_decode_v1(const pa_params_t* params, const void* q, const 
  * exp(m_p - max_p m_p) * s_p and writes `out`.
  * `workspace` must hold pa_workspace_size(params) bytes, its control block
  * initialised by pa_workspace_init.
- * One launch: when the tensor-core kernel runs as a persistent grid with at
- * least one CTA per reduce unit (num_seqs * num_heads * head_dim / 32 units:
+ * One launch: when a tensor-core kernel (either cache layout) runs as a
+ * persistent grid with at least one CTA per reduce unit (num_seqs * num_heads * head_dim / 32 units:
  * few long sequences, e.g. one 100K-token sequence), pass 2 runs in the same
  * launch.  Each CTA, after its partitions, counts itself finished in the
  * workspace; CTAs that finish once every CTA of the grid has started take
