@@ -19,7 +19,10 @@
 // or the whole sequence (V1); the G <= 8 query heads of the KV head are
 // served together.  The grid is persistent (at most two CTAs per SM, the
 // items dealt out in balanced rounds): CTA c takes items c, c + gridDim.x,
-// ...  Warp 4 streams the blocks of all its items, one after the other, into
+// ...; with fewer items than SMs, a cluster of up to 16 CTAs shares each
+// item instead (each CTA a balanced run of its chunks) and the CTAs merge
+// their partial results through distributed shared memory at the end.
+// Warp 4 streams the blocks of all its items, one after the other, into
 // one ring of whole blocks (keys and values), so the next item's blocks are
 // in flight while the current one finishes, and loads each item's q rows by
 // bulk copy into one of two q tiles; warps 0-3 consume the ring in chunks of
@@ -374,7 +377,8 @@ __global__ void __launch_bounds__(sx::kThreads, 2)
     const Item it = item_at<BS>(a, k, kV2, rank, cs);
     const int64_t row0 = static_cast<int64_t>(it.b) * Hq + static_cast<int64_t>(it.kvh) * G;
     if (it.nblk == 0) {
-      if (!it.len_ok && tid == 0 && it.part == 0 && rank == 0) set_status(a.status, PA_ERR_BAD_SEQ_LEN);
+      if (!it.len_ok && tid == 0 && it.part == 0 && rank == 0)
+        set_status(a.status, PA_ERR_BAD_SEQ_LEN);
       if (cs > 1) {  // an empty share: the merge sees m = -inf, s = 0, O = 0
         write_partial(-INFINITY, 0.f, nullptr, false);
         continue;
