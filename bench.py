@@ -53,8 +53,9 @@ L2_FLUSH_BYTES = 256 << 20
 L2_BYTES = 129 << 20
 
 # DRAM bytes (read + write) per launch of the dominant kernel, from one ncu
-# capture, keyed by a hash of the sources that kernel is built from.  A change
-# to any of them makes the figure stale, and the bench then reports null.
+# capture, keyed by a hash of the code (comments and layout left out) of the
+# sources that kernel is built from.  A change to any of them makes the
+# figure stale, and the bench then reports null.
 KERNEL_SOURCES = {
     "pa_tc_kernel": ("pa_tc.cuh", "pa_tc_host.cu", "pa_tc_bf16.cu", "pa_sm100.cuh",
                      "pa_device.cuh", "pa_internal.h", "pa_grid_reduce.cuh"),
@@ -68,20 +69,47 @@ KERNEL_SOURCES = {
 NCU_TRAFFIC = {
     # (kernel, source hash, workload, partition size, path): bytes per launch
     # the one-launch V2 kernel (pass 1 and the in-grid reduce)
-    ("pa_tc_kernel", "7ce83006e435e1ac", "long_100k", 512, "v2"): 409_759_744 + 3_002_880,
+    ("pa_tc_kernel", "3d7ca941fdab05a2", "long_100k", 512, "v2"): 409_759_744 + 3_002_880,
     # the split-x kernel in one launch (its own pass 1 and the same in-grid reduce)
-    ("pa_sx_kernel", "65c2770a449a512d", "long_100k", 512, "v2"): 409_756_928 + 4_888_320,
-    ("pa_prefill_kernel", "18ddecd480df6262", "prefill_32k", 0, "prefill"):
+    ("pa_sx_kernel", "30358b6f94ffe4b1", "long_100k", 512, "v2"): 409_756_928 + 4_888_320,
+    ("pa_prefill_kernel", "a751245a46a2df8a", "prefill_32k", 0, "prefill"):
         1_355_374_592 + 193_046_528,
 }
+
+
+def _code_only(text: str) -> str:
+    """C / C++ source without its comments and with whitespace runs folded
+    to one space (string literals kept as they are), so that an edit of a
+    comment or of the layout does not count as a change of the kernel."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        ch = text[i]
+        if ch == '"':  # string literal, escapes included
+            j = i + 1
+            while j < n and text[j] != '"':
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(ch)
+            i += 1
+    return " ".join("".join(out).split())
 
 
 def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
     for name in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(ROOT, "paged_attention_decode_v2_gb300", "csrc", name), "rb") as fh:
+        with open(os.path.join(ROOT, "paged_attention_decode_v2_gb300", "csrc", name),
+                  encoding="utf-8") as fh:
             h.update(name.encode())
-            h.update(fh.read())
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 
