@@ -81,11 +81,12 @@ typedef enum pa_dtype { PA_F32 = 0, PA_BF16 = 1, PA_F16 = 2 } pa_dtype_t;
 /* Flags (pa_params_t.flags). */
 #define PA_FLAG_PORTABLE 1 /* use the CUDA-core kernels even where the
                               TMA / tensor-core kernels apply              */
-#define PA_FLAG_SELFTEST_STALL 2 /* diagnostic: the tensor-core kernel first
-                              waits for an event that never happens, with a
-                              short (~10 ms) bound, so its bounded-wait path
+#define PA_FLAG_SELFTEST_STALL 2 /* diagnostic: the tensor-core kernels
+                              (either cache layout; prefill too) first wait
+                              for an event that never happens, with a short
+                              (~10 ms) bound, so their bounded-wait path
                               runs: the call's outputs become NaN and the
-                              workspace status word reads
+                              workspace status word (V2) reads
                               PA_ERR_DEVICE_TIMEOUT.  Ignored by the
                               CUDA-core kernels, which have no such waits. */
 #define PA_FLAG_SPLIT_X 4 /* the caches are in the layout commit 4eb83a7e

@@ -246,12 +246,14 @@ def _params_for(q, k_cache, block_tables, out, max_seq_len, scale, partition_siz
 
 
 def decode_v1(q, k_cache, v_cache, block_tables, seq_lens, out, *, max_seq_len: int,
-              scale: float, portable: bool = False, split_x: bool = False, stream=None):
+              scale: float, portable: bool = False, split_x: bool = False, flags: int = 0,
+              stream=None):
     """``pa_decode_v1``: single pass per (sequence, KV head), into ``out``.
-    ``split_x``: the caches are in the split-x layout (``PA_FLAG_SPLIT_X``)."""
+    ``split_x``: the caches are in the split-x layout (``PA_FLAG_SPLIT_X``);
+    ``flags``: further ``PA_FLAG_*`` bits."""
     _check_inputs(q, k_cache, v_cache, block_tables, seq_lens, out, split_x)
     p = _params_for(q, k_cache, block_tables, out, max_seq_len, scale, 512,
-                    DEFAULT_V1_MAX_SEQ_LEN, portable, split_x=split_x)
+                    DEFAULT_V1_MAX_SEQ_LEN, portable, flags, split_x)
     st = lib().pa_decode_v1(ctypes.byref(p), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                             _ptr(block_tables), _ptr(seq_lens), _ptr(out), _stream(stream))
     if st != PA_OK:

@@ -65,6 +65,7 @@ constexpr int kChunk = 32;                           // tokens per chunk
 constexpr int kRingBytes = 96 * 1024;                // two CTAs per SM
 constexpr int kMaxStages = 24;
 constexpr long long kWaitBudget = 4000000000LL;      // cycles (about 2 s)
+constexpr long long kSelftestBudget = 20000000LL;    // cycles (about 10 ms)
 
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
@@ -145,9 +146,10 @@ struct Layout {
   static constexpr int kPOff = kQOff + 2 * kQTile * 2;
   static constexpr int kRedOff = kPOff + 16 * kPStride * 2;  // [4 warps][8 heads] max, sum
   static constexpr int kBarOff = kRedOff + 2 * kConsumerWarps * 8 * 4;
-  // full[kMaxStages], empty[kMaxStages], qfull[2], qempty[2], and for the
-  // one-launch V2 grid red_bar (a reduce unit's tile copy)
-  static constexpr int kFlagOff = kBarOff + (2 * kMaxStages + 5) * 8;
+  // full[kMaxStages], empty[kMaxStages], qfull[2], qempty[2], for the
+  // one-launch V2 grid red_bar (a reduce unit's tile copy), and never (the
+  // self-test's wait: nothing arrives there)
+  static constexpr int kFlagOff = kBarOff + (2 * kMaxStages + 6) * 8;
   // [0] abort; [1 + s] ring slot s holds no block (its id was out of range);
   // [kWsOk] the workspace carries the init marker; [kRedWord ..] three ints
   // for the reduce's broadcasts
@@ -223,6 +225,7 @@ __global__ void __launch_bounds__(sx::kThreads, 2)
   uint64_t* qfull = empty + kMaxStages;
   uint64_t* qempty = qfull + 2;
   uint64_t* red_bar = qempty + 2;
+  uint64_t* never = red_bar + 1;
   int* flags = reinterpret_cast<int*>(smem + Lay::kFlagOff);
   volatile int* abort_flag = &flags[0];
   volatile int* bad = flags + 1;
@@ -248,6 +251,7 @@ __global__ void __launch_bounds__(sx::kThreads, 2)
       sm100::mbar_init(&qfull[i], 1);
       sm100::mbar_init(&qempty[i], kConsumerWarps);
     }
+    sm100::mbar_init(never, 1);
     flags[0] = 0;
     // one-launch V2: the counters are usable only in an initialised workspace;
     // the CTA counts itself started (the result is first used at the end)
@@ -278,6 +282,10 @@ __global__ void __launch_bounds__(sx::kThreads, 2)
     const char* qg = static_cast<const char*>(a.q);
     if (fused && lane == 0) sm100::tma_prefetch_desc(&pmap);
     bool ok = true;
+    // self-test (PA_FLAG_SELFTEST_STALL): a wait that runs out, so that the
+    // abort path runs (no copy issued; every output of the call becomes NaN)
+    if (a.selftest_stall)
+      ok = __all_sync(0xffffffffu, sm100::mbar_wait(never, 0, kSelftestBudget, abort_flag));
     uint32_t jg = 0;  // ring blocks issued, over all items (a CTA streams far
                       // fewer than 2^32 blocks, so 32 bits keep the slot
                       // arithmetic short)

@@ -94,3 +94,50 @@ def test_prefill_wait_that_runs_out_gives_nan_and_context_survives():
     ref = oracle.prefill(pb.q, pb.k, pb.v, pb.k_cache, pb.v_cache, pb.block_tables,
                          pb.query_start, pb.ctx_lens, pb.scale)
     assert float(np.max(np.abs(out.double().cpu().numpy() - ref))) <= 4e-3
+
+
+def test_split_x_wait_that_runs_out():
+    """The split-x tensor-core kernel's bounded waits (PA_FLAG_SELFTEST_STALL):
+    the one-launch V2 step (persistent grid, pass 2 in the same launch) and
+    V1 in clusters (CTAs sharing a sequence and merging in distributed shared
+    memory) both end with NaN outputs instead of hanging, V2's status word
+    reads PA_ERR_DEVICE_TIMEOUT, and the next calls on the same context are
+    exact."""
+    from gpu_helpers import split_x_caches
+    bc = wl.make(wl.scaled(wl.WORKLOADS["long_100k"], seq_len=30000), poison=True)
+    bg = bc.to("cuda")
+    k5, v4 = split_x_caches(bg)
+    P = 512
+    params = pa.make_params(bg.q, k5, bg.block_tables, max_seq_len=bg.max_seq_len,
+                            scale=bg.scale, partition_size=P, out_dtype=torch.float32,
+                            split_x=True)
+    assert pa.decode_kernel(params) == 2 and pa.decode_launches(params) == 1
+    ws = pa.alloc_workspace(params)
+    kw = dict(max_seq_len=bg.max_seq_len, scale=bg.scale, split_x=True)
+    ref = oracle.decode(bc.q, bc.k_cache, bc.v_cache, bc.block_tables, bc.seq_lens, bc.scale)
+    out = torch.zeros(tuple(bg.q.shape), dtype=torch.float32, device="cuda")
+    pa.decode_v2(bg.q, k5, v4, bg.block_tables, bg.seq_lens, out, ws, partition_size=P,
+                 flags=pa.PA_FLAG_SELFTEST_STALL, **kw)
+    torch.cuda.synchronize()
+    assert pa.read_device_status(ws) == pa.PA_ERR_DEVICE_TIMEOUT
+    assert torch.isnan(out).all().item()
+    marker, epoch, started, _, _ = control_words(ws)
+    assert (marker, epoch, started) == (MARKER, 1, 0)
+    pa.decode_v2(bg.q, k5, v4, bg.block_tables, bg.seq_lens, out, ws, partition_size=P, **kw)
+    torch.cuda.synchronize()
+    assert pa.read_device_status(ws) == pa.PA_OK
+    assert float(np.max(np.abs(out.double().cpu().numpy() - ref))) <= 2e-3
+    # V1 on one 8192-token sequence: clusters of CTAs share it
+    bc = wl.make(wl.WORKLOADS["gqa_8k"], poison=True)
+    bg = bc.to("cuda")
+    k5, v4 = split_x_caches(bg)
+    out = torch.zeros(tuple(bg.q.shape), dtype=torch.float32, device="cuda")
+    kw = dict(max_seq_len=bg.max_seq_len, scale=bg.scale, split_x=True)
+    pa.decode_v1(bg.q, k5, v4, bg.block_tables, bg.seq_lens, out,
+                 flags=pa.PA_FLAG_SELFTEST_STALL, **kw)
+    torch.cuda.synchronize()
+    assert torch.isnan(out).all().item()
+    pa.decode_v1(bg.q, k5, v4, bg.block_tables, bg.seq_lens, out, **kw)
+    torch.cuda.synchronize()
+    ref = oracle.decode(bc.q, bc.k_cache, bc.v_cache, bc.block_tables, bc.seq_lens, bc.scale)
+    assert float(np.max(np.abs(out.double().cpu().numpy() - ref))) <= 2e-3
