@@ -71,7 +71,7 @@ NCU_TRAFFIC = {
     # the one-launch V2 kernel (pass 1 and the in-grid reduce)
     ("pa_tc_kernel", "3d7ca941fdab05a2", "long_100k", 512, "v2"): 409_759_744 + 3_002_880,
     # the split-x kernel in one launch (its own pass 1 and the same in-grid reduce)
-    ("pa_sx_kernel", "30358b6f94ffe4b1", "long_100k", 512, "v2"): 409_756_928 + 4_888_320,
+    ("pa_sx_kernel", "eb346a8e51b8c4f0", "long_100k", 512, "v2"): 409_754_624 + 4_745_216,
     ("pa_prefill_kernel", "a751245a46a2df8a", "prefill_32k", 0, "prefill"):
         1_355_374_592 + 193_046_528,
 }
