@@ -769,10 +769,19 @@ def cpu_baseline(batch, nrows, seconds):
         spent += _oracle_rows(bc, rows)
         reps += 1
     per_step_us = spent / reps * 1e6 * total_rows / len(rows)
-    return {"value": round(per_step_us, 1), "unit": UNIT, "cores": oracle.max_threads(),
-            "kind": "oracle",
+    cores = oracle.max_threads()
+    one_core = None  # the same sample once more on one core
+    if cores > 1:
+        oracle.set_threads(1)
+        try:
+            one_core = round(_oracle_rows(bc, rows) * 1e6 * total_rows / len(rows), 1)
+        finally:
+            oracle.set_threads(cores)
+    return {"value": round(per_step_us, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "one_core_value": one_core,
             "sample": f"{len(rows)} of {total_rows} query-head rows of one step, "
-                      f"{reps} repetitions ({spent:.1f} s), scaled to the full step"}
+                      f"{reps} repetitions ({spent:.1f} s) on {cores} cores and one more on "
+                      f"one core, scaled to the full step"}
 
 
 def run_reference(args, rank, world):
