@@ -189,10 +189,9 @@ pa_status_t prepare_v2(const pa_params_t* p, const void* q, const void* k, const
 // itself): the tensor-core kernel serves these parameters as a persistent
 // grid with at least one CTA per reduce unit (pa_internal.h).
 bool one_launch_v2(const pa_params_t* p, int64_t np) {
-  const bool tc = tc_applicable(p);
-  if (!tc && !sx_applicable(p)) return false;
+  if (!tc_applicable(p) && !sx_applicable(p)) return false;
   return one_launch_plan(p->num_seqs, p->num_heads, p->num_kv_heads, p->head_dim, np,
-                         sm100_num_sms(), tc);
+                         sm100_num_sms());
 }
 
 }  // namespace

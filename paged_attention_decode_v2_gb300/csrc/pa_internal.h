@@ -77,13 +77,11 @@ inline int64_t tc_persistent_grid(int64_t items, bool compact, int num_sms) {
 // takes at most one reduce unit (query row x 32 elements of head_dim) per
 // CTA, so its own CTAs run pass 2 in one round after their streaming; other
 // batches use the dependent reduce kernel, which has more CTAs in flight.
-// `compact_list`: the kernel walks a compact work list for batches of 2 to
-// 1024 sequences (the standard-layout kernel; the split-x kernel walks the
-// full space).
+// Both tensor-core kernels (either cache layout) size their grids this way.
 inline bool one_launch_plan(int64_t num_seqs, int64_t num_heads, int64_t num_kv_heads,
-                            int64_t head_dim, int64_t np, int num_sms, bool compact_list) {
+                            int64_t head_dim, int64_t np, int num_sms) {
   const int64_t items = num_seqs * num_kv_heads * np;
-  const bool compact = compact_list && num_seqs > 1 && num_seqs <= 1024;
+  const bool compact = num_seqs > 1 && num_seqs <= 1024;  // the kernels' compact work list
   const int64_t grid = tc_persistent_grid(items, compact, num_sms);
   // a unit holds the statistics of up to 1024 partitions
   return grid > 0 && np <= 1024 && num_seqs * num_heads * (head_dim / 32) <= grid;

@@ -26,12 +26,13 @@
 // one ring of whole blocks (keys and values), so the next item's blocks are
 // in flight while the current one finishes, and loads each item's q rows by
 // bulk copy into one of two q tiles; warps 0-3 consume the ring in chunks of
-// 32 tokens:
-//   QK^T   warp w: S[h, t] for the chunk's 8 tokens 8w .. 8w + 7, over all of
-//          head_dim (A = q, rows 0..7 = the query heads; B = keys);
+// 32 tokens at head_dim 256 (64 at 128, 128 at 64: the same bytes):
+//   QK^T   warp w: S[h, t] for its quarter of the chunk, in n-tiles of 8
+//          tokens, over all of head_dim (A = q, rows 0..7 = the query
+//          heads; B = keys);
 //   softmax the chunk's max per head across the four warps (shared memory),
 //          p = exp2(l - m), the running max / sum / rescale across chunks;
-//   P.V    warp w: head_dim slice w of O[h, d] over the chunk's 32 tokens;
+//   P.V    warp w: head_dim slice w of O[h, d] over the chunk's tokens;
 //          A = P with rows 0..7 its 16-bit hi part and rows 8..15 the
 //          rounded remainder, so one MMA carries ~16 significant bits of p
 //          and O = (rows 0..7) + (rows 8..15) at the end.
@@ -61,7 +62,11 @@ namespace sx {
 
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
-constexpr int kChunk = 32;                           // tokens per chunk
+// Tokens per chunk: 8 per consumer warp and n-tile of QK^T, with more
+// n-tiles per warp for smaller head_dim, so that a chunk carries as many
+// bytes (and amortises its barriers as well) at every head_dim
+template <int D>
+constexpr int chunk_tokens() { return D >= 256 ? 32 : (D == 128 ? 64 : 128); }
 constexpr int kRingBytes = 96 * 1024;                // two CTAs per SM
 constexpr int kMaxStages = 24;
 constexpr long long kWaitBudget = 4000000000LL;      // cycles (about 2 s)
@@ -128,6 +133,7 @@ __device__ __forceinline__ uint32_t pack2(T lo, T hi) {
 }
 
 constexpr int kQRows = 8;  // q tile rows: the query heads of one KV head
+constexpr int kMaxCompactSeqs = 1024;  // V2 batches up to this size walk a compact list
 // A cluster share's partial at the start of the ring (floats): per head m
 // and s, a poison flag, then O [8 heads][head_dim] (unnormalised)
 constexpr int kMergeM = 0, kMergeS = 8, kMergePoison = 16, kMergeO = 32;
@@ -138,6 +144,8 @@ struct Layout {
   static constexpr int kStageBytes = 2 * kBlockBytes;       // keys + values
   static constexpr int kStages =
       kRingBytes / kStageBytes < kMaxStages ? kRingBytes / kStageBytes : kMaxStages;
+  static constexpr int kChunk = chunk_tokens<D>();
+  static constexpr int kNT = kChunk / 32;                    // QK^T n-tiles per warp
   static constexpr int kChunkBlocks = kChunk / BS > 0 ? kChunk / BS : 1;
   static constexpr int kQStride = D + 8;                     // q tile row (elements), padded
   static constexpr int kQTile = kQRows * kQStride;           // elements of one q tile
@@ -155,7 +163,12 @@ struct Layout {
   // for the reduce's broadcasts
   static constexpr int kWsOk = 1 + kMaxStages;
   static constexpr int kRedWord = kWsOk + 1;
-  static constexpr int kSmem = kFlagOff + (kRedWord + 3) * 4 + 64;
+  static constexpr int kScan = kRedWord + 3;       // [kThreads / 32] warp totals
+  static constexpr int kTotalOff = (kFlagOff + (kScan + 8) * 4 + 7) / 8 * 8;  // int64 items
+  // compact work list (V2, 2..kMaxCompactSeqs sequences): prefix[b] =
+  // partitions of the sequences before b
+  static constexpr int kPrefixOff = kTotalOff + 8;
+  static constexpr int kSmem = kPrefixOff + (kMaxCompactSeqs + 1) * 4 + 64;
   // One-launch V2: the reduce's scratch is the ring once streaming is done.
   // (No dry run of the reduce at the start, unlike the standard-layout
   // kernel: here it would hold back the first fill of the ring slots it
@@ -180,15 +193,31 @@ struct Item {
 // Item k of the (partition, sequence, KV head) space, partition-major for V2
 // (ranges past a sequence's end come out empty), (sequence, KV head) for V1.
 // With a cluster of cs CTAs sharing the item, CTA `rank` takes a balanced
-// run of its 32-token chunks.
-template <int BS>
-__device__ __forceinline__ Item item_at(const KernelArgs& a, int64_t k, bool v2, int rank, int cs) {
+// run of its kChunk-token chunks.
+// With a compact work list (`prefix`, V2) k runs over the (sequence,
+// partition, KV head) triples that exist, sequence-major.
+template <int BS, int kChunk>
+__device__ __forceinline__ Item item_at(const KernelArgs& a, const int32_t* prefix, int64_t k,
+                                        bool v2, int rank, int cs) {
   Item it;
-  const int64_t per_part = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads;
-  it.part = v2 ? static_cast<int>(k / per_part) : 0;
-  const int64_t rem = v2 ? k % per_part : k;
-  it.b = static_cast<int>(rem / a.num_kv_heads);
-  it.kvh = static_cast<int>(rem % a.num_kv_heads);
+  if (prefix) {
+    const int64_t j = k / a.num_kv_heads;
+    it.kvh = static_cast<int>(k % a.num_kv_heads);
+    int lo = 0, hi = a.num_seqs;  // largest lo with prefix[lo] <= j
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (prefix[mid] <= j) lo = mid;
+      else hi = mid;
+    }
+    it.b = lo;
+    it.part = static_cast<int>(j - prefix[lo]);
+  } else {
+    const int64_t per_part = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads;
+    it.part = v2 ? static_cast<int>(k / per_part) : 0;
+    const int64_t rem = v2 ? k % per_part : k;
+    it.b = static_cast<int>(rem / a.num_kv_heads);
+    it.kvh = static_cast<int>(rem % a.num_kv_heads);
+  }
   const int32_t L = __ldg(a.seq_lens + it.b);
   it.len_ok = seq_len_ok(a, L);
   it.t0 = v2 ? it.part * a.partition_size : 0;  // a multiple of BS
@@ -209,8 +238,8 @@ __device__ __forceinline__ Item item_at(const KernelArgs& a, int64_t k, bool v2,
 
 template <typename T, int D, int BS, bool kV2>
 __global__ void __launch_bounds__(sx::kThreads, 2)
-    pa_sx_kernel(const KernelArgs a, const __grid_constant__ CUtensorMap pmap, int64_t total_items,
-                 int cs) {
+    pa_sx_kernel(const KernelArgs a, const __grid_constant__ CUtensorMap pmap, int64_t grid_items,
+                 int compact, int cs) {
   using namespace sx;
   using Lay = Layout<D, BS>;
   static_assert(BS == 16 || BS == 32, "block size");
@@ -271,7 +300,52 @@ __global__ void __launch_bounds__(sx::kThreads, 2)
     const int r = (i / D) % kQRows, tile = i / (kQRows * D);
     if (r >= G) qs[tile * Lay::kQTile + r * Lay::kQStride + i % D] = zero;
   }
+  int32_t* const prefix_s = reinterpret_cast<int32_t*>(smem + Lay::kPrefixOff);
+  int64_t* const total_s = reinterpret_cast<int64_t*>(smem + Lay::kTotalOff);
+  if (compact) {
+    // Compact work list: prefix[b] = partitions of the sequences before b.
+    // A sequence whose length is outside 0..max_seq_len contributes none
+    // (the reduce writes its NaN rows).
+    int* const scan = flags + Lay::kScan;
+    int carry = 0;
+    for (int base = 0; base < a.num_seqs; base += kThreads) {
+      const int b = base + tid;
+      int n = 0;
+      if (b < a.num_seqs) {
+        const int32_t L = __ldg(a.seq_lens + b);
+        if (seq_len_ok(a, L))
+          n = (L + a.partition_size - 1) / a.partition_size;
+        else if (blockIdx.x == 0)
+          set_status(a.status, PA_ERR_BAD_SEQ_LEN);
+      }
+      int x = n;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (lane == 31) scan[warp] = x;
+      __syncthreads();
+      int off = 0, round_total = 0;
+#pragma unroll
+      for (int w = 0; w < kThreads / 32; ++w) {
+        off += w < warp ? scan[w] : 0;
+        round_total += scan[w];
+      }
+      if (b < a.num_seqs) prefix_s[b + 1] = carry + off + x;
+      carry += round_total;
+      __syncthreads();
+    }
+    if (tid == 0) {
+      prefix_s[0] = 0;
+      *total_s = static_cast<int64_t>(carry) * a.num_kv_heads;
+    }
+  } else if (tid == 0) {
+    *total_s = grid_items;
+  }
   __syncthreads();
+  const int32_t* const prefix = compact ? prefix_s : nullptr;
+  const int64_t total_items = *total_s;
 
   if (warp == kConsumerWarps) {
     // ========================= producer =======================================
@@ -291,7 +365,7 @@ __global__ void __launch_bounds__(sx::kThreads, 2)
                       // arithmetic short)
     int nq = 0;      // q tiles issued
     for (int64_t k = cid; k < total_items && ok; k += cstride) {
-      const Item it = item_at<BS>(a, k, kV2, rank, cs);
+      const Item it = item_at<BS, Lay::kChunk>(a, prefix, k, kV2, rank, cs);
       if (it.nblk == 0) continue;
       const int qb = nq & 1;
       ok = __all_sync(0xffffffffu, sm100::mbar_wait(&qempty[qb], ((nq >> 1) & 1) ^ 1,
@@ -382,7 +456,7 @@ __global__ void __launch_bounds__(sx::kThreads, 2)
   int nq = 0;                     // q tiles consumed
   int* const red_word = flags + Lay::kRedWord;
   for (int64_t k = cid; k < total_items; k += cstride) {
-    const Item it = item_at<BS>(a, k, kV2, rank, cs);
+    const Item it = item_at<BS, Lay::kChunk>(a, prefix, k, kV2, rank, cs);
     const int64_t row0 = static_cast<int64_t>(it.b) * Hq + static_cast<int64_t>(it.kvh) * G;
     if (it.nblk == 0) {
       if (!it.len_ok && tid == 0 && it.part == 0 && rank == 0)
@@ -428,10 +502,10 @@ __global__ void __launch_bounds__(sx::kThreads, 2)
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[i][e] = 0.f;
     float m_run = -INFINITY, s_run = 0.f;  // for head g (rows g and g + 8)
-    const int nchunks = (it.t1 - it.t0 + kChunk - 1) / kChunk;
+    const int nchunks = (it.t1 - it.t0 + Lay::kChunk - 1) / Lay::kChunk;
     for (int ci = 0; ci < nchunks; ++ci) {
-      const int c0 = it.t0 + ci * kChunk;
-      const int n = min(kChunk, it.t1 - c0);
+      const int c0 = it.t0 + ci * Lay::kChunk;
+      const int n = min(Lay::kChunk, it.t1 - c0);
       const int nb = (n + BS - 1) / BS;
       // every block of the chunk landed
       for (int i = 0; i < nb; ++i) {
@@ -446,30 +520,34 @@ __global__ void __launch_bounds__(sx::kThreads, 2)
         }
         poison |= bad[slot] != 0;
       }
-      // ---- QK^T: this warp's 8 tokens 8w .. 8w + 7 of the chunk --------------------
-      const int tk = warp * 8;  // first token of the n-tile within the chunk
-      const int so = tk % BS;
-      const uint32_t kblk =
-          ring_base + wrap(hs + tk / BS) * Lay::kStageBytes;
-      float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
-      if (tk < n) {
+      // ---- QK^T: this warp's kNT n-tiles of 8 tokens from 8 kNT w ------------------
+      constexpr int kNT = Lay::kNT;
+      const int tk0 = warp * 8 * kNT;  // first token of this warp's n-tiles in the chunk
+      float l[kNT][2];                 // logits of head g, tokens tk + 2t, tk + 2t + 1
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          uint32_t kb[2];
-          const uint32_t qa[4] = {qf[ks][0], 0u, qf[ks][1], 0u};
-          // B: tokens so .. so + 7 of key groups 2 ks and 2 ks + 1 (16 bytes each)
-          ldsm_x2(kb, kblk + (((2 * ks + ((lane >> 3) & 1)) * BS + so + (lane & 7)) * 16));
-          if (ks & 1) mma16816<T>(sd, qa, kb);  // two chains: half the dependent MMAs
-          else mma16816<T>(sc, qa, kb);
+      for (int nt = 0; nt < kNT; ++nt) {
+        const int tk = tk0 + 8 * nt;
+        const int so = tk % BS;
+        const uint32_t kblk = ring_base + wrap(hs + tk / BS) * Lay::kStageBytes;
+        float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
+        if (tk < n) {
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            uint32_t kb[2];
+            const uint32_t qa[4] = {qf[ks][0], 0u, qf[ks][1], 0u};
+            // B: tokens so .. so + 7 of key groups 2 ks and 2 ks + 1 (16 bytes each)
+            ldsm_x2(kb, kblk + (((2 * ks + ((lane >> 3) & 1)) * BS + so + (lane & 7)) * 16));
+            if (ks & 1) mma16816<T>(sd, qa, kb);  // two chains: half the dependent MMAs
+            else mma16816<T>(sc, qa, kb);
+          }
         }
+        // c[0], c[1]: head g, tokens tk + 2t, tk + 2t + 1; c[2], c[3] are padding
+        l[nt][0] = (tk + 2 * t < n && g < G) ? (sc[0] + sd[0]) * sl2 : -INFINITY;
+        l[nt][1] = (tk + 2 * t + 1 < n && g < G) ? (sc[1] + sd[1]) * sl2 : -INFINITY;
       }
-      sc[0] += sd[0];
-      sc[1] += sd[1];
-      // logits of head g, tokens tk + 2t, tk + 2t + 1 (c[0], c[1]); c[2], c[3] are padding
-      float l0 = (tk + 2 * t < n) ? sc[0] * sl2 : -INFINITY;
-      float l1 = (tk + 2 * t + 1 < n) ? sc[1] * sl2 : -INFINITY;
-      if (g >= G) l0 = l1 = -INFINITY;
-      float mx = fmaxf(l0, l1);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int nt = 0; nt < kNT; ++nt) mx = fmaxf(mx, fmaxf(l[nt][0], l[nt][1]));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
       if (t == 0) red_max[warp * 8 + g] = mx;
@@ -478,20 +556,23 @@ __global__ void __launch_bounds__(sx::kThreads, 2)
 #pragma unroll
       for (int w = 1; w < kConsumerWarps; ++w) mc = fmaxf(mc, red_max[w * 8 + g]);
       const float m_new = fmaxf(m_run, mc);
-      const float p0 = l0 == -INFINITY ? 0.f : exp2f(l0 - m_new);
-      const float p1 = l1 == -INFINITY ? 0.f : exp2f(l1 - m_new);
-      float ssum = p0 + p1;
-      ssum += __shfl_xor_sync(0xffffffffu, ssum, 1);
-      ssum += __shfl_xor_sync(0xffffffffu, ssum, 2);
-      if (t == 0) red_sum[warp * 8 + g] = ssum;
-      // P tile: row g = the hi parts, row g + 8 = the remainders, tokens tk + 2t, +1
-      {
+      float ssum = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < kNT; ++nt) {
+        const float p0 = l[nt][0] == -INFINITY ? 0.f : exp2f(l[nt][0] - m_new);
+        const float p1 = l[nt][1] == -INFINITY ? 0.f : exp2f(l[nt][1] - m_new);
+        ssum += p0 + p1;
+        // P tile: row g = the hi parts, row g + 8 = the remainders
+        const int col = tk0 + 8 * nt + 2 * t;
         const T h0 = round16(p0, static_cast<T*>(nullptr)), h1 = round16(p1, static_cast<T*>(nullptr));
         const T r0 = round16(p0 - to_float(h0), static_cast<T*>(nullptr));
         const T r1 = round16(p1 - to_float(h1), static_cast<T*>(nullptr));
-        *reinterpret_cast<uint32_t*>(ps + g * Lay::kPStride + tk + 2 * t) = pack2<T>(h0, h1);
-        *reinterpret_cast<uint32_t*>(ps + (g + 8) * Lay::kPStride + tk + 2 * t) = pack2<T>(r0, r1);
+        *reinterpret_cast<uint32_t*>(ps + g * Lay::kPStride + col) = pack2<T>(h0, h1);
+        *reinterpret_cast<uint32_t*>(ps + (g + 8) * Lay::kPStride + col) = pack2<T>(r0, r1);
       }
+      ssum += __shfl_xor_sync(0xffffffffu, ssum, 1);
+      ssum += __shfl_xor_sync(0xffffffffu, ssum, 2);
+      if (t == 0) red_sum[warp * 8 + g] = ssum;
       // the tail block: value columns past the range are cleared (P is 0 there,
       // but 0 * NaN would be NaN); the slot is refilled by bulk copy later
       if (n < nb * BS) {
@@ -593,7 +674,7 @@ __global__ void __launch_bounds__(sx::kThreads, 2)
   if (cs > 1) {
     sm100::cluster_sync_all();
     if (warp < kConsumerWarps && cid < total_items) {
-      const Item it = item_at<BS>(a, cid, kV2, rank, cs);
+      const Item it = item_at<BS, Lay::kChunk>(a, nullptr, cid, kV2, rank, cs);
       const int64_t row0 = static_cast<int64_t>(it.b) * Hq + static_cast<int64_t>(it.kvh) * G;
       if (it.any) {
         const int ncol = D / cs;
@@ -692,8 +773,11 @@ cudaError_t launch_sx_v(const KernelArgs& a, const CUtensorMap& pm, int64_t item
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
   if (cudaError_t e = configure_sx<T, D, BS, V2>(dev)) return e;
-  // persistent: at most two CTAs per SM, items dealt out in balanced rounds
-  const int64_t persistent = sms > 0 ? tc_persistent_grid(items, false, sms) : 0;
+  // persistent: at most two CTAs per SM (items dealt out in balanced rounds,
+  // or for a compact work list, whose length only the kernel counts, one
+  // CTA per slot)
+  const int compact = (V2 && a.num_seqs > 1 && a.num_seqs <= sx::kMaxCompactSeqs) ? 1 : 0;
+  const int64_t persistent = sms > 0 ? tc_persistent_grid(items, compact != 0, sms) : 0;
   int cs = 1;
   if (persistent == 0 && sms > 0) {
     // Fewer items than SMs: a cluster of cs CTAs (up to 16) shares each item,
@@ -701,9 +785,8 @@ cudaError_t launch_sx_v(const KernelArgs& a, const CUtensorMap& pm, int64_t item
     // distributed shared memory, while every CTA keeps at least 8 chunks
     // (256 tokens), below which the merge costs more than the split saves.
     const int range = V2 ? std::min(a.partition_size, a.max_seq_len) : a.max_seq_len;
-    const int chunks = (range + sx::kChunk - 1) / sx::kChunk;
     int want = 1;
-    while (want < 16 && items * want * 2 <= 2LL * sms && want * 2 * 8 <= chunks) want *= 2;
+    while (want < 16 && items * want * 2 <= 2LL * sms && want * 2 * 256 <= range) want *= 2;
     if (want > 1 && !a.fused) cs = fit_sx_cluster<T, D, BS, V2>(dev, want, items);
   }
   const int64_t grid = persistent > 0 ? persistent : items * cs;
@@ -720,7 +803,8 @@ cudaError_t launch_sx_v(const KernelArgs& a, const CUtensorMap& pm, int64_t item
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = cs > 1 ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, pa_sx_kernel<T, D, BS, V2>, a, pm, items, cs);
+  return cudaLaunchKernelEx(&cfg, pa_sx_kernel<T, D, BS, V2>, a, pm, items,
+                            cs > 1 ? 0 : compact, cs);
 }
 
 template <typename T, int D, int BS>
