@@ -69,11 +69,11 @@ KERNEL_SOURCES = {
 NCU_TRAFFIC = {
     # (kernel, source hash, workload, partition size, path): bytes per launch
     # the one-launch V2 kernel (pass 1 and the in-grid reduce)
-    ("pa_tc_kernel", "3d7ca941fdab05a2", "long_100k", 512, "v2"): 409_759_744 + 3_002_880,
+    ("pa_tc_kernel", "c6cec55e5b4e9c57", "long_100k", 512, "v2"): 409_757_440 + 3_322_880,
     # the split-x kernel in one launch (its own pass 1 and the same in-grid reduce)
-    ("pa_sx_kernel", "eb346a8e51b8c4f0", "long_100k", 512, "v2"): 409_754_624 + 4_745_216,
-    ("pa_prefill_kernel", "a751245a46a2df8a", "prefill_32k", 0, "prefill"):
-        1_355_374_592 + 193_046_528,
+    ("pa_sx_kernel", "b9d31cdbf8604998", "long_100k", 512, "v2"): 409_761_280 + 4_934_400,
+    ("pa_prefill_kernel", "fb27f3351a287baf", "prefill_32k", 0, "prefill"):
+        1_358_718_464 + 194_669_824,
 }
 
 
