@@ -96,12 +96,14 @@ def test_reduce_slice_widths(num_seqs, max_len):
         assert np.all(np.abs(got16 - ref) <= 2e-3 + np.abs(bf16_round(ref)) * 2.0 ** -8)
 
 
+@pytest.mark.parametrize("split_x", [False, True], ids=["standard", "split_x"])
 @pytest.mark.parametrize("num_seqs", [1024, 1025])
-def test_compact_work_list_boundary(num_seqs):
+def test_compact_work_list_boundary(num_seqs, split_x):
     """V2 batches of up to 1024 sequences walk a compact list of the
     partitions that exist; larger ones walk the dense (sequence, KV head,
     partition) space.  Both sides of the boundary, and V1 on the same batch,
-    against the oracle on every row."""
+    against the oracle on every row, on both tensor-core kernels (standard
+    and split-x cache layouts)."""
     w = dataclasses.replace(
         wl.WORKLOADS["mixed_32"], name=f"boundary_{num_seqs}", num_seqs=num_seqs, num_heads=8,
         num_kv_heads=2, head_dim=128, block_size=16, pool_blocks=None,
@@ -111,8 +113,8 @@ def test_compact_work_list_boundary(num_seqs):
     ref = _ref(bc)
     bg = bc.to("cuda")
     for path, P in (("v2", 256), ("v2", 64), ("v1", 256)):
-        assert_close(run(bg, path=path, partition_size=P), ref, TOL[w.dtype],
-                     f"B={num_seqs} {path} P={P}")
+        assert_close(run(bg, path=path, partition_size=P, split_x=split_x), ref, TOL[w.dtype],
+                     f"B={num_seqs} {path} P={P} split_x={split_x}")
 
 
 def test_v1_v2_agree():
