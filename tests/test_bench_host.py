@@ -66,3 +66,23 @@ def test_reference_arm_prints_one_json_line():
     assert d["metric"] == bench.METRIC and d["higher_is_better"] is False
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+
+
+def test_traffic_key_ignores_comments_not_code():
+    """The ncu traffic table is keyed by the kernels' code with comments and
+    layout left out: editing a comment or re-wrapping a line keeps the key,
+    a change of code (or of a string literal, as in inline assembly) does
+    not, and comment markers inside a string literal are code."""
+    src = 'int f(int x) {  // doubles x\n  /* the\n  body */ return 2 * x;\n}\nconst char* s = "a // b";\n'
+    same = 'int f(int x) {\n    /* twice x */\n  return 2 *   x; }  // end\nconst char* s = "a // b";\n'
+    code = src.replace("2 * x", "3 * x")
+    lit = src.replace('"a // b"', '"a // c"')
+    k = bench._code_only
+    assert k(src) == k(same)
+    assert k(src) != k(code)
+    assert k(src) != k(lit)
+    assert "// b" in k(src) and "doubles" not in k(src) and "body" not in k(src)
+    # every listed kernel hashes, and the table's keys name listed kernels
+    for name in bench.KERNEL_SOURCES:
+        assert len(bench.kernel_source_hash(name)) == 16
+    assert all(key[0] in bench.KERNEL_SOURCES for key in bench.NCU_TRAFFIC)
