@@ -277,14 +277,23 @@ def test_concurrent_host_threads():
         assert_close(results[i], refs[i], 2e-3, f"thread {i}")
 
 
-def test_bf16_output():
-    bc = wl.make(wl.scaled(wl.WORKLOADS["gqa_8k"], seq_len=2100), poison=True)
-    ref = _ref(bc)
-    for path in ("v1", "v2"):
-        got = run(bc.to("cuda"), path=path, out_dtype=torch.bfloat16)
-        # float32 result within 2e-3, then one bf16 rounding: half an ulp more
-        ulp_half = np.abs(bf16_round(ref)) * 2.0 ** -8
-        assert np.all(np.abs(got - ref) <= 2e-3 + ulp_half), path
+@pytest.mark.parametrize("split_x", [False, True], ids=["standard", "split_x"])
+def test_bf16_output(split_x):
+    """A bf16 `out` on every way the tensor-core kernels write it: V1 (in
+    clusters for one 2100-token sequence), V2 through the reduce kernel, and
+    the one-launch V2 step (a 30000-token sequence), on both cache
+    layouts."""
+    cases = [(wl.scaled(wl.WORKLOADS["gqa_8k"], seq_len=2100), ("v1", "v2")),
+             (wl.scaled(wl.WORKLOADS["long_100k"], seq_len=30000), ("v2",))]
+    for w, paths in cases:
+        bc = wl.make(w, poison=True)
+        ref = _ref(bc)
+        bg = bc.to("cuda")
+        for path in paths:
+            got = run(bg, path=path, out_dtype=torch.bfloat16, split_x=split_x)
+            # float32 result within 2e-3, then one bf16 rounding: half an ulp more
+            ulp_half = np.abs(bf16_round(ref)) * 2.0 ** -8
+            assert np.all(np.abs(got - ref) <= 2e-3 + ulp_half), (w.name, path, split_x)
 
 
 # ---------------------------------------------------------------------------
